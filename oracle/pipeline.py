@@ -1,0 +1,81 @@
+"""Whole-path composition of the oracle stages for one workload.
+
+TEST INFRASTRUCTURE ONLY (see csa_oracle).  Takes numpy copies of a workload's
+inputs (as produced by the seeded generators) and runs the four stages of the
+DeepSeek-V4 CSA forward (compress -> index -> top-k -> attend; DeepSeek-V4
+Chinese translation, blog.uika.cn, §2.3.1) or the two of HCA (compress ->
+dense attend, §2.3.2) for a chosen subset of query rows.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from . import csa_oracle as O
+
+
+def entries_of(cfg: dict, x: dict, b: int) -> np.ndarray:
+    """Compressed entries of batch row b, float64 [N, d]."""
+    kind = cfg["kind"]
+    if kind == "csa_prefill":
+        return O.compress_csa(x["Ca"][b], x["Cb"][b], x["Za"][b], x["Zb"][b], cfg["m"])
+    if kind == "hca_prefill":
+        return O.compress_hca(x["C"][b], x["Z"][b], cfg["m"])
+    if "entries" in x:
+        return np.asarray(x["entries"][b], dtype=np.float64)
+    return O.decode_mixed_entries(x["ent_nope"][b], x["ent_scale"][b], x["ent_rope"][b])
+
+
+def window_of(x: dict, b: int) -> np.ndarray:
+    if "win" in x:
+        return np.asarray(x["win"][b], dtype=np.float64)
+    return O.decode_mixed_entries(x["win_nope"][b], x["win_scale"][b], x["win_rope"][b])
+
+
+def indexer_inputs(x: dict, b: int, rows):
+    """(qI [len(rows), H, c], K [N, c]) of batch row b, float64."""
+    if "qI" in x:
+        qI = np.asarray(x["qI"][b][rows], dtype=np.float64)
+        K = np.asarray(x["K"][b], dtype=np.float64)
+    else:
+        qI = O.decode_fp4_blocks(x["qI_fp4"][b][rows], x["qI_sf"][b][rows])
+        K = O.decode_fp4_blocks(x["K_fp4"][b], x["K_sf"][b])
+    return qI, K
+
+
+def run_rows(cfg: dict, x: dict, b: int, rows, selected=None, entries=None):
+    """Oracle outputs for query rows ``rows`` of batch row b.
+
+    Returns a dict with 'scores' [len(rows), N] (CSA only), 'selected' (list of
+    index arrays, CSA only) and 'out' [len(rows), n_h, d].  ``selected`` may
+    supply the index sets the attention uses (e.g. a set already checked
+    against the oracle's own top-k rule); ``entries`` may supply precomputed
+    compressed entries.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    m, r, base, n_win = cfg["m"], cfg["r"], cfg["rope_base"], cfg["n_win"]
+    t_pos = cfg["q_pos0"] + rows
+    ent = entries_of(cfg, x, b) if entries is None else entries
+    win = window_of(x, b)
+    q = x["q"][b]
+    res = {}
+    outs = []
+    if cfg["kind"].startswith("csa"):
+        qI, K = indexer_inputs(x, b, rows)
+        w = np.asarray(x["w"][b][rows], dtype=np.float64)
+        scores = O.index_scores(qI, w, K, t_pos, m)
+        res["scores"] = scores
+        if selected is None:
+            selected = [O.topk_select(scores[i], cfg["k"], min(cfg["N"], O.visible_count(int(t), m)))
+                        for i, t in enumerate(t_pos)]
+        res["selected"] = selected
+        for i, t in enumerate(t_pos):
+            outs.append(O.csa_attend_token(np.asarray(q[rows[i]], dtype=np.float64), int(t), ent,
+                                           selected[i], win, cfg["win_base"], x["sink"], m, n_win,
+                                           r, base))
+    else:
+        for i, t in enumerate(t_pos):
+            outs.append(O.hca_attend_token(np.asarray(q[rows[i]], dtype=np.float64), int(t), ent,
+                                           win, cfg["win_base"], x["sink"], m, n_win, r, base))
+    res["out"] = np.stack(outs) if outs else np.zeros((0,))
+    return res
