@@ -1,0 +1,10 @@
+"""B300 (sm_103a) kernels for the DeepSeek-V4 CSA / HCA attention forward.
+
+The stages are C-ABI calls into ``lib/libcsa_b300.so`` (include/csa.h):
+``csa_compress``, ``csa_index``, ``csa_topk``, ``csa_attend``, ``hca_attend``.
+``path`` composes them into the prefill and decode passes of one layer.
+"""
+
+from ._lib import (CsaError, attend_workspace_size, csa_attend, csa_compress,  # noqa: F401
+                   csa_index, csa_topk, device_error, hca_attend, lib)
+from . import path  # noqa: F401

@@ -1,0 +1,196 @@
+"""ctypes binding of libcsa_b300.so (include/csa.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (PyTorch provides device memory and
+the current stream); shapes are read from them and passed as plain ints.
+Loading fails loudly when the library has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libcsa_b300.so")
+
+DT_F32, DT_BF16, DT_E4M3_BF16ROPE, DT_E2M1_BLOCK16 = 0, 1, 2, 3
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or dtype",
+          3: "workspace missing or too small", 4: "CUDA runtime error",
+          5: "device wait timed out", 6: "device-side fault"}
+
+
+class CsaError(RuntimeError):
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+class KV(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("data", ctypes.c_void_p),
+                ("scale", ctypes.c_void_p), ("rope", ctypes.c_void_p)]
+
+
+_lib = None
+
+_I, _P, _F, _Z = ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "csa_compress": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
+    "csa_index": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
+    "csa_topk": [_P, _P, _I, _I, _I, _I, _I, _I, _P],
+    "csa_attend": [_P, KV, _P, KV, _P, _P] + [_I] * 12 + [_F, _P, _Z, _P],
+    "hca_attend": [_P, KV, KV, _P, _P] + [_I] * 11 + [_F, _P, _Z, _P],
+    "csa_attend_workspace_size": [_I] * 14,
+    "csa_device_error": [_P],
+    "csa_status_string": [_I],
+    "csa_last_cuda_error": [],
+    "csa_version": [],
+}
+_RESTYPES = {"csa_attend_workspace_size": _Z, "csa_status_string": ctypes.c_char_p,
+             "csa_last_cuda_error": ctypes.c_char_p}
+
+
+def lib():
+    """The loaded library (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m compressed_sparse_long_05_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = _RESTYPES.get(name, ctypes.c_int)
+        _lib = L
+    return _lib
+
+
+def _check(fn, status):
+    if status != 0:
+        detail = lib().csa_last_cuda_error().decode() if status == 4 else ""
+        raise CsaError(fn, status, detail)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dt(t):
+    if t.dtype == torch.float32:
+        return DT_F32
+    if t.dtype == torch.bfloat16:
+        return DT_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _kv(rows):
+    """A row set: a float32/bf16 tensor [B, rows, d] or (e4m3 bytes, scale, bf16 rope)."""
+    if isinstance(rows, (tuple, list)):
+        nope, scale, rope = rows
+        return KV(DT_E4M3_BF16ROPE, nope.data_ptr(), scale.data_ptr(), rope.data_ptr())
+    return KV(_dt(rows), rows.data_ptr(), None, None)
+
+
+def _rows_shape(rows):
+    if isinstance(rows, (tuple, list)):
+        nope, _, rope = rows
+        return nope.shape[0], nope.shape[1], nope.shape[2] + rope.shape[2]
+    return rows.shape[0], rows.shape[1], rows.shape[2]
+
+
+# ----------------------------------------------------------------------------
+
+
+def csa_compress(Ca, Za, m, Cb=None, Zb=None, Ba=None, Bb=None, out=None):
+    """Compressed entries [B, T//m, d] (Cb = Zb = None: HCA, no overlap)."""
+    B, T, d = Ca.shape
+    if out is None:
+        out = torch.empty((B, T // m, d), dtype=Ca.dtype, device=Ca.device)
+    _check("csa_compress", lib().csa_compress(_p(Ca), _p(Cb), _p(Za), _p(Zb), _p(Ba), _p(Bb),
+                                              _p(out), B, T, d, m, _dt(Ca), _stream()))
+    return out
+
+
+def csa_index(qI, w, K, m, q_pos0, qI_sf=None, K_sf=None, scores=None):
+    """Indexer scores [B, Tq, N] float32 (-inf where not visible)."""
+    fp4 = qI.dtype == torch.uint8
+    B, Tq, H = qI.shape[:3]
+    c = qI.shape[3] * (2 if fp4 else 1)
+    N = K.shape[1]
+    dt = DT_E2M1_BLOCK16 if fp4 else _dt(qI)
+    if scores is None:
+        scores = torch.empty((B, Tq, N), dtype=torch.float32, device=qI.device)
+    _check("csa_index", lib().csa_index(_p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(scores),
+                                        B, Tq, N, H, c, m, q_pos0, dt, _stream()))
+    return scores
+
+
+def csa_topk(scores, k, m, q_pos0, idx=None):
+    """Selected entry indices [B, Tq, k] int32, ascending, -1 padded."""
+    B, Tq, N = scores.shape
+    if idx is None:
+        idx = torch.empty((B, Tq, k), dtype=torch.int32, device=scores.device)
+    _check("csa_topk", lib().csa_topk(_p(scores), _p(idx), B, Tq, N, k, m, q_pos0, _stream()))
+    return idx
+
+
+def attend_workspace_size(q, entries, win, k, m, n_win, q_pos0, r, is_hca):
+    B, Tq, n_h, d = q.shape
+    _, N, _ = _rows_shape(entries)
+    _, T_win, _ = _rows_shape(win)
+    kv_dt = _kv(entries).dtype
+    return lib().csa_attend_workspace_size(B, Tq, N, k, T_win, n_h, d, r, m, n_win, q_pos0,
+                                           _dt(q), kv_dt, 1 if is_hca else 0)
+
+
+def _workspace(ws, nbytes, device):
+    if nbytes == 0:
+        return ws
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws
+
+
+def csa_attend(q, entries, idx, win, sink, m, n_win, win_base, q_pos0, r, rope_base=10000.0,
+               out=None, ws=None):
+    """Sparse shared-KV attention output [B, Tq, n_h, d] (dtype of q)."""
+    B, Tq, n_h, d = q.shape
+    _, N, _ = _rows_shape(entries)
+    _, T_win, _ = _rows_shape(win)
+    k = idx.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = attend_workspace_size(q, entries, win, k, m, n_win, q_pos0, r, False)
+    ws = _workspace(ws, nbytes, q.device)
+    _check("csa_attend", lib().csa_attend(
+        _p(q), _kv(entries), _p(idx), _kv(win), _p(sink), _p(out), B, Tq, N, k, T_win, win_base,
+        n_h, d, r, m, n_win, q_pos0, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
+    return out
+
+
+def hca_attend(q, entries, win, sink, m, n_win, win_base, q_pos0, r, rope_base=10000.0,
+               out=None, ws=None):
+    """Dense (HCA) shared-KV attention output [B, Tq, n_h, d] (dtype of q)."""
+    B, Tq, n_h, d = q.shape
+    _, N, _ = _rows_shape(entries)
+    _, T_win, _ = _rows_shape(win)
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = attend_workspace_size(q, entries, win, 0, m, n_win, q_pos0, r, True)
+    ws = _workspace(ws, nbytes, q.device)
+    _check("hca_attend", lib().hca_attend(
+        _p(q), _kv(entries), _kv(win), _p(sink), _p(out), B, Tq, N, T_win, win_base, n_h, d, r,
+        m, n_win, q_pos0, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
+    return out
+
+
+def device_error():
+    """Reads and clears the library's sticky device error word; raises if it was set."""
+    _check("csa_device_error", lib().csa_device_error(_stream()))

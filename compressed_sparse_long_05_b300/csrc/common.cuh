@@ -1,0 +1,84 @@
+// Shared device helpers for the CSA / HCA kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#define CSA_DEVINL __device__ __forceinline__
+
+// Sticky device error word (one per device, in this library's module).
+// Bit values: see the ERRBIT_* constants.
+__device__ unsigned int g_csa_error_word;
+
+enum : unsigned int {
+  ERRBIT_TIMEOUT = 1u,      // a bounded mbarrier wait gave up
+  ERRBIT_BAD_INDEX = 2u,    // an index list held an entry >= N
+  ERRBIT_TMEM = 4u          // tensor-memory allocation returned an unusable address
+};
+
+CSA_DEVINL void csa_flag_error(unsigned int bit) { atomicOr(&g_csa_error_word, bit); }
+
+// ----------------------------------------------------------------------------
+// numeric helpers
+// ----------------------------------------------------------------------------
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static CSA_DEVINL float to_f(float x) { return x; }
+  static CSA_DEVINL float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static CSA_DEVINL float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static CSA_DEVINL __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+// 8 bf16 <-> 8 float, through one 16-byte vector.
+CSA_DEVINL void bf16x8_to_f(const uint4& v, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+CSA_DEVINL uint4 f_to_bf16x8(const float* f) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+CSA_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ----------------------------------------------------------------------------
+// RoPE angle from a fixed-point phase.
+// The host stores, per frequency j, F_j = round(theta_j / (2*pi) * 2^64) as a
+// uint64.  For an integer position p the rotation phase in revolutions is
+// p * F_j / 2^64 modulo 1, which unsigned 64-bit multiplication gives exactly
+// (wrap-around is the modulo).  The top bits, read as a signed fraction in
+// [-1/2, 1/2), feed sincospif, so the angle stays accurate to ~2^-24
+// revolutions at any position up to 2^40.
+// ----------------------------------------------------------------------------
+struct RopeFreqs {
+  unsigned long long F[64];  // one per rotated pair; r/2 <= 64
+  int half;                  // r / 2
+};
+
+CSA_DEVINL void rope_cos_sin(long long pos, unsigned long long F, float& c, float& s) {
+  unsigned long long ph = (unsigned long long)pos * F;
+  float rev = (float)((long long)ph >> 40) * 5.9604644775390625e-8f;  // * 2^-24
+  sincospif(2.0f * rev, &s, &c);
+}
+
+// ----------------------------------------------------------------------------
+// ordered keys for float radix selection: unsigned order == float order
+// ----------------------------------------------------------------------------
+CSA_DEVINL uint32_t float_to_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}

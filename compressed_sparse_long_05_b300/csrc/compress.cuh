@@ -1,0 +1,124 @@
+// Softmax-weighted block compression (CSA overlapped, HCA non-overlapped).
+//
+// DeepSeek-V4 report (Chinese translation, blog.uika.cn) §2.3.1 compression
+// equations and §2.3.2: entry i, channel c is sum_j S[j,c] * C[j,c] with
+// S = softmax over the entry's rows of (Z + bias).  CSA rows: a-rows of block
+// i and b-rows of block i-1 (none for i = 0); HCA rows: the block's m rows.
+//
+// HBM streaming reduction: one CTA per compressed entry.  Thread (v, g) owns
+// one 16-byte channel vector v and visits rows g, g+G, ... with an online
+// softmax (running max, running sum, running weighted sum per channel); the G
+// row groups merge through shared memory at the end.  Every input byte is read
+// once with 16-byte coalesced loads.
+#pragma once
+#include "common.cuh"
+
+namespace csa {
+
+template <typename T>
+struct VecTraits;
+template <> struct VecTraits<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static CSA_DEVINL void load(const __nv_bfloat16* p, float* f) {
+    bf16x8_to_f(__ldg(reinterpret_cast<const uint4*>(p)), f);
+  }
+  static CSA_DEVINL void store(__nv_bfloat16* p, const float* f) {
+    *reinterpret_cast<uint4*>(p) = f_to_bf16x8(f);
+  }
+};
+template <> struct VecTraits<float> {
+  static constexpr int N = 4;
+  static CSA_DEVINL void load(const float* p, float* f) {
+    float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
+  static CSA_DEVINL void store(float* p, const float* f) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+
+struct CompressArgs {
+  const void* Ca; const void* Cb; const void* Za; const void* Zb;
+  const float* Ba; const float* Bb;
+  void* out;
+  int B, T, d, m, N;
+  int overlap;      // 1 = CSA (b-rows of the previous block join), 0 = HCA
+  int vecs;         // d / VEC
+  int groups;       // row groups G (blockDim.x = vecs * groups)
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
+  using V = VecTraits<T>;
+  constexpr int VEC = V::N;
+  const int i = blockIdx.x;            // entry
+  const int b = blockIdx.y;            // batch row
+  const int v = threadIdx.x % a.vecs;  // channel vector
+  const int g = threadIdx.x / a.vecs;  // row group
+  const int c0 = v * VEC;
+
+  const size_t seq = (size_t)b * a.T * a.d;
+  const T* Ca = reinterpret_cast<const T*>(a.Ca) + seq;
+  const T* Za = reinterpret_cast<const T*>(a.Za) + seq;
+  const T* Cb = a.overlap ? reinterpret_cast<const T*>(a.Cb) + seq : nullptr;
+  const T* Zb = a.overlap ? reinterpret_cast<const T*>(a.Zb) + seq : nullptr;
+
+  float mx[VEC], sum[VEC], acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) { mx[e] = -INFINITY; sum[e] = 0.f; acc[e] = 0.f; }
+
+  // rows 0..m-1: a-rows of block i; rows m..2m-1: b-rows of block i-1
+  const int nrows = (a.overlap && i > 0) ? 2 * a.m : a.m;
+  for (int j = g; j < nrows; j += a.groups) {
+    const bool is_a = j < a.m;
+    const int jj = is_a ? j : j - a.m;
+    const size_t tok = is_a ? (size_t)a.m * i + jj : (size_t)a.m * (i - 1) + jj;
+    float z[VEC], cv[VEC];
+    V::load((is_a ? Za : Zb) + tok * a.d + c0, z);
+    V::load((is_a ? Ca : Cb) + tok * a.d + c0, cv);
+    const float* bias = is_a ? a.Ba : a.Bb;
+    if (bias) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) z[e] += __ldg(bias + (size_t)jj * a.d + c0 + e);
+    }
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      float nm = fmaxf(mx[e], z[e]);
+      float sc = __expf(mx[e] - nm);       // 0 on the first row (mx = -inf)
+      float p = __expf(z[e] - nm);
+      sum[e] = sum[e] * sc + p;
+      acc[e] = acc[e] * sc + p * cv[e];
+      mx[e] = nm;
+    }
+  }
+
+  // merge the row groups: group 0 of each vector gathers the others
+  extern __shared__ float sm[];                  // [groups][vecs][3*VEC]
+  float* mine = sm + ((size_t)g * a.vecs + v) * 3 * VEC;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) {
+    mine[e] = mx[e]; mine[VEC + e] = sum[e]; mine[2 * VEC + e] = acc[e];
+  }
+  __syncthreads();
+  if (g != 0) return;
+  for (int gg = 1; gg < a.groups; ++gg) {
+    const float* o = sm + ((size_t)gg * a.vecs + v) * 3 * VEC;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      float om = o[e];
+      if (om == -INFINITY) continue;             // group saw no rows
+      float nm = fmaxf(mx[e], om);
+      float s0 = __expf(mx[e] - nm), s1 = __expf(om - nm);
+      sum[e] = sum[e] * s0 + o[VEC + e] * s1;
+      acc[e] = acc[e] * s0 + o[2 * VEC + e] * s1;
+      mx[e] = nm;
+    }
+  }
+  float res[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) res[e] = acc[e] / sum[e];
+  T* out = reinterpret_cast<T*>(a.out) + ((size_t)b * a.N + i) * a.d + c0;
+  V::store(out, res);
+}
+
+}  // namespace csa

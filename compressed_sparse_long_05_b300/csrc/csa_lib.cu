@@ -1,0 +1,269 @@
+// C ABI of the CSA / HCA forward kernels (declared in include/csa.h).
+//
+// One translation unit: the kernels live in the included .cuh files so that
+// they share the device error word without relocatable device code.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/csa.h"
+#include "common.cuh"
+#include "compress.cuh"
+#include "topk.cuh"
+#include "simt_f32.cuh"
+
+namespace {
+
+thread_local char g_cuda_msg[256] = "";
+
+csa_status_t cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_cuda_msg, sizeof(g_cuda_msg), "%s: %s", where, cudaGetErrorString(e));
+  return CSA_ERR_CUDA;
+}
+
+#define CSA_CHECK_LAUNCH(where)                          \
+  do {                                                   \
+    cudaError_t e_ = cudaGetLastError();                 \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where);  \
+  } while (0)
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+RopeFreqs make_rope(int r, float base) {
+  RopeFreqs rf;
+  memset(&rf, 0, sizeof(rf));
+  rf.half = r / 2;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int j = 0; j < r / 2; ++j) {
+    const double theta = std::pow((double)base, -2.0 * j / (double)r);
+    const double frac = theta / two_pi;                 // revolutions per position, < 1
+    rf.F[j] = (unsigned long long)std::ldexp(frac, 64);
+  }
+  return rf;
+}
+
+int visible(long long t, int m, int N) {
+  long long v = (t + 1) / m;
+  if (v < 0) v = 0;
+  return (int)(v < N ? v : N);
+}
+
+}  // namespace
+
+extern "C" {
+
+int csa_version(void) { return 1; }
+
+const char* csa_last_cuda_error(void) { return g_cuda_msg; }
+
+const char* csa_status_string(csa_status_t s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case CSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA_ERR_CUDA: return "CUDA runtime error";
+    case CSA_ERR_TIMEOUT: return "device wait timed out";
+    case CSA_ERR_DEVICE: return "device-side fault";
+  }
+  return "unknown status";
+}
+
+csa_status_t csa_device_error(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(S(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "csa_device_error sync");
+  unsigned int word = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&word, g_csa_error_word, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "csa_device_error read");
+  e = cudaMemcpyToSymbol(g_csa_error_word, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "csa_device_error clear");
+  if (word & ERRBIT_TIMEOUT) return CSA_ERR_TIMEOUT;
+  if (word) return CSA_ERR_DEVICE;
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------------------
+csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const void* Zb,
+                          const float* Ba, const float* Bb, void* out, int B, int T, int d,
+                          int m, int dtype, void* stream) {
+  const int overlap = (Cb != nullptr) ? 1 : 0;
+  if ((Cb == nullptr) != (Zb == nullptr)) return CSA_ERR_INVALID_ARG;
+  if (B < 0 || T < 0 || d <= 0 || m <= 0 || m > 4096) return CSA_ERR_INVALID_ARG;
+  if (dtype != CSA_DT_F32 && dtype != CSA_DT_BF16) return CSA_ERR_UNSUPPORTED;
+  const int vec = dtype == CSA_DT_BF16 ? 8 : 4;
+  if (d % vec || d / vec > 256) return CSA_ERR_UNSUPPORTED;
+  if (B == 0 || T / m == 0) return CSA_OK;   // nothing to compress (outputs may be empty)
+  if (!Ca || !Za || !out) return CSA_ERR_INVALID_ARG;
+  const void* ptrs[] = {Ca, Cb, Za, Zb, out};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return CSA_ERR_INVALID_ARG;
+  if ((Ba && !aligned(Ba, 4)) || (Bb && !aligned(Bb, 4))) return CSA_ERR_INVALID_ARG;
+  const int N = T / m;
+  if (B == 0 || N == 0) return CSA_OK;
+  csa::CompressArgs a;
+  a.Ca = Ca; a.Cb = Cb; a.Za = Za; a.Zb = Zb; a.Ba = Ba; a.Bb = Bb; a.out = out;
+  a.B = B; a.T = T; a.d = d; a.m = m; a.N = N; a.overlap = overlap;
+  a.vecs = d / vec;
+  int rows = overlap ? 2 * m : m;
+  int groups = 256 / a.vecs;
+  if (groups > rows) groups = rows;
+  if (groups < 1) groups = 1;
+  a.groups = groups;
+  dim3 grid(N, B);
+  dim3 block(a.vecs * groups);
+  size_t smem = (size_t)groups * a.vecs * 3 * vec * sizeof(float);
+  if (dtype == CSA_DT_BF16)
+    csa::compress_kernel<__nv_bfloat16><<<grid, block, smem, S(stream)>>>(a);
+  else
+    csa::compress_kernel<float><<<grid, block, smem, S(stream)>>>(a);
+  CSA_CHECK_LAUNCH("csa_compress");
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------------------
+csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
+                       const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
+                       int m, int q_pos0, int dtype, void* stream) {
+  if (B < 0 || Tq < 0 || N < 0 || H <= 0 || c <= 0 || m <= 0 || q_pos0 < 0)
+    return CSA_ERR_INVALID_ARG;
+  if (B == 0 || Tq == 0 || N == 0) return CSA_OK;
+  if (!qI || !w || !K || !scores) return CSA_ERR_INVALID_ARG;
+  if (dtype == CSA_DT_F32) {
+    if (c > 256) return CSA_ERR_UNSUPPORTED;
+    csa::IndexF32Args a{reinterpret_cast<const float*>(qI), w, reinterpret_cast<const float*>(K),
+                        scores, Tq, N, H, c, m, q_pos0};
+    dim3 grid((N + 7) / 8, B * Tq);
+    csa::index_f32_kernel<<<grid, 256, 0, S(stream)>>>(a);
+    CSA_CHECK_LAUNCH("csa_index f32");
+    return CSA_OK;
+  }
+  (void)qI_sf; (void)K_sf;
+  return CSA_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------------------
+csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, int k, int m,
+                      int q_pos0, void* stream) {
+  if (B < 0 || Tq < 0 || N < 0 || k < 1 || k > 4096 || m <= 0 || q_pos0 < 0)
+    return CSA_ERR_INVALID_ARG;
+  if (B == 0 || Tq == 0) return CSA_OK;
+  if (!idx || (N > 0 && !scores)) return CSA_ERR_INVALID_ARG;
+  if (!aligned(scores, 4) || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
+  const int rows = B * Tq;
+  // cluster size: spread long rows of small batches over up to 16 SMs
+  int CL = 1;
+  if (N > 8192 && rows < 64) CL = rows <= 9 ? 16 : 8;
+  int slice = (N + CL - 1) / CL;
+  slice = (slice + 3) & ~3;
+  const size_t smem = (size_t)slice * sizeof(uint32_t);
+  if (smem > 200 * 1024) return CSA_ERR_UNSUPPORTED;
+  csa::TopkArgs a{scores, idx, Tq, N, k, m, q_pos0, slice};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows * CL);
+  cfg.blockDim = dim3(csa::TOPK_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = S(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  switch (CL) {
+    case 1:
+      e = cudaFuncSetAttribute(csa::topk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_fail(e, "csa_topk attr");
+      e = cudaLaunchKernelEx(&cfg, csa::topk_kernel<1>, a);
+      break;
+    case 8:
+      e = cudaFuncSetAttribute(csa::topk_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_fail(e, "csa_topk attr");
+      e = cudaLaunchKernelEx(&cfg, csa::topk_kernel<8>, a);
+      break;
+    default:
+      e = cudaFuncSetAttribute(csa::topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_fail(e, "csa_topk attr");
+      e = cudaFuncSetAttribute(csa::topk_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return cuda_fail(e, "csa_topk attr");
+      e = cudaLaunchKernelEx(&cfg, csa::topk_kernel<16>, a);
+      break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "csa_topk launch");
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------------------
+static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* idx, csa_kv_t win,
+                                  const float* sink, void* out, int B, int Tq, int N, int k,
+                                  int T_win, int win_base, int n_h, int d, int r, int m, int n_win,
+                                  int q_pos0, float rope_base, void* ws, size_t ws_bytes,
+                                  void* stream, int dense) {
+  if (B < 0 || Tq < 0 || N < 0 || T_win < 0 || n_h <= 0 || d <= 0 || r < 0 || r > d || (r & 1) ||
+      r > 128 || m <= 0 || n_win <= 0 || q_pos0 < 0 || win_base < 0 || !(rope_base > 0.f))
+    return CSA_ERR_INVALID_ARG;
+  if (!dense && (k < 1 || k > 4096)) return CSA_ERR_INVALID_ARG;
+  if (N > 0 && !ent.data) return CSA_ERR_INVALID_ARG;
+  if (B == 0 || Tq == 0) return CSA_OK;
+  if (!q || !sink || !out || !win.data) return CSA_ERR_INVALID_ARG;
+  if (!dense && !idx) return CSA_ERR_INVALID_ARG;
+  // every window position of every query row must lie in the window buffer
+  const long long t_first = q_pos0, t_last = (long long)q_pos0 + Tq - 1;
+  const long long w_lo = t_first - n_win + 1 < 0 ? 0 : t_first - n_win + 1;
+  if (w_lo < win_base || t_last >= (long long)win_base + T_win) return CSA_ERR_INVALID_ARG;
+  (void)ws; (void)ws_bytes;
+  const RopeFreqs rf = make_rope(r, rope_base);
+  // q dtype is implied by the kv dtype for the tensor-core path; float32 here
+  if (ent.dtype == CSA_DT_F32 && win.dtype == CSA_DT_F32) {
+    if (d > 512 || (size_t)n_h * d > 16384) return CSA_ERR_UNSUPPORTED;
+    csa::AttendF32Args a;
+    a.q = reinterpret_cast<const float*>(q);
+    a.ent = reinterpret_cast<const float*>(ent.data);
+    a.idx = dense ? nullptr : idx;
+    a.win = reinterpret_cast<const float*>(win.data);
+    a.sink = sink;
+    a.out = reinterpret_cast<float*>(out);
+    a.Tq = Tq; a.N = N; a.k = dense ? 0 : k; a.T_win = T_win; a.win_base = win_base;
+    a.n_h = n_h; a.d = d; a.r = r; a.m = m; a.n_win = n_win; a.q_pos0 = q_pos0;
+    a.dense = dense;
+    a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+    a.rf = rf;
+    const size_t smem = ((size_t)2 * n_h * d + d + 5 * n_h) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(csa::attend_f32_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_attend f32 attr");
+    csa::attend_f32_kernel<<<B * Tq, csa::ATT_F32_THREADS, smem, S(stream)>>>(a);
+    CSA_CHECK_LAUNCH("csa_attend f32");
+    return CSA_OK;
+  }
+  return CSA_ERR_UNSUPPORTED;
+}
+
+csa_status_t csa_attend(const void* q, csa_kv_t entries, const int32_t* idx, csa_kv_t win,
+                        const float* sink, void* out, int B, int Tq, int N, int k, int T_win,
+                        int win_base, int n_h, int d, int r, int m, int n_win, int q_pos0,
+                        float rope_base, void* ws, size_t ws_bytes, void* stream) {
+  return attend_common(q, entries, idx, win, sink, out, B, Tq, N, k, T_win, win_base, n_h, d, r,
+                       m, n_win, q_pos0, rope_base, ws, ws_bytes, stream, 0);
+}
+
+csa_status_t hca_attend(const void* q, csa_kv_t entries, csa_kv_t win, const float* sink,
+                        void* out, int B, int Tq, int N, int T_win, int win_base, int n_h, int d,
+                        int r, int m, int n_win, int q_pos0, float rope_base, void* ws,
+                        size_t ws_bytes, void* stream) {
+  return attend_common(q, entries, nullptr, win, sink, out, B, Tq, N, 0, T_win, win_base, n_h, d,
+                       r, m, n_win, q_pos0, rope_base, ws, ws_bytes, stream, 1);
+}
+
+size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h, int d, int r,
+                                 int m, int n_win, int q_pos0, int q_dtype, int kv_dtype,
+                                 int is_hca) {
+  (void)B; (void)Tq; (void)N; (void)k; (void)T_win; (void)n_h; (void)d; (void)r; (void)m;
+  (void)n_win; (void)q_pos0; (void)q_dtype; (void)kv_dtype; (void)is_hca;
+  return 0;
+}
+
+}  // extern "C"

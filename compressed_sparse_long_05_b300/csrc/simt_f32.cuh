@@ -1,0 +1,178 @@
+// float32 CUDA-core kernels for the lightning indexer and the core attention.
+//
+// These serve float32 workloads (and shapes too small for tensor-core tiles,
+// e.g. 4 query heads of dim 128).  They follow the same definitions as the
+// tensor-core kernels: DeepSeek-V4 report (Chinese translation,
+// blog.uika.cn) §2.3.1 indexer score and shared-KV MQA, §2.3.3 partial RoPE
+// with inverse rotation of the output, sliding window and attention sink.
+#pragma once
+#include "common.cuh"
+
+namespace csa {
+
+// ----------------------------------------------------------------------------
+// indexer: one warp per (row, entry s); lanes split the H*c products
+// ----------------------------------------------------------------------------
+struct IndexF32Args {
+  const float* q; const float* w; const float* K; float* scores;
+  int Tq, N, H, c, m, q_pos0;
+};
+
+__global__ void __launch_bounds__(256) index_f32_kernel(IndexF32Args a) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int row = blockIdx.y;                      // b * Tq + i
+  if (gw >= a.N) return;
+  const int s = (int)gw;
+  const int b = row / a.Tq, i = row % a.Tq;
+  const long long t = (long long)a.q_pos0 + i;
+  float* out = a.scores + (size_t)row * a.N + s;
+  if ((long long)(s + 1) * a.m > t + 1) {          // not visible
+    if (lane == 0) *out = -INFINITY;
+    return;
+  }
+  const float* qr = a.q + (size_t)row * a.H * a.c;
+  const float* kr = a.K + ((size_t)b * a.N + s) * a.c;
+  const float* wr = a.w + (size_t)row * a.H;
+  float acc = 0.f;
+  for (int h = 0; h < a.H; ++h) {
+    float dot = 0.f;
+    for (int j = lane; j < a.c; j += 32) dot = fmaf(qr[(size_t)h * a.c + j], kr[j], dot);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    acc = fmaf(wr[h], fmaxf(dot, 0.f), acc);
+  }
+  if (lane == 0) *out = acc;
+}
+
+// ----------------------------------------------------------------------------
+// attention: one CTA per query row; online softmax over the row set
+// (selected compressed entries, then the window), float32 throughout.
+// ----------------------------------------------------------------------------
+struct AttendF32Args {
+  const float* q; const float* ent; const int32_t* idx; const float* win; const float* sink;
+  float* out;
+  int Tq, N, k, T_win, win_base, n_h, d, r, m, n_win, q_pos0;
+  int dense;        // 1 = HCA: every visible entry, idx unused
+  float inv_sqrt_d;
+  RopeFreqs rf;
+};
+
+constexpr int ATT_F32_THREADS = 256;
+
+__global__ void __launch_bounds__(ATT_F32_THREADS) attend_f32_kernel(AttendF32Args a) {
+  extern __shared__ float sm[];
+  const int row = blockIdx.x;                    // b * Tq + i
+  const int b = row / a.Tq, i = row % a.Tq;
+  const long long t = (long long)a.q_pos0 + i;
+  const int nh = a.n_h, d = a.d, r = a.r;
+  float* qs = sm;                                // [n_h][d] rotated queries
+  float* acc = qs + (size_t)nh * d;              // [n_h][d]
+  float* er = acc + (size_t)nh * d;              // [d] current rotated row
+  float* lg = er + d;                            // [n_h] logits of the current row
+  float* mrun = lg + nh;                         // [n_h] running max
+  float* lrun = mrun + nh;                       // [n_h] running denominator
+  float* scl = lrun + nh;                        // [n_h] rescale of acc for this row
+  float* pw = scl + nh;                          // [n_h] weight of this row
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, wid = tid >> 5, nw = ATT_F32_THREADS / 32;
+
+  const float* qg = a.q + (size_t)row * nh * d;
+  for (int x = tid; x < nh * d; x += ATT_F32_THREADS) {
+    qs[x] = qg[x];
+    acc[x] = 0.f;
+  }
+  for (int h = tid; h < nh; h += ATT_F32_THREADS) { mrun[h] = -INFINITY; lrun[h] = 0.f; }
+  __syncthreads();
+  // rotate the query's RoPE dims at position t
+  for (int x = tid; x < nh * (r / 2); x += ATT_F32_THREADS) {
+    const int h = x / (r / 2), j = x % (r / 2);
+    float c, s;
+    rope_cos_sin(t, a.rf.F[j], c, s);
+    float* p = qs + (size_t)h * d + (d - r) + 2 * j;
+    float x0 = p[0], x1 = p[1];
+    p[0] = x0 * c - x1 * s;
+    p[1] = x0 * s + x1 * c;
+  }
+  __syncthreads();
+
+  // row list: [0, nsel) compressed entries, then the window tokens
+  int nsel;
+  const int32_t* irow = a.idx ? a.idx + (size_t)row * a.k : nullptr;
+  int vis = (int)min((long long)a.N, (t + 1) / a.m);
+  if (vis < 0) vis = 0;
+  nsel = a.dense ? vis : a.k;
+  const long long w0 = max(0LL, t - a.n_win + 1);
+  const int nwin = (int)(t - w0 + 1);
+  for (int jr = 0; jr < nsel + nwin; ++jr) {
+    const float* src;
+    long long pos;
+    if (jr < nsel) {
+      int s = a.dense ? jr : irow[jr];
+      if (s < 0) continue;                       // uniform across the block
+      if (s >= a.N) { if (tid == 0) csa_flag_error(ERRBIT_BAD_INDEX); continue; }
+      src = a.ent + ((size_t)b * a.N + s) * d;
+      pos = (long long)a.m * (s + 1) - 1;
+    } else {
+      const long long tok = w0 + (jr - nsel);
+      src = a.win + ((size_t)b * a.T_win + (size_t)(tok - a.win_base)) * d;
+      pos = tok;
+    }
+    for (int x = tid; x < d; x += ATT_F32_THREADS) er[x] = src[x];
+    __syncthreads();
+    for (int j = tid; j < r / 2; j += ATT_F32_THREADS) {
+      float c, s;
+      rope_cos_sin(pos, a.rf.F[j], c, s);
+      float* p = er + (d - r) + 2 * j;
+      float x0 = p[0], x1 = p[1];
+      p[0] = x0 * c - x1 * s;
+      p[1] = x0 * s + x1 * c;
+    }
+    __syncthreads();
+    for (int h = wid; h < nh; h += nw) {
+      float dot = 0.f;
+      for (int x = lane; x < d; x += 32) dot = fmaf(qs[(size_t)h * d + x], er[x], dot);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      if (lane == 0) {
+        const float l = dot * a.inv_sqrt_d;
+        const float nm = fmaxf(mrun[h], l);
+        const float sc = expf(mrun[h] - nm);
+        const float p = expf(l - nm);
+        lrun[h] = lrun[h] * sc + p;
+        mrun[h] = nm;
+        scl[h] = sc;
+        pw[h] = p;
+      }
+    }
+    __syncthreads();
+    for (int x = tid; x < nh * d; x += ATT_F32_THREADS) {
+      const int h = x / d;
+      acc[x] = acc[x] * scl[h] + pw[h] * er[x % d];
+    }
+    __syncthreads();
+  }
+  // sink joins the denominator, then normalise and rotate back by -t
+  for (int x = tid; x < nh * d; x += ATT_F32_THREADS) {
+    const int h = x / d;
+    const float z = a.sink[h];
+    const float M = fmaxf(mrun[h], z);
+    const float den = lrun[h] * expf(mrun[h] - M) + expf(z - M);
+    acc[x] = acc[x] * expf(mrun[h] - M) / den;
+  }
+  __syncthreads();
+  for (int x = tid; x < nh * (r / 2); x += ATT_F32_THREADS) {
+    const int h = x / (r / 2), j = x % (r / 2);
+    float c, s;
+    rope_cos_sin(-t, a.rf.F[j], c, s);
+    float* p = acc + (size_t)h * d + (d - r) + 2 * j;
+    float x0 = p[0], x1 = p[1];
+    p[0] = x0 * c - x1 * s;
+    p[1] = x0 * s + x1 * c;
+  }
+  __syncthreads();
+  float* og = a.out + (size_t)row * nh * d;
+  for (int x = tid; x < nh * d; x += ATT_F32_THREADS) og[x] = acc[x];
+}
+
+}  // namespace csa

@@ -1,0 +1,162 @@
+/*
+ * csa.h — C ABI of the B300 (sm_103a) kernels for the DeepSeek-V4 Compressed
+ * Sparse Attention (CSA) and Heavily Compressed Attention (HCA) forward path.
+ *
+ * The operator is defined only mathematically by the pages this library
+ * follows: the DeepSeek-V4 technical report in Chinese translation
+ * (blog.uika.cn) §2.3.1 "Compressed Sparse Attention", §2.3.2 "Heavily
+ * Compressed Attention", §2.3.3 (RMS-normalised q / entries, partial RoPE with
+ * the output rotated back, sliding window, attention sink) and §2.3.4 (FP8 /
+ * BF16 KV storage, FP4 indexer QK), and the paper notes at
+ * awesome.papernotes.org ("关键设计 1" / "关键设计 2" equations).
+ *
+ * Conventions shared by every call:
+ *   - Every pointer is caller-owned DEVICE memory of the current CUDA device,
+ *     except where a comment says otherwise.  The library never allocates,
+ *     frees or synchronises in these calls; work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *   - Tensors are dense and row-major in the shapes given (last dim fastest).
+ *   - Argument, shape and alignment errors are returned before any launch.
+ *     CSA_ERR_CUDA means a launch or runtime call failed (cudaGetLastError
+ *     text via csa_last_cuda_error()).  Faults found on the device (a bounded
+ *     wait that gave up, an out-of-range index) set a sticky device error word
+ *     that csa_device_error() reads.
+ *   - Query row i of a call sits at absolute token position q_pos0 + i, the
+ *     same for every batch row.  Compressed entry s is visible to the query
+ *     at position t iff (s+1)*m <= t+1, and its RoPE position is m*(s+1)-1.
+ *     T mod m tail tokens are not compressed (§3.6.1: they wait in a buffer).
+ */
+#ifndef CSA_B300_H
+#define CSA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size or misaligned pointer */
+  CSA_ERR_UNSUPPORTED = 2,  /* valid arguments this build has no kernel for */
+  CSA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  CSA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  CSA_ERR_TIMEOUT = 5,      /* device error word: a bounded wait gave up */
+  CSA_ERR_DEVICE = 6        /* device error word: other device-side fault */
+} csa_status_t;
+
+/* Element formats. */
+typedef enum {
+  CSA_DT_F32 = 0,            /* float32 */
+  CSA_DT_BF16 = 1,           /* bfloat16 */
+  CSA_DT_E4M3_BF16ROPE = 2,  /* KV rows: first d-r dims e4m3fn bytes times one float32
+                                scale per row, last r (RoPE) dims bfloat16 (§2.3.4) */
+  CSA_DT_E2M1_BLOCK16 = 3    /* indexer q/K: e2m1 codes two per byte (element 2j in the
+                                low nibble of byte j) times one e4m3fn scale byte per
+                                16 consecutive elements (§3.4 FP4 indexer QK path) */
+} csa_dtype_t;
+
+/* A set of key=value rows (compressed entries or raw window tokens).
+ *   dtype F32 / BF16 : data = [B, rows, d]; scale, rope unused.
+ *   dtype E4M3_BF16ROPE : data = e4m3 [B, rows, d-r], scale = float32 [B, rows],
+ *                         rope = bf16 [B, rows, r]. */
+typedef struct {
+  int32_t dtype;
+  const void* data;
+  const float* scale;
+  const void* rope;
+} csa_kv_t;
+
+/* ---------------------------------------------------------------------------
+ * csa_compress — softmax-weighted block compression of per-token entries.
+ * CSA (§2.3.1 compression equations): entry i, channel c = sum over the a-rows
+ * of block i and the b-rows of block i-1 of softmax_rows(Z + B)[j,c] * C[j,c];
+ * entry 0 has no previous block (its softmax runs over the m a-rows alone).
+ * HCA (§2.3.2): pass Cb = Zb = NULL; entry i uses the m rows of block i only.
+ *   Ca, Za (and Cb, Zb): [B, T, d] in `dtype` (F32 or BF16).
+ *   Ba, Bb: optional learnable position biases [m, d] float32 (NULL = zero).
+ *   out: [B, floor(T/m), d] in `dtype`.
+ *   Requires d % 8 == 0 (BF16) or d % 4 == 0 (F32), d <= 2048, 1 <= m <= 4096,
+ *   16-byte aligned tensors.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const void* Zb,
+                          const float* Ba, const float* Bb, void* out, int B, int T, int d,
+                          int m, int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_index — lightning-indexer scores (§2.3.1 "Lightning Indexer"):
+ *   scores[b,i,s] = sum_h w[b,i,h] * ReLU(qI[b,i,h,:] . K[b,s,:])  if visible,
+ *                   -inf                                           otherwise.
+ *   dtype F32 / BF16: qI [B, Tq, H, c], K [B, N, c]; qI_sf, K_sf unused (NULL).
+ *   dtype E2M1_BLOCK16: qI [B, Tq, H, c/2] bytes, qI_sf [B, Tq, H, c/16] bytes,
+ *                       K [B, N, c/2] bytes, K_sf [B, N, c/16] bytes.
+ *   w: [B, Tq, H] float32.  scores: [B, Tq, N] float32 (every element written).
+ *   BF16 / E2M1 need H in {16,32,64,128}, c in {64,128}; F32 any H, c <= 256.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
+                       const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
+                       int m, int q_pos0, int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_topk — per query row, the k visible entries with the largest scores
+ * (§2.3.1 "top-k selector"; C_t = TopK_k(I_t,:)).  Ties are broken toward the
+ * lower entry index.  idx[b,i,:] holds the min(k, vis) selected entry indices
+ * in ascending order, then -1 up to k.
+ *   scores: [B, Tq, N] float32 (only s < vis(t) is read); idx: [B, Tq, k] int32.
+ *   Requires 1 <= k <= 4096.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, int k, int m,
+                      int q_pos0, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_attend — shared-KV multi-query core attention (§2.3.1 "Shared KV MQA",
+ * §2.3.3).  For query row i at position t and head h:
+ *   rows J = {compressed entries idx[b,i,:] >= 0} U {raw tokens max(0,t-n_win+1)..t}
+ *   every row is both key and value; the last r dims of q and of each row are
+ *   rotated by RoPE (interleaved pairs, theta_j = rope_base^(-2j/r)) at their
+ *   positions (t; m*(s+1)-1 for entry s; the token position for window rows);
+ *   logits = q.row / sqrt(d); p = exp(logit) / (sum exp(logits) + exp(sink[h]));
+ *   o = sum p * rotated row; out = o with its last r dims rotated by -t.
+ *   q: [B, Tq, n_h, d] (F32 or BF16); out: same shape and dtype as q.
+ *   entries: [B, N, d] rows (F32, BF16 or E4M3_BF16ROPE).
+ *   win: [B, T_win, d] rows; row j holds raw token win_base + j and must cover
+ *        every window position of every query row.
+ *   idx: [B, Tq, k] int32 from csa_topk (-1 entries are skipped).
+ *   sink: [n_h] float32.
+ *   ws / ws_bytes: scratch of at least csa_attend_workspace_size(...) bytes,
+ *   256-byte aligned (may be NULL when that size is 0).
+ *   BF16 / E4M3 need d == 512, r == 64, n_h % 64 == 0; F32 needs d <= 512,
+ *   n_h * d <= 16384.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_attend(const void* q, csa_kv_t entries, const int32_t* idx, csa_kv_t win,
+                        const float* sink, void* out, int B, int Tq, int N, int k, int T_win,
+                        int win_base, int n_h, int d, int r, int m, int n_win, int q_pos0,
+                        float rope_base, void* ws, size_t ws_bytes, void* stream);
+
+/* hca_attend — csa_attend over every visible compressed entry (block size m = m'),
+ * with no index list (§2.3.2: HCA keeps shared-KV MQA but has no top-k). */
+csa_status_t hca_attend(const void* q, csa_kv_t entries, csa_kv_t win, const float* sink,
+                        void* out, int B, int Tq, int N, int T_win, int win_base, int n_h, int d,
+                        int r, int m, int n_win, int q_pos0, float rope_base, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* Scratch bytes csa_attend / hca_attend need for these sizes (k = 0 for HCA).
+ * q_dtype / kv_dtype as in the calls. */
+size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h, int d, int r,
+                                 int m, int n_win, int q_pos0, int q_dtype, int kv_dtype,
+                                 int is_hca);
+
+/* Reads and clears the sticky device error word (synchronises `stream`).
+ * Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE. */
+csa_status_t csa_device_error(void* stream);
+
+const char* csa_status_string(csa_status_t status);
+const char* csa_last_cuda_error(void);  /* text of the last CSA_ERR_CUDA (host memory) */
+int csa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_B300_H */

@@ -1,0 +1,72 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol that
+include/csa.h declares, and rejects bad arguments on the host (no GPU needed:
+these calls return before touching CUDA)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from compressed_sparse_long_05_b300 import build as B
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    from compressed_sparse_long_05_b300 import _lib
+    return _lib.lib()
+
+
+def declared(root):
+    txt = open(os.path.join(root, "include", "csa.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    names = re.findall(r"^\s*(?:csa_status_t|size_t|int|const char\*)\s+(\w+)\s*\(", txt, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L, root):
+    names = declared(root)
+    assert "csa_attend" in names and "csa_topk" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    assert L.csa_status_string(0) == b"ok"
+    assert L.csa_status_string(2) == b"unsupported shape or dtype"
+    assert L.csa_version() >= 1
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_host_side_argument_errors(L):
+    from compressed_sparse_long_05_b300._lib import KV
+    fake = _p(0x10000)      # never dereferenced: every call below fails validation first
+    mis = _p(0x10002)
+    # null output / input
+    assert L.csa_compress(None, None, None, None, None, None, None, 1, 8, 64, 4, 1, None) == 1
+    # half an overlap pair
+    assert L.csa_compress(fake, fake, fake, None, None, None, fake, 1, 8, 64, 4, 1, None) == 1
+    # misaligned pointer
+    assert L.csa_compress(mis, None, fake, None, None, None, fake, 1, 8, 64, 4, 1, None) == 1
+    # unsupported dtype / width
+    assert L.csa_compress(fake, None, fake, None, None, None, fake, 1, 8, 64, 4, 3, None) == 2
+    assert L.csa_compress(fake, None, fake, None, None, None, fake, 1, 8, 60, 4, 1, None) == 2
+    # top-k: k out of range, negative sizes
+    assert L.csa_topk(fake, fake, 1, 1, 100, 0, 4, 0, None) == 1
+    assert L.csa_topk(fake, fake, 1, 1, 100, 5000, 4, 0, None) == 1
+    assert L.csa_topk(fake, fake, -1, 1, 100, 5, 4, 0, None) == 1
+    # index: null scores
+    assert L.csa_index(fake, None, fake, fake, None, None, 1, 1, 8, 4, 32, 4, 0, 0, None) == 1
+    # attend: window buffer does not cover the query's window
+    kv = KV(1, 0x10000, None, None)
+    assert L.csa_attend(fake, kv, fake, kv, fake, fake, 1, 1, 8, 4, 16, 0, 128, 512, 64, 4, 128,
+                        1000, 10000.0, None, 0, None) == 1
+    # attend: odd rope dims
+    assert L.csa_attend(fake, kv, fake, kv, fake, fake, 1, 1, 8, 4, 128, 0, 128, 512, 63, 4, 128,
+                        127, 10000.0, None, 0, None) == 1
+    # empty batch is a no-op
+    assert L.csa_topk(fake, fake, 0, 1, 100, 5, 4, 0, None) == 0
