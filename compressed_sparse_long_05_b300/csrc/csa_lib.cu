@@ -11,6 +11,9 @@
 #include "compress.cuh"
 #include "topk.cuh"
 #include "simt_f32.cuh"
+#include "index_tc.cuh"
+
+#include <cudaTypedefs.h>
 
 namespace {
 
@@ -44,10 +47,79 @@ RopeFreqs make_rope(int r, float base) {
   return rf;
 }
 
-int visible(long long t, int m, int N) {
-  long long v = (t + 1) / m;
-  if (v < 0) v = 0;
-  return (int)(v < N ? v : N);
+int sm_count() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor map (x fastest), 128-byte swizzle, zero fill out of bounds.
+bool tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, uint64_t z,
+                  uint64_t y_stride_bytes, uint64_t z_stride_bytes, uint32_t box_x, uint32_t box_y) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {x, y, z};
+  cuuint64_t strides[2] = {y_stride_bytes, z_stride_bytes};
+  cuuint32_t box[3] = {box_x, box_y, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int H, int C>
+csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, float* scores, int B,
+                             int Tq, int N, int m, int q_pos0, cudaStream_t stream) {
+  csa::IndexTcArgs a;
+  a.w = w; a.scores = scores; a.B = B; a.Tq = Tq; a.N = N; a.m = m; a.q_pos0 = q_pos0;
+  a.QT = 256 / H;
+  if (a.QT > Tq) a.QT = Tq;
+  a.G = (Tq + a.QT - 1) / a.QT;
+  a.tiles_max = (N + csa::IDX_TILE - 1) / csa::IDX_TILE;
+  const int sms = sm_count();
+  if ((long long)B * a.G >= sms) {
+    a.chunk_tiles = a.tiles_max;
+  } else {
+    long long total = (long long)B * a.G * a.tiles_max;
+    a.chunk_tiles = (int)((total + sms - 1) / sms);
+    if (a.chunk_tiles < 1) a.chunk_tiles = 1;
+  }
+  a.chunks = (a.tiles_max + a.chunk_tiles - 1) / a.chunk_tiles;
+  long long items = (long long)B * a.G * a.chunks;
+  if (items > 0x7fffffff) return CSA_ERR_UNSUPPORTED;
+  a.items = (int)items;
+  const int nqh = a.QT * H;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * nqh)) cols <<= 1;
+  a.tmem_cols = cols;
+  CUtensorMap tmK, tmq;
+  if (!tmap_bf16_3d(&tmK, K, C, N, B, (uint64_t)C * 2, (uint64_t)N * C * 2, 64, csa::IDX_TILE) ||
+      !tmap_bf16_3d(&tmq, qI, C, (uint64_t)Tq * H, B, (uint64_t)C * 2, (uint64_t)Tq * H * C * 2,
+                    64, nqh))
+    return CSA_ERR_UNSUPPORTED;
+  const int smem = csa::IndexSmem<H, C>::BYTES;
+  auto kern = csa::index_tc_kernel<H, C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_index tc attr");
+  const int grid = a.items < sms ? a.items : sms;
+  kern<<<grid, csa::IDX_THREADS, smem, stream>>>(tmK, tmq, a);
+  CSA_CHECK_LAUNCH("csa_index tc");
+  return CSA_OK;
 }
 
 }  // namespace
@@ -138,6 +210,19 @@ csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const 
     csa::index_f32_kernel<<<grid, 256, 0, S(stream)>>>(a);
     CSA_CHECK_LAUNCH("csa_index f32");
     return CSA_OK;
+  }
+  if (dtype == CSA_DT_BF16) {
+    if (!aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4) || !aligned(scores, 4))
+      return CSA_ERR_INVALID_ARG;
+    if (H == 64 && c == 128)
+      return launch_index_tc<64, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
+    if (H == 64 && c == 64)
+      return launch_index_tc<64, 64>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
+    if (H == 32 && c == 128)
+      return launch_index_tc<32, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
+    if (H == 128 && c == 128)
+      return launch_index_tc<128, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
+    return CSA_ERR_UNSUPPORTED;
   }
   (void)qI_sf; (void)K_sf;
   return CSA_ERR_UNSUPPORTED;

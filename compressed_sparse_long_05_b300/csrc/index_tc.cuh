@@ -1,0 +1,254 @@
+// Lightning-indexer scores on the tcgen05 tensor cores.
+//
+// DeepSeek-V4 report (Chinese translation, blog.uika.cn) §2.3.1 "Lightning
+// Indexer": I[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . K[s,:]); paper notes
+// (awesome.papernotes.org) 关键设计 1.  Entry s is visible to query t iff
+// (s+1)*m <= t+1; invisible scores are -inf.
+//
+// Tile: D[128 entries x (QT queries * H heads)] = K_tile[128 x c] * q_group^T,
+// one tcgen05.mma chain (M=128, N=QT*H <= 256, K=c in steps of 16), bf16
+// operands staged by TMA in 128-byte-swizzled K-major tiles, fp32 accumulators
+// double-buffered in tensor memory.  The epilogue reads each entry's row of
+// the accumulator (one TMEM lane per entry) and folds the H heads with
+// ReLU * w into QT scores per entry: the head reduction never leaves
+// registers, and each warp stores 32 consecutive scores per query.
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
+// issuer, warps 2-5 epilogue (one TMEM lane quarter each).
+//
+// Work items are (batch row b, query group g, chunk of entry tiles), dealt
+// round-robin to persistent CTAs.  Tiles past the last entry any query of the
+// group can see take no MMA: the epilogue writes -inf there directly.
+#pragma once
+#include "tc.cuh"
+
+namespace csa {
+
+constexpr int IDX_THREADS = 192;
+constexpr int IDX_STAGES = 4;
+constexpr int IDX_TILE = 128;   // entries per tile (MMA M)
+
+struct IndexTcArgs {
+  const float* w;        // [B, Tq, H]
+  float* scores;         // [B, Tq, N]
+  int B, Tq, N, m, q_pos0;
+  int QT;                // queries per group (QT * H <= 256)
+  int G;                 // query groups per batch row
+  int tiles_max;         // ceil(N / 128)
+  int chunk_tiles;       // entry tiles per work item
+  int chunks;            // work items per group
+  int items;             // B * G * chunks
+  uint32_t tmem_cols;    // allocated TMEM columns (power of 2 >= 2 * QT * H)
+};
+
+template <int H, int C>
+struct IndexSmem {
+  static constexpr int A_BYTES = IDX_TILE * C * 2;       // one K tile
+  static constexpr int B_BYTES_MAX = 256 * C * 2;        // one q group (QT*H <= 256 rows)
+  static constexpr int KCH = C / 64;                     // 64-element swizzle chunks along c
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + IDX_STAGES * A_BYTES;
+  static constexpr int OFF_W = OFF_B + B_BYTES_MAX;      // float w_s[4 warps][2][256]
+  static constexpr int OFF_BAR = OFF_W + 4 * 2 * 256 * 4;
+  static constexpr int BYTES = OFF_BAR + 256 + 1024;     // + alignment slack
+};
+
+CSA_DEVINL int vis_of(long long t, int m, int N) {
+  long long v = (t + 1) / m;
+  if (v < 0) v = 0;
+  return (int)(v < N ? v : N);
+}
+
+struct IdxItem {
+  int b, g, t0, nq, j0, j1, jv;   // tiles [j0, j1) of the chunk; MMA for j < jv
+};
+
+CSA_DEVINL IdxItem idx_item(const IndexTcArgs& a, int it) {
+  IdxItem x;
+  x.b = it / (a.G * a.chunks);
+  const int rem = it % (a.G * a.chunks);
+  x.g = rem / a.chunks;
+  const int c = rem % a.chunks;
+  x.t0 = x.g * a.QT;
+  x.nq = min(a.QT, a.Tq - x.t0);
+  const int vis_last = vis_of((long long)a.q_pos0 + x.t0 + x.nq - 1, a.m, a.N);
+  const int tiles_vis = (vis_last + IDX_TILE - 1) / IDX_TILE;
+  x.j0 = c * a.chunk_tiles;
+  x.j1 = min(a.tiles_max, x.j0 + a.chunk_tiles);
+  x.jv = max(x.j0, min(x.j1, tiles_vis));
+  return x;
+}
+
+template <int H, int C>
+__global__ void __launch_bounds__(IDX_THREADS, 1)
+index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant__ CUtensorMap tm_q,
+                IndexTcArgs a) {
+  using L = IndexSmem<H, C>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + L::OFF_A;
+  uint8_t* sB = smem + L::OFF_B;
+  float* w_s = reinterpret_cast<float*>(smem + L::OFF_W);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* full = bars;                         // [STAGES]
+  uint64_t* empty = bars + IDX_STAGES;           // [STAGES]
+  uint64_t* acc_full = bars + 2 * IDX_STAGES;    // [2]
+  uint64_t* acc_empty = acc_full + 2;            // [2]
+  uint64_t* b_full = acc_empty + 2;
+  uint64_t* b_free = b_full + 1;
+  uint64_t* mma_done = b_free + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NQH = a.QT * H;                      // MMA N
+  const uint32_t B_BYTES = (uint32_t)NQH * C * 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < IDX_STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(acc_full + s, 1); mbar_init(acc_empty + s, 4); }
+    mbar_init(b_full, 1);
+    mbar_init(b_free, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, a.tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) { prefetch_tmap(&tm_K); prefetch_tmap(&tm_q); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t ia = 0, nitem = 0;
+      bool ok = true, b_issued = false;
+      for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+        const IdxItem x = idx_item(a, it);
+        if (x.jv <= x.j0) continue;
+        const int ntl = x.jv - x.j0;
+        auto load_a = [&](int j) -> bool {
+          const uint32_t st = ia % IDX_STAGES, ph = (ia / IDX_STAGES) & 1;
+          if (!mbar_wait(empty + st, ph ^ 1, abort_flag)) return false;
+          mbar_arrive_expect_tx(full + st, L::A_BYTES);
+#pragma unroll
+          for (int kc = 0; kc < L::KCH; ++kc)
+            tma_load_3d(sA + st * L::A_BYTES + kc * (IDX_TILE * 128), &tm_K, full + st, kc * 64,
+                        j * IDX_TILE, x.b);
+          ++ia;
+          return true;
+        };
+        // prefetch the first tiles of this item, then swap in its query group
+        const int pre = min(ntl, IDX_STAGES);
+        for (int jj = 0; jj < pre && ok; ++jj) ok = load_a(x.j0 + jj);
+        if (!ok) break;
+        if (nitem > 0 && !mbar_wait(b_free, (nitem - 1) & 1, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(b_full, B_BYTES);
+        for (int kc = 0; kc < L::KCH; ++kc)
+          tma_load_3d(sB + kc * (NQH * 128), &tm_q, b_full, kc * 64, x.t0 * H, x.b);
+        b_issued = true;
+        ++nitem;
+        for (int jj = pre; jj < ntl && ok; ++jj) ok = load_a(x.j0 + jj);
+      }
+      // drain copies still in flight before the CTA may exit
+      for (uint32_t k = (ia > IDX_STAGES ? ia - IDX_STAGES : 0); k < ia; ++k)
+        mbar_drain(full + (k % IDX_STAGES), (k / IDX_STAGES) & 1);
+      if (b_issued) mbar_drain(b_full, (nitem - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t ia = 0, iacc = 0, nitem = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_bf16(IDX_TILE, NQH);
+      for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+        const IdxItem x = idx_item(a, it);
+        if (x.jv <= x.j0) continue;
+        if (!mbar_wait(b_full, nitem & 1, abort_flag)) { ok = false; break; }
+        for (int j = x.j0; j < x.jv; ++j) {
+          const uint32_t st = ia % IDX_STAGES, ph = (ia / IDX_STAGES) & 1;
+          const uint32_t buf = iacc & 1, aph = (iacc >> 1) & 1;
+          if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(full + st, ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t aBase = smem_u32(sA + st * L::A_BYTES);
+          const uint32_t bBase = smem_u32(sB);
+          const uint32_t d = tmem + buf * (uint32_t)NQH;
+#pragma unroll
+          for (int kk = 0; kk < C / 16; ++kk) {
+            const uint32_t kc = kk / 4, ko = (kk % 4) * 32;
+            const uint64_t ad = sdesc_sw128(aBase + kc * (IDX_TILE * 128) + ko, 16, 1024);
+            const uint64_t bd = sdesc_sw128(bBase + kc * (NQH * 128) + ko, 16, 1024);
+            umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(empty + st);
+          umma_commit(acc_full + buf);
+          ++ia;
+          ++iacc;
+        }
+        umma_commit(b_free);
+        ++nitem;
+      }
+      umma_commit(mma_done);
+      mbar_drain(mma_done, 0);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q4 = warp & 3;                       // TMEM lane quarter of this warp
+    uint32_t iacc = 0, nitem = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+      const IdxItem x = idx_item(a, it);
+      // this warp's own copy of the group's head weights (no cross-warp barrier,
+      // so a warp that stops on a timed-out wait cannot strand the others)
+      float* ws = w_s + ((q4 * 2) + (nitem & 1)) * 256;
+      for (int e = lane; e < x.nq * H; e += 32)
+        ws[e] = __ldg(a.w + ((size_t)x.b * a.Tq + x.t0) * H + e);
+      __syncwarp();
+      ++nitem;
+      for (int j = x.j0; j < x.j1; ++j) {
+        const int s = j * IDX_TILE + q4 * 32 + lane;
+        float* srow = a.scores + ((size_t)x.b * a.Tq + x.t0) * a.N + s;
+        if (j < x.jv) {
+          const uint32_t buf = iacc & 1, aph = (iacc >> 1) & 1;
+          if (!mbar_wait(acc_full + buf, aph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
+          for (int qi = 0; qi < x.nq; ++qi) {
+            float acc = 0.f;
+#pragma unroll
+            for (int h0 = 0; h0 < H; h0 += 32) {
+              uint32_t r[32];
+              tmem_ld32(tbase + qi * H + h0, r);
+              tmem_ld_wait();
+              const float* wq = ws + qi * H + h0;
+#pragma unroll
+              for (int h = 0; h < 32; ++h) acc = fmaf(wq[h], fmaxf(__uint_as_float(r[h]), 0.f), acc);
+            }
+            const int vis = vis_of((long long)a.q_pos0 + x.t0 + qi, a.m, a.N);
+            if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty + buf);
+          ++iacc;
+        } else {
+          for (int qi = 0; qi < x.nq; ++qi)
+            if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+}  // namespace csa

@@ -170,3 +170,31 @@ def test_hca_attend_f32(K):
         for t in (0, 1, 126, 127, 128, 300, 699):
             ref = O.hca_attend_token(q64[t], t, e64, w64, 0, f64(sink), m, n_win, r, 1e4)
             assert_close(f64(out[b, t]), ref, TOL_F32, TOL_F32, f"b={b} t={t}")
+
+
+# ----------------------------------------------------------------------------
+# index (bf16, tcgen05 path)
+# ----------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("B,Tq,N,H,c,q_pos0", [
+    (2, 1, 5000, 64, 128, 19999),      # decode rows, ragged last tile
+    (1, 1030, 257, 64, 128, 0),        # causal prefill, ragged query groups
+    (1, 9, 300, 64, 128, 700),         # mid-sequence query block
+    (3, 5, 1000, 64, 64, 3990),        # c = 64
+    (1, 33, 700, 32, 128, 2700),       # H = 32
+    (1, 6, 640, 128, 128, 2540),       # H = 128
+])
+def test_index_bf16(K, B, Tq, N, H, c, q_pos0):
+    m = 4
+    qI = _randn((B, Tq, H, c), torch.bfloat16, 41, scale=c ** -0.5)
+    Kt = _randn((B, N, c), torch.bfloat16, 42, scale=c ** -0.5)
+    w = torch.rand((B, Tq, H), generator=_gen(43), device=DEV) / H
+    s = K.csa_index(qI, w, Kt, m, q_pos0)
+    torch.cuda.synchronize()
+    K.device_error()
+    for b in range(B):
+        ref = O.index_scores(f64(qI[b]), f64(w[b]), f64(Kt[b]), q_pos0 + np.arange(Tq), m)
+        got = f64(s[b])
+        for i in range(Tq):
+            assert_scores_close(got[i], ref[i], f"b={b} row {i}")
