@@ -1,0 +1,697 @@
+// Shared-KV multi-query core attention on the tcgen05 tensor cores
+// (d = 512, RoPE on the last 64 dims, bf16 rows and queries).
+//
+// DeepSeek-V4 report (Chinese translation, blog.uika.cn) §2.3.1 "Shared KV
+// MQA" (each selected compressed entry is both key and value, all query heads
+// share it), §2.3.2 (HCA: every visible compressed entry), §2.3.3 (partial
+// RoPE with the output rotated back at -t, 128-token sliding window, per-head
+// attention sink in the softmax denominator).
+//
+// One CTA handles one work item = (query row, group of 64 heads, chunk of the
+// row set).  The row set of query t is its selected compressed entries (or,
+// for HCA, every visible one) followed by the raw window tokens; rows are
+// gathered 128 at a time into shared memory as a 128-byte-swizzled tile E
+// [128 rows x 512 dims].  The same bytes are the K-major A operand of
+//     S^T[128 rows x 64 heads]  = E * Q^T            (tcgen05, M=128, N=64, K=512)
+// and the MN-major A operand of
+//     O^T[512 dims x 64 heads] += E^T * P^T          (4 MMAs of M=128, N=64, K=128)
+// so one tile feeds both products without a transpose.  O^T (4 x 64 columns)
+// and two S^T buffers (2 x 64) live in tensor memory.
+//
+// Softmax runs over rows (TMEM lanes) per head (column): each warp reduces its
+// 32 rows with a reduce-scatter butterfly (lane l ends with heads 2l, 2l+1),
+// warps combine through shared memory behind mbarriers.  The running max is
+// raised lazily (only when a tile's max exceeds it by 8 in log2 units), so O^T
+// is rescaled in tensor memory only on those rare tiles.  P^T is written as
+// bf16 and the row sums use the same rounded values.
+//
+// Warp roles (288 threads): warps 0-3 softmax / epilogue (one TMEM lane
+// quarter each), warps 4-7 gather (cp.async, 32 rows each, plus the RoPE of
+// the query and, unless the rows come pre-rotated, of the gathered rows),
+// warp 8 TMEM owner + MMA issuer.  Gathering chunk c of tile n+1 waits only
+// for the PV block that read it in tile n, so loads overlap the tail of PV.
+//
+// A single-chunk item finishes in the kernel: divide by the softmax
+// denominator plus exp(sink), rotate the RoPE dims back by -t, store bf16.
+// A multi-chunk item (decode: few query rows, many rows each) stores its
+// unnormalised O^T, running max and denominator for attend_combine_kernel.
+#pragma once
+#include <cuda_fp8.h>
+#include "tc.cuh"
+
+namespace csa {
+
+constexpr int ATT_THREADS = 288;
+constexpr int ATT_D = 512;
+constexpr int ATT_R = 64;
+constexpr int ATT_HG = 64;          // heads per CTA
+constexpr int ATT_TILE = 128;       // rows per tile
+constexpr int ATT_LAG = 3;          // cp.async chunk groups in flight per gather warp
+constexpr float ATT_TAU = 8.0f;     // lazy-rescale threshold (log2 units)
+
+struct AttendTcArgs {
+  const __nv_bfloat16* q;        // [B, Tq, n_h, 512]
+  const void* ent;               // [B, N, 512] bf16 (or e4m3 nope, see kv_mixed)
+  const float* ent_scale;        // [B, N] (kv_mixed)
+  const __nv_bfloat16* ent_rope; // [B, N, 64] (kv_mixed)
+  const void* win;               // [B, T_win, 512] bf16 (or e4m3 nope)
+  const float* win_scale;
+  const __nv_bfloat16* win_rope;
+  const int32_t* idx;            // [B, Tq, k] or null (dense)
+  const float* sink;             // [n_h]
+  __nv_bfloat16* out;            // [B, Tq, n_h, 512]
+  float* part_o;                 // [items][64][512] (split mode)
+  float* part_ml;                // [items][64][2]   (split mode)
+  int B, Tq, N, k, T_win, win_base, n_h, m, n_win, q_pos0;
+  int HG;                        // head groups = n_h / 64
+  int nch;                       // chunks per (query row, head group)
+  int chunk_rows;                // rows per chunk (multiple of 128)
+  int items;                     // B * Tq * HG * nch
+  int rotate_rows;               // 1 = rotate gathered rows in shared memory
+  int kv_mixed;                  // 1 = e4m3 + scale + bf16 rope rows
+  float scale_log2;              // log2(e) / sqrt(d)
+  RopeFreqs rf;
+};
+
+struct AttSmem {
+  static constexpr int E = 0;                              // 8 chunks x 16 KB
+  static constexpr int Q = E + 8 * 16384;                  // 8 chunks x 8 KB
+  static constexpr int P = Q + 8 * 8192;                   // 128 rows x 128 B
+  static constexpr int MAXP = P + 16384;                   // [2][4][64] f32
+  static constexpr int SUMP = MAXP + 2 * 4 * 64 * 4;       // [2][4][64] f32
+  static constexpr int MROW = SUMP + 2 * 4 * 64 * 4;       // [4 warps][64] f32 running max
+  static constexpr int FAC = MROW + 4 * 64 * 4;            // [4][64] f32 rescale factors
+  static constexpr int RMASK = FAC + 4 * 64 * 4;          // [2 tiles][4 warps] u32 row-valid bits
+  static constexpr int BAR = RMASK + 64;
+  static constexpr int NBAR = 32;
+  static constexpr int MISC = BAR + NBAR * 8;
+  static constexpr int BYTES = MISC + 64 + 1024;           // + alignment slack
+};
+
+// row set of one query row
+struct AttRow {
+  int b, i, hg, c;
+  long long t;
+  int nsel;        // compressed rows (selected or visible)
+  long long w0;    // first window token
+  int nrows;       // nsel + window size
+  int r0, r1;      // this chunk's rows [r0, r1)
+};
+
+CSA_DEVINL AttRow att_item(const AttendTcArgs& a, int it) {
+  AttRow x;
+  x.c = it % a.nch;
+  int rest = it / a.nch;
+  x.hg = rest % a.HG;
+  rest /= a.HG;
+  x.i = rest % a.Tq;
+  x.b = rest / a.Tq;
+  x.t = (long long)a.q_pos0 + x.i;
+  long long vis = (x.t + 1) / a.m;
+  if (vis > a.N) vis = a.N;
+  if (vis < 0) vis = 0;
+  x.nsel = a.idx ? (int)min((long long)a.k, vis) : (int)vis;
+  x.w0 = x.t - a.n_win + 1;
+  if (x.w0 < 0) x.w0 = 0;
+  x.nrows = x.nsel + (int)(x.t - x.w0 + 1);
+  x.r0 = min(x.nrows, x.c * a.chunk_rows);
+  x.r1 = min(x.nrows, x.r0 + a.chunk_rows);
+  return x;
+}
+
+CSA_DEVINL void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+CSA_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+CSA_DEVINL void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+CSA_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+CSA_DEVINL void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// rotate the 4 (x0, x1) pairs of one 16-byte bf16 unit; pair p uses frequency j0 + p
+CSA_DEVINL uint4 rope_unit(uint4 v, long long pos, const RopeFreqs& rf, int j0) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[p]);
+    float2 f = __bfloat1622float2(h);
+    float c, s;
+    rope_cos_sin(pos, rf.F[j0 + p], c, s);
+    w[p] = pack_bf16x2(f.x * c - f.y * s, f.x * s + f.y * c);
+  }
+  return v;
+}
+
+// reduce-scatter butterfly over the warp: on entry x[0..63] per lane; on exit
+// lane l holds op-reduced columns 2l (x[0]) and 2l+1 (x[1]) over all 32 lanes.
+template <bool IS_MAX>
+CSA_DEVINL void warp_reduce_scatter64(float* x, int lane) {
+#pragma unroll
+  for (int lvl = 0; lvl < 5; ++lvl) {
+    const int off = 16 >> lvl;        // partner distance
+    const int hs = 32 >> lvl;         // half of the values still held
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int e = 0; e < hs; ++e) {
+      const float lo = x[e], hi = x[e + hs];
+      const float send = upper ? lo : hi;
+      const float keep = upper ? hi : lo;
+      const float got = __shfl_xor_sync(0xffffffffu, send, off);
+      x[e] = IS_MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+}
+
+// gather one 16-byte unit of a mixed-precision row (dims 8u..8u+7 of 512)
+CSA_DEVINL uint4 load_mixed_unit(const uint8_t* nope_row, float scale,
+                                 const __nv_bfloat16* rope_row, int unit) {
+  if (unit < (ATT_D - ATT_R) / 8) {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(nope_row + unit * 8));
+    float f[8];
+    const __nv_fp8x2_storage_t* p2 = reinterpret_cast<const __nv_fp8x2_storage_t*>(&raw);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(p2[e], __NV_E4M3);
+      __half2 h2 = *reinterpret_cast<__half2*>(&hr);
+      float2 v = __half22float2(h2);
+      f[2 * e] = v.x * scale;
+      f[2 * e + 1] = v.y * scale;
+    }
+    return f_to_bf16x8(f);
+  }
+  return __ldg(reinterpret_cast<const uint4*>(rope_row + (unit - (ATT_D - ATT_R) / 8) * 8));
+}
+
+__global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sE = smem + AttSmem::E;
+  uint8_t* sQ = smem + AttSmem::Q;
+  uint8_t* sP = smem + AttSmem::P;
+  float* maxp = reinterpret_cast<float*>(smem + AttSmem::MAXP);
+  float* sump = reinterpret_cast<float*>(smem + AttSmem::SUMP);
+  float* mrow = reinterpret_cast<float*>(smem + AttSmem::MROW);
+  float* facs = reinterpret_cast<float*>(smem + AttSmem::FAC);
+  volatile uint32_t* rmask = reinterpret_cast<volatile uint32_t*>(smem + AttSmem::RMASK);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + AttSmem::BAR);
+  uint64_t* chunk_full = bar;        // [8]  gather warps -> MMA (count 4)
+  uint64_t* chunk_free = bar + 8;    // [4]  PV block done -> gather (commit)
+  uint64_t* s_full = bar + 12;       // [2]  QK done -> softmax (commit)
+  uint64_t* s_free = bar + 14;       // [2]  softmax read S -> MMA (count 4)
+  uint64_t* p_full = bar + 16;       // P^T written (+ O rescaled) -> MMA (count 4)
+  uint64_t* p_free = bar + 17;       // PV done (commit)
+  uint64_t* q_full = bar + 18;       // Q staged -> MMA (count 4)
+  uint64_t* q_free = bar + 19;       // last QK of the item done (commit)
+  uint64_t* o_free = bar + 20;       // epilogue read O -> MMA (count 4)
+  uint64_t* grp_a = bar + 21;        // softmax warps: tile max partials (count 4)
+  uint64_t* grp_b = bar + 22;        // softmax warps: sum partials (count 4)
+  uint64_t* mma_done = bar + 23;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttSmem::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttSmem::MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < 8; ++c) mbar_init(chunk_full + c, 4);
+    for (int c = 0; c < 4; ++c) mbar_init(chunk_free + c, 1);
+    for (int s = 0; s < 2; ++s) { mbar_init(s_full + s, 1); mbar_init(s_free + s, 4); }
+    mbar_init(p_full, 4);
+    mbar_init(p_free, 1);
+    mbar_init(q_full, 4);
+    mbar_init(q_free, 1);
+    mbar_init(o_free, 4);
+    mbar_init(grp_a, 4);
+    mbar_init(grp_b, 4);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t TM_O = 0, TM_S = 256;     // O^T blocks at 0..255, S^T buffers at 256..383
+
+  if (warp >= 4 && warp < 8) {
+    // ======================= gather warps =======================
+    const int gw = warp - 4;
+    uint32_t n = 0, nitem = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+      const AttRow x = att_item(a, it);
+      if (x.r1 <= x.r0) continue;
+      // ---- queries of this head group, RoPE at t, swizzled K-major [64 heads][512] ----
+      if (!mbar_wait(q_free, (nitem & 1) ^ 1, abort_flag)) { ok = false; break; }
+      ++nitem;
+      {
+        const __nv_bfloat16* qrow0 =
+            a.q + (((size_t)x.b * a.Tq + x.i) * a.n_h + (size_t)x.hg * ATT_HG + gw * 16) * ATT_D;
+#pragma unroll 4
+        for (int k2 = 0; k2 < 32; ++k2) {
+          const int u_all = k2 * 32 + lane;          // 0..1023 over 16 heads x 64 units
+          const int hl = u_all >> 6, ur = u_all & 63;
+          const int c = ur >> 3, u = ur & 7;
+          uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow0 + (size_t)hl * ATT_D + ur * 8));
+          if (c == 7) v = rope_unit(v, x.t, a.rf, u * 4);
+          const int h = gw * 16 + hl;
+          *reinterpret_cast<uint4*>(sQ + c * 8192 + h * 128 + ((u ^ (h & 7)) << 4)) = v;
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
+      }
+      // ---- tiles ----
+      for (int r0 = x.r0; r0 < x.r1 && ok; r0 += ATT_TILE, ++n) {
+        // this lane's row: tile row gw*32 + lane
+        const int rr = r0 + gw * 32 + lane;
+        const uint8_t* src = nullptr;        // bf16 row, or e4m3 nope row
+        const __nv_bfloat16* rsrc = nullptr; // mixed: rope row
+        float rscale = 0.f;
+        long long pos = 0;
+        if (rr < x.r1) {
+          if (rr < x.nsel) {
+            int s = a.idx ? __ldg(a.idx + ((size_t)x.b * a.Tq + x.i) * a.k + rr) : rr;
+            if (s >= a.N) { csa_flag_error(ERRBIT_BAD_INDEX); s = -1; }
+            if (s >= 0) {
+              const size_t row = (size_t)x.b * a.N + s;
+              if (a.kv_mixed) {
+                src = reinterpret_cast<const uint8_t*>(a.ent) + row * (ATT_D - ATT_R);
+                rsrc = a.ent_rope + row * ATT_R;
+                rscale = __ldg(a.ent_scale + row);
+              } else {
+                src = reinterpret_cast<const uint8_t*>(a.ent) + row * ATT_D * 2;
+              }
+              pos = (long long)a.m * (s + 1) - 1;
+            }
+          } else {
+            const long long tok = x.w0 + (rr - x.nsel);
+            const size_t row = (size_t)x.b * a.T_win + (size_t)(tok - a.win_base);
+            if (a.kv_mixed) {
+              src = reinterpret_cast<const uint8_t*>(a.win) + row * (ATT_D - ATT_R);
+              rsrc = a.win_rope + row * ATT_R;
+              rscale = __ldg(a.win_scale + row);
+            } else {
+              src = reinterpret_cast<const uint8_t*>(a.win) + row * ATT_D * 2;
+            }
+            pos = tok;
+          }
+        }
+        // rows with no source (past the chunk, index -1) take logit -inf in the softmax
+        {
+          const uint32_t bits = __ballot_sync(0xffffffffu, src != nullptr);
+          if (lane == 0) rmask[(n & 1) * 4 + gw] = bits;
+        }
+        for (int c = 0; c < 8 && ok; ++c) {
+          if ((c & 1) == 0 && !mbar_wait(chunk_free + (c >> 1), (n & 1) ^ 1, abort_flag)) { ok = false; break; }
+          uint8_t* dst_chunk = sE + c * 16384;
+#pragma unroll
+          for (int k2 = 0; k2 < 8; ++k2) {
+            const int rl = k2 * 4 + (lane >> 3);           // row within this warp's 32
+            const int u = lane & 7;
+            const uint8_t* s_row = reinterpret_cast<const uint8_t*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src), rl));
+            const int tr = gw * 32 + rl;                   // tile row
+            const uint32_t dst = smem_u32(dst_chunk + tr * 128 + ((u ^ (tr & 7)) << 4));
+            if (!a.kv_mixed) {
+              cp_async16(dst, s_row ? s_row + c * 128 + u * 16 : reinterpret_cast<const uint8_t*>(a.q),
+                         s_row != nullptr);
+            } else {
+              const __nv_bfloat16* r_row = reinterpret_cast<const __nv_bfloat16*>(
+                  __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rsrc), rl));
+              const float sc = __shfl_sync(0xffffffffu, rscale, rl);
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (s_row) v = load_mixed_unit(s_row, sc, r_row, c * 8 + u);
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
+                           "r"(v.z), "r"(v.w)
+                           : "memory");
+            }
+          }
+          cp_async_commit();
+          if (c >= ATT_LAG) {
+            cp_async_wait<ATT_LAG>();
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(chunk_full + (c - ATT_LAG));
+          }
+        }
+        if (!ok) break;
+        cp_async_wait<0>();
+        __syncwarp();
+        if (a.rotate_rows) {
+          // RoPE of this warp's 32 rows: chunk 7 holds dims 448..511
+          uint8_t* c7 = sE + 7 * 16384;
+#pragma unroll 2
+          for (int k2 = 0; k2 < 8; ++k2) {
+            const int rl = k2 * 4 + (lane >> 3);
+            const int u = lane & 7;
+            const long long p = __shfl_sync(0xffffffffu, pos, rl);
+            const int tr = gw * 32 + rl;
+            uint4* ptr = reinterpret_cast<uint4*>(c7 + tr * 128 + ((u ^ (tr & 7)) << 4));
+            *ptr = rope_unit(*ptr, p, a.rf, u * 4);
+          }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0)
+          for (int c = 8 - ATT_LAG; c < 8; ++c) mbar_arrive(chunk_full + c);
+      }
+    }
+  } else if (warp == 8) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16(ATT_TILE, ATT_HG);
+      const uint32_t id_pv = idesc_bf16(ATT_TILE, ATT_HG) | (1u << 15) | (1u << 16);
+      uint32_t n = 0, nitem = 0;
+      bool ok = true;
+      const uint32_t e_base = smem_u32(sE), q_base = smem_u32(sQ), p_base = smem_u32(sP);
+      for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+        const AttRow x = att_item(a, it);
+        if (x.r1 <= x.r0) continue;
+        if (!mbar_wait(q_full, nitem & 1, abort_flag)) { ok = false; break; }
+        const uint32_t item = nitem++;
+        int j = 0;
+        for (int r0 = x.r0; r0 < x.r1; r0 += ATT_TILE, ++n, ++j) {
+          const uint32_t sb = n & 1;
+          if (!mbar_wait(s_free + sb, ((n >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          // S^T = E * Q^T over the 8 dim chunks as they land
+          for (int c = 0; c < 8; ++c) {
+            if (!mbar_wait(chunk_full + c, n & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(e_base + c * 16384 + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(q_base + c * 8192 + kk * 32, 16, 1024);
+              umma_f16(tmem + TM_S + sb * ATT_HG, ad, bd, id_qk, (c | kk) ? 1u : 0u);
+            }
+          }
+          if (!ok) break;
+          umma_commit(s_full + sb);
+          if (r0 + ATT_TILE >= x.r1) umma_commit(q_free);
+          if (j == 0 && !mbar_wait(o_free, (item & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(p_full, n & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // O^T[dims block bk] += E^T * P^T
+          for (int bk = 0; bk < 4; ++bk) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = sdesc_sw128(e_base + bk * 32768 + kk * 2048, 16384, 1024);
+              const uint64_t bd = sdesc_sw128(p_base + kk * 2048, 8192, 1024);
+              umma_f16(tmem + TM_O + bk * ATT_HG, ad, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(chunk_free + bk);
+          }
+          umma_commit(p_free);
+        }
+      }
+      umma_commit(mma_done);
+      mbar_drain(mma_done, 0);
+    }
+  } else {
+    // ======================= softmax / epilogue (warps 0-3) =======================
+    const int q4 = warp;                              // TMEM lane quarter
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    float* my_m = mrow + q4 * 64;
+    float* my_f = facs + q4 * 64;
+    uint32_t n = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+      const AttRow x = att_item(a, it);
+      float m_run[2] = {-INFINITY, -INFINITY};        // heads 2*lane, 2*lane+1
+      float l_run[2] = {0.f, 0.f};
+      int j = 0;
+      for (int r0 = x.r0; r0 < x.r1; r0 += ATT_TILE, ++n, ++j) {
+        const uint32_t sb = n & 1, par = n & 1;
+        if (!mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float xs[64];
+        {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + TM_S + sb * ATT_HG, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) xs[e] = __uint_as_float(r[e]);
+          tmem_ld32(tmem + lane_base + TM_S + sb * ATT_HG + 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) xs[32 + e] = __uint_as_float(r[e]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free + sb);
+        const bool valid = (rmask[(n & 1) * 4 + q4] >> lane) & 1u;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) xs[e] = valid ? xs[e] * a.scale_log2 : -INFINITY;
+        // ---- per-head tile max over the 128 rows ----
+        float red[64];
+#pragma unroll
+        for (int e = 0; e < 64; ++e) red[e] = xs[e];
+        warp_reduce_scatter64<true>(red, lane);
+        maxp[(par * 4 + q4) * 64 + 2 * lane] = red[0];
+        maxp[(par * 4 + q4) * 64 + 2 * lane + 1] = red[1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(grp_a);
+        if (!mbar_wait(grp_a, par, abort_flag)) { ok = false; break; }
+        bool resc = false;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * lane + e;
+          float tm = maxp[(par * 4 + 0) * 64 + h];
+          tm = fmaxf(tm, maxp[(par * 4 + 1) * 64 + h]);
+          tm = fmaxf(tm, maxp[(par * 4 + 2) * 64 + h]);
+          tm = fmaxf(tm, maxp[(par * 4 + 3) * 64 + h]);
+          float f = 1.f;
+          if (j == 0) {
+            m_run[e] = tm;
+          } else if (tm > m_run[e] + ATT_TAU) {
+            f = exp2f(m_run[e] - tm);
+            m_run[e] = tm;
+            resc = true;
+          }
+          my_m[h] = m_run[e];
+          my_f[h] = f;
+          l_run[e] *= f;
+        }
+        resc = __any_sync(0xffffffffu, resc);
+        __syncwarp();
+        // ---- P = exp2(x - m), bf16; row pieces of P^T ----
+        uint32_t pk[32];
+        float* pr = red;                              // reused: rounded P for the row sums
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = exp2f(xs[2 * e] - my_m[2 * e]);
+          const float p1 = exp2f(xs[2 * e + 1] - my_m[2 * e + 1]);
+          pk[e] = pack_bf16x2(p0, p1);
+          const float2 back = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk[e]));
+          pr[2 * e] = back.x;
+          pr[2 * e + 1] = back.y;
+        }
+        // PV of the previous tile must be done before P^T and O^T are touched
+        if (!mbar_wait(p_free, (n & 1) ^ 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const int tr = q4 * 32 + lane;
+          uint8_t* prow = sP + tr * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(prow + ((u ^ (tr & 7)) << 4)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        if (resc && j > 0) {
+          // O^T columns (heads) times their factors; this warp owns dims rows
+          // q4*32 + lane of each 128-dim block
+#pragma unroll 1
+          for (int bk = 0; bk < 4; ++bk) {
+#pragma unroll
+            for (int hh = 0; hh < 64; hh += 32) {
+              uint32_t r[32];
+              const uint32_t ta = tmem + lane_base + TM_O + bk * ATT_HG + hh;
+              tmem_ld32(ta, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * my_f[hh + e]);
+              tmem_st32(ta, r);
+            }
+          }
+          tmem_st_wait();
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+        // ---- per-head row sums ----
+        warp_reduce_scatter64<false>(pr, lane);
+        sump[(par * 4 + q4) * 64 + 2 * lane] = pr[0];
+        sump[(par * 4 + q4) * 64 + 2 * lane + 1] = pr[1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(grp_b);
+        if (!mbar_wait(grp_b, par, abort_flag)) { ok = false; break; }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * lane + e;
+          l_run[e] += sump[(par * 4 + 0) * 64 + h] + sump[(par * 4 + 1) * 64 + h] +
+                      sump[(par * 4 + 2) * 64 + h] + sump[(par * 4 + 3) * 64 + h];
+        }
+      }
+      if (!ok) break;
+      // ======================= item epilogue =======================
+      const bool single = (a.nch == 1);
+      if (j > 0) {
+        if (!mbar_wait(p_free, (n - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+      }
+      // per-head output scale into this warp's table
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * lane + e;
+        if (single) {
+          const float zs = __ldg(a.sink + x.hg * ATT_HG + h) * 1.4426950408889634f;
+          const float M = fmaxf(m_run[e], zs);
+          const float den = l_run[e] * exp2f(m_run[e] - M) + exp2f(zs - M);
+          my_f[h] = exp2f(m_run[e] - M) / den;
+        } else {
+          my_f[h] = 1.f;
+          float* ml = a.part_ml + ((size_t)it * ATT_HG + h) * 2;
+          if (q4 == 0) { ml[0] = m_run[e]; ml[1] = l_run[e]; }
+        }
+      }
+      __syncwarp();
+      const size_t orow = ((size_t)x.b * a.Tq + x.i) * a.n_h + (size_t)x.hg * ATT_HG;
+#pragma unroll 1
+      for (int bk = 0; bk < 4; ++bk) {
+        const int dim = bk * 128 + q4 * 32 + lane;
+        float c = 1.f, s = 0.f;
+        const bool rope_dim = dim >= ATT_D - ATT_R;
+        if (single && rope_dim) rope_cos_sin(-x.t, a.rf.F[(dim - (ATT_D - ATT_R)) >> 1], c, s);
+#pragma unroll
+        for (int hh = 0; hh < 64; hh += 32) {
+          uint32_t r[32];
+          if (j > 0) {
+            tmem_ld32(tmem + lane_base + TM_O + bk * ATT_HG + hh, r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = 0u;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float v = __uint_as_float(r[e]) * my_f[hh + e];
+            if (single) {
+              const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
+              if (rope_dim) v = (lane & 1) ? (pv * s + v * c) : (v * c - pv * s);
+              a.out[(orow + hh + e) * ATT_D + dim] = __float2bfloat16_rn(v);
+            } else {
+              a.part_o[((size_t)it * ATT_HG + hh + e) * ATT_D + dim] = v;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && j > 0) mbar_arrive(o_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 8) tmem_dealloc(tmem, 512);
+}
+
+// ----------------------------------------------------------------------------
+// split-chunk combine: out[b,i,h,:] = sum_c 2^(m_c - M) O_c / (sum_c 2^(m_c - M) l_c
+// + 2^(z'_h log2 e - M)), then the RoPE dims rotated back by -t.
+// ----------------------------------------------------------------------------
+struct CombineArgs {
+  const float* part_o; const float* part_ml; const float* sink;
+  __nv_bfloat16* out;
+  int Tq, n_h, HG, nch, q_pos0;
+  RopeFreqs rf;
+};
+
+__global__ void __launch_bounds__(128) attend_combine_kernel(const CombineArgs a) {
+  const int row = blockIdx.x;                   // (b * Tq + i) * n_h + h
+  const int h = row % a.n_h;
+  const int bi = row / a.n_h;
+  const int i = bi % a.Tq;
+  const int hg = h / ATT_HG, hl = h % ATT_HG;
+  const size_t it0 = ((size_t)bi * a.HG + hg) * a.nch;
+  const float zs = __ldg(a.sink + h) * 1.4426950408889634f;
+  float M = zs;
+  for (int c = 0; c < a.nch; ++c) M = fmaxf(M, __ldg(a.part_ml + ((it0 + c) * ATT_HG + hl) * 2));
+  float den = exp2f(zs - M);
+  const int d0 = threadIdx.x * 4;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = 0; c < a.nch; ++c) {
+    const float* ml = a.part_ml + ((it0 + c) * ATT_HG + hl) * 2;
+    const float mc = __ldg(ml);
+    if (mc == -INFINITY) continue;
+    const float wgt = exp2f(mc - M);
+    den += __ldg(ml + 1) * wgt;
+    const float4 o = __ldg(reinterpret_cast<const float4*>(a.part_o + ((it0 + c) * ATT_HG + hl) * ATT_D + d0));
+    acc[0] += o.x * wgt; acc[1] += o.y * wgt; acc[2] += o.z * wgt; acc[3] += o.w * wgt;
+  }
+  const float inv = 1.f / den;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) acc[e] *= inv;
+  if (d0 >= ATT_D - ATT_R) {
+    const long long t = (long long)a.q_pos0 + i;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      float c, s;
+      rope_cos_sin(-t, a.rf.F[((d0 - (ATT_D - ATT_R)) >> 1) + p], c, s);
+      const float x0 = acc[2 * p], x1 = acc[2 * p + 1];
+      acc[2 * p] = x0 * c - x1 * s;
+      acc[2 * p + 1] = x0 * s + x1 * c;
+    }
+  }
+  __nv_bfloat16* o = a.out + (size_t)row * ATT_D + d0;
+  *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+}
+
+// ----------------------------------------------------------------------------
+// RoPE pre-rotation of a row set (bf16 rows, rotated copy of the last 64 dims
+// at each row's position): used when many query rows gather the same rows.
+// ----------------------------------------------------------------------------
+struct RotateArgs {
+  const __nv_bfloat16* src; __nv_bfloat16* dst;
+  long long rows;                 // B * rows per batch row
+  int rows_per_b;
+  int m;                          // >0: compressed entries (pos = m(s+1)-1); 0: tokens
+  long long base;                 // token position of row 0 (tokens)
+  RopeFreqs rf;
+};
+
+__global__ void __launch_bounds__(256) rope_rotate_rows_kernel(const RotateArgs a) {
+  // one thread per 16-byte unit; 64 units per 512-dim row
+  const long long u_all = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u_all >= a.rows * 64) return;
+  const long long row = u_all >> 6;
+  const int u = (int)(u_all & 63);
+  uint4 v = __ldg(reinterpret_cast<const uint4*>(a.src + row * ATT_D + u * 8));
+  if (u >= (ATT_D - ATT_R) / 8) {
+    const long long s = row % a.rows_per_b;
+    const long long pos = a.m > 0 ? (long long)a.m * (s + 1) - 1 : a.base + s;
+    v = rope_unit(v, pos, a.rf, (u - (ATT_D - ATT_R) / 8) * 4);
+  }
+  *reinterpret_cast<uint4*>(a.dst + row * ATT_D + u * 8) = v;
+}
+
+}  // namespace csa

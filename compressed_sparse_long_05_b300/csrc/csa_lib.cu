@@ -12,6 +12,7 @@
 #include "topk.cuh"
 #include "simt_f32.cuh"
 #include "index_tc.cuh"
+#include "attend_tc.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -120,6 +121,62 @@ csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, floa
   kern<<<grid, csa::IDX_THREADS, smem, stream>>>(tmK, tmq, a);
   CSA_CHECK_LAUNCH("csa_index tc");
   return CSA_OK;
+}
+
+// Work split and scratch layout of the tensor-core attention path.
+struct AttPlan {
+  int HG, nch, chunk_rows, items, rotate_rows;
+  size_t off_part_o, off_part_ml, off_rot_ent, off_rot_win, bytes;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int m, int n_win, int q_pos0,
+                    int dense, int kv_mixed) {
+  AttPlan p;
+  memset(&p, 0, sizeof(p));
+  p.HG = n_h / csa::ATT_HG;
+  const long long t_last = (long long)q_pos0 + Tq - 1;
+  long long vis = (t_last + 1) / m;
+  if (vis > N) vis = N;
+  const long long nsel = dense ? vis : (vis < k ? vis : k);
+  const long long win = t_last + 1 < n_win ? t_last + 1 : n_win;
+  const long long rows_max = nsel + win;
+  const int tiles = (int)((rows_max + csa::ATT_TILE - 1) / csa::ATT_TILE);
+  const long long units = (long long)B * Tq * p.HG;
+  const int sms = sm_count();
+  int chunk_tiles = tiles;
+  if (units < sms && tiles > 1) {
+    chunk_tiles = (int)((units * tiles + sms - 1) / sms);
+    if (chunk_tiles < 1) chunk_tiles = 1;
+  }
+  p.nch = (tiles + chunk_tiles - 1) / chunk_tiles;
+  if (p.nch < 1) p.nch = 1;
+  p.chunk_rows = chunk_tiles * csa::ATT_TILE;
+  p.items = (int)(units * p.nch);
+  // rotate every stored row once when the queries gather far more rows than exist
+  const long long gathered = (long long)B * Tq * rows_max;
+  p.rotate_rows = (kv_mixed || gathered <= 2LL * B * ((long long)N + T_win)) ? 1 : 0;
+  size_t off = 0;
+  if (p.nch > 1) {
+    p.off_part_o = off;
+    off = align256(off + (size_t)p.items * csa::ATT_HG * csa::ATT_D * sizeof(float));
+    p.off_part_ml = off;
+    off = align256(off + (size_t)p.items * csa::ATT_HG * 2 * sizeof(float));
+  }
+  if (!p.rotate_rows) {
+    p.off_rot_ent = off;
+    off = align256(off + (size_t)B * N * csa::ATT_D * 2);
+    p.off_rot_win = off;
+    off = align256(off + (size_t)B * T_win * csa::ATT_D * 2);
+  }
+  p.bytes = off;
+  return p;
+}
+
+bool tc_attend_shape(int n_h, int d, int r, int kv_dtype) {
+  return d == csa::ATT_D && r == csa::ATT_R && n_h % csa::ATT_HG == 0 &&
+         (kv_dtype == CSA_DT_BF16 || kv_dtype == CSA_DT_E4M3_BF16ROPE);
 }
 
 }  // namespace
@@ -324,7 +381,72 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
     CSA_CHECK_LAUNCH("csa_attend f32");
     return CSA_OK;
   }
-  return CSA_ERR_UNSUPPORTED;
+  if (!tc_attend_shape(n_h, d, r, ent.dtype) || ent.dtype != win.dtype) return CSA_ERR_UNSUPPORTED;
+  const int mixed = ent.dtype == CSA_DT_E4M3_BF16ROPE;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(win.data, 16) || (N > 0 && !aligned(ent.data, 16)))
+    return CSA_ERR_INVALID_ARG;
+  if (mixed && (!win.scale || !win.rope || !aligned(win.rope, 16) ||
+                (N > 0 && (!ent.scale || !ent.rope || !aligned(ent.rope, 16)))))
+    return CSA_ERR_INVALID_ARG;
+  const AttPlan p = plan_attend(B, Tq, N, k, T_win, n_h, m, n_win, q_pos0, dense, mixed);
+  if (p.bytes > 0 && (!ws || ws_bytes < p.bytes || !aligned(ws, 256))) return CSA_ERR_WORKSPACE;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  csa::AttendTcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  a.ent = ent.data; a.ent_scale = ent.scale;
+  a.ent_rope = reinterpret_cast<const __nv_bfloat16*>(ent.rope);
+  a.win = win.data; a.win_scale = win.scale;
+  a.win_rope = reinterpret_cast<const __nv_bfloat16*>(win.rope);
+  a.idx = dense ? nullptr : idx;
+  a.sink = sink;
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.B = B; a.Tq = Tq; a.N = N; a.k = dense ? 0 : k; a.T_win = T_win; a.win_base = win_base;
+  a.n_h = n_h; a.m = m; a.n_win = n_win; a.q_pos0 = q_pos0;
+  a.HG = p.HG; a.nch = p.nch; a.chunk_rows = p.chunk_rows; a.items = p.items;
+  a.rotate_rows = p.rotate_rows; a.kv_mixed = mixed;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  a.rf = rf;
+  cudaStream_t st = S(stream);
+  if (!p.rotate_rows) {
+    // rotate the RoPE dims of every stored row once
+    csa::RotateArgs ra;
+    ra.rf = rf;
+    if (N > 0) {
+      ra.src = reinterpret_cast<const __nv_bfloat16*>(ent.data);
+      ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_ent);
+      ra.rows = (long long)B * N; ra.rows_per_b = N; ra.m = m; ra.base = 0;
+      csa::rope_rotate_rows_kernel<<<(unsigned)((ra.rows * 64 + 255) / 256), 256, 0, st>>>(ra);
+      CSA_CHECK_LAUNCH("csa_attend rotate entries");
+      a.ent = ra.dst;
+    }
+    ra.src = reinterpret_cast<const __nv_bfloat16*>(win.data);
+    ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_win);
+    ra.rows = (long long)B * T_win; ra.rows_per_b = T_win; ra.m = 0; ra.base = win_base;
+    csa::rope_rotate_rows_kernel<<<(unsigned)((ra.rows * 64 + 255) / 256), 256, 0, st>>>(ra);
+    CSA_CHECK_LAUNCH("csa_attend rotate window");
+    a.win = ra.dst;
+  }
+  if (p.nch > 1) {
+    a.part_o = reinterpret_cast<float*>(wsb + p.off_part_o);
+    a.part_ml = reinterpret_cast<float*>(wsb + p.off_part_ml);
+  }
+  const int smem = csa::AttSmem::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(csa::attend_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc attr");
+  const int sms = sm_count();
+  const int grid = p.items < sms ? p.items : sms;
+  csa::attend_tc_kernel<<<grid, csa::ATT_THREADS, smem, st>>>(a);
+  CSA_CHECK_LAUNCH("csa_attend tc");
+  if (p.nch > 1) {
+    csa::CombineArgs ca;
+    ca.part_o = a.part_o; ca.part_ml = a.part_ml; ca.sink = sink; ca.out = a.out;
+    ca.Tq = Tq; ca.n_h = n_h; ca.HG = p.HG; ca.nch = p.nch; ca.q_pos0 = q_pos0; ca.rf = rf;
+    csa::attend_combine_kernel<<<(unsigned)((size_t)B * Tq * n_h), 128, 0, st>>>(ca);
+    CSA_CHECK_LAUNCH("csa_attend combine");
+  }
+  return CSA_OK;
 }
 
 csa_status_t csa_attend(const void* q, csa_kv_t entries, const int32_t* idx, csa_kv_t win,
@@ -346,9 +468,11 @@ csa_status_t hca_attend(const void* q, csa_kv_t entries, csa_kv_t win, const flo
 size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h, int d, int r,
                                  int m, int n_win, int q_pos0, int q_dtype, int kv_dtype,
                                  int is_hca) {
-  (void)B; (void)Tq; (void)N; (void)k; (void)T_win; (void)n_h; (void)d; (void)r; (void)m;
-  (void)n_win; (void)q_pos0; (void)q_dtype; (void)kv_dtype; (void)is_hca;
-  return 0;
+  (void)q_dtype;
+  if (B <= 0 || Tq <= 0 || n_h <= 0 || m <= 0 || N < 0) return 0;
+  if (!tc_attend_shape(n_h, d, r, kv_dtype)) return 0;
+  return plan_attend(B, Tq, N, is_hca ? 0 : k, T_win, n_h, m, n_win, q_pos0, is_hca ? 1 : 0,
+                     kv_dtype == CSA_DT_E4M3_BF16ROPE ? 1 : 0).bytes;
 }
 
 }  // extern "C"

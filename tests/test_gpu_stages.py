@@ -198,3 +198,89 @@ def test_index_bf16(K, B, Tq, N, H, c, q_pos0):
         got = f64(s[b])
         for i in range(Tq):
             assert_scores_close(got[i], ref[i], f"b={b} row {i}")
+
+
+# ----------------------------------------------------------------------------
+# attention (bf16, tcgen05 path)
+# ----------------------------------------------------------------------------
+
+
+def _rms(shape, seed):
+    x = torch.randn(shape, generator=_gen(seed), device=DEV)
+    return (x * torch.rsqrt(x.square().mean(-1, keepdim=True))).to(torch.bfloat16)
+
+
+def _attend_case(K, B, Tq, N, k, q_pos0, T_win, win_base, n_h=128, m=4, n_win=128, dense=False,
+                 rows=None, seed=50):
+    d, r = 512, 64
+    q = _rms((B, Tq, n_h, d), seed)
+    ent = _rms((B, N, d), seed + 1)
+    win = _rms((B, T_win, d), seed + 2)
+    sink = torch.randn((n_h,), generator=_gen(seed + 3), device=DEV)
+    if dense:
+        out = K.hca_attend(q, ent, win, sink, m, n_win, win_base, q_pos0, r)
+        idx = None
+    else:
+        scores = torch.rand((B, Tq, N), generator=_gen(seed + 4), device=DEV)
+        idx = K.csa_topk(scores, k, m, q_pos0)
+        out = K.csa_attend(q, ent, idx, win, sink, m, n_win, win_base, q_pos0, r)
+    torch.cuda.synchronize()
+    K.device_error()
+    e64, w64, s64 = f64(ent), f64(win), f64(sink)
+    rows = range(Tq) if rows is None else rows
+    for b in range(B):
+        for i in rows:
+            t = q_pos0 + i
+            q64 = f64(q[b, i])
+            if dense:
+                ref = O.hca_attend_token(q64, t, e64[b], w64[b], win_base, s64, m, n_win, r, 1e4)
+            else:
+                ref = O.csa_attend_token(q64, t, e64[b], idx[b, i].cpu().numpy(), w64[b], win_base,
+                                         s64, m, n_win, r, 1e4)
+            assert_close(f64(out[b, i]), ref, TOL_BF16, TOL_BF16, f"b={b} i={i} t={t}")
+
+
+def test_attend_bf16_decode_split(K):
+    # few query rows: rows split over CTAs, partials merged by the combine kernel
+    N = 3000
+    L = 4 * N
+    _attend_case(K, B=2, Tq=1, N=N, k=1024, q_pos0=L - 1, T_win=128, win_base=L - 128)
+
+
+def test_attend_bf16_decode_small_k(K):
+    N = 800
+    _attend_case(K, B=3, Tq=2, N=N, k=200, q_pos0=4 * N - 2, T_win=129, win_base=4 * N - 129, seed=60)
+
+
+def test_attend_bf16_prefill_prerotated(K):
+    # many query rows: one chunk per row, rows rotated once up front, early rows
+    # see fewer than k entries and fewer than n_win window tokens
+    T = 700
+    _attend_case(K, B=1, Tq=T, N=T // 4, k=64, q_pos0=0, T_win=T, win_base=0,
+                 rows=[0, 1, 3, 4, 5, 127, 128, 255, 256, 257, 400, 511, 600, 699], seed=70)
+
+
+def test_attend_bf16_rotate_in_smem_single_chunk(K):
+    # many query rows over a long cache: in-kernel RoPE of gathered rows
+    N = 20000
+    _attend_case(K, B=1, Tq=160, N=N, k=256, q_pos0=4 * N - 160, T_win=300,
+                 win_base=4 * N - 300, rows=[0, 1, 77, 159], seed=80)
+
+
+def test_hca_attend_bf16_decode(K):
+    N = 2500
+    L = 128 * N
+    _attend_case(K, B=2, Tq=1, N=N, k=0, q_pos0=L - 1, T_win=128, win_base=L - 128, m=128,
+                 dense=True, seed=90)
+
+
+def test_hca_attend_bf16_prefill(K):
+    T = 1100
+    _attend_case(K, B=1, Tq=T, N=T // 128, k=0, q_pos0=0, T_win=T, win_base=0, m=128, dense=True,
+                 rows=[0, 5, 126, 127, 128, 129, 300, 1023, 1099], seed=100)
+
+
+def test_attend_bf16_heads_64(K):
+    N = 500
+    _attend_case(K, B=1, Tq=3, N=N, k=128, q_pos0=4 * N - 3, T_win=140, win_base=4 * N - 140,
+                 n_h=64, seed=110)
