@@ -1,0 +1,544 @@
+"""Benchmark of one CSA / HCA attention-layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Default workload: CSA decode at V4-Pro shape, 128K context, batch 4 (one new
+query token per sequence: index -> top-k -> attend over a given compressed
+cache).  A step is one pass of every stage of the workload over one batch of
+seeded synthetic inputs already resident in HBM.  Steps are CUDA-graph
+replays; consecutive steps cycle through enough copies of the inputs that the
+working set exceeds twice the L2, so no step reads another step's data from L2.
+
+Prints one JSON line (rank 0).  With torchrun (N > 1) every rank runs an
+independent replica of the workload ("replicas only": the path has no
+exchange step) and the slowest rank's time counts.
+
+--impl reference times the float64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "CSA tokens/s (decode @128K ctx, prefill @32K) and % of HBM/tensor roofline"
+DEFAULT_WORKLOAD = "csa_decode_128k"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work per stage (bytes that must move, flops that must be done)
+# ----------------------------------------------------------------------------
+
+
+def _vis(t, m, N):
+    return min(N, (t + 1) // m)
+
+
+def row_bytes(cfg):
+    d, r = cfg["d"], cfg["r"]
+    return (d - r) + 4 + 2 * r if cfg["dtype"] == "mixed" else d * (4 if cfg["dtype"] == "f32" else 2)
+
+
+def work(cfg):
+    """{stage: (bytes, flops)} for one step of the workload."""
+    B, Tq, N, m, d = cfg["B"], cfg["Tq"], cfg["N"], cfg["m"], cfg["d"]
+    n_h, n_win, q0 = cfg["n_h"], cfg["n_win"], cfg["q_pos0"]
+    el = 4 if cfg["dtype"] == "f32" else 2
+    rb = row_bytes(cfg)
+    t = q0 + np.arange(Tq, dtype=np.int64)
+    vis = np.minimum(N, (t + 1) // m)
+    win = np.minimum(n_win, t + 1)
+    out = {}
+    kind = cfg["kind"]
+    if kind.endswith("prefill"):
+        T = cfg["T"]
+        nt = 4 if kind == "csa_prefill" else 2
+        out["compress"] = (B * (nt * T * d * el + N * d * el), 0.0)
+    if kind.startswith("csa"):
+        H, c, k = cfg["H_I"], cfg["c_I"], cfg["k"]
+        kb = (c // 2 + c // 16) if cfg["dtype"] == "mixed" else c * el
+        pairs = int(vis.sum())
+        out["index"] = (B * (N * kb + Tq * H * kb + Tq * H * 4 + Tq * N * 4), 2.0 * B * pairs * H * c)
+        out["topk"] = (B * (pairs * 4 + Tq * k * 4), 0.0)
+        rows = np.minimum(k, vis) + win
+        out["attend"] = (B * (int(rows.sum()) * rb + int(np.minimum(k, vis).sum()) * 4 +
+                              2 * Tq * n_h * d * el), 4.0 * B * int(rows.sum()) * n_h * d)
+    else:
+        rows = vis + win
+        if kind == "hca_decode":
+            gathered = B * int(rows.max()) * rb        # every query row of a sequence shares the rows
+        else:
+            gathered = B * (N + cfg["T_win"]) * rb
+        out["attend"] = (gathered + 2 * B * Tq * n_h * d * el, 4.0 * B * int(rows.sum()) * n_h * d)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+
+class NvmlClocks:
+    """Samples SM clock and throttle reasons in a thread while the timed region runs."""
+
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, index):
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+        self.samples, self.reasons = [], set()
+        self._stop = threading.Event()
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for name, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(0.005)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples), "source": "nvml" if self.ok else "unavailable"}
+
+
+def make_step(K, cfg, x, buf):
+    """Stage callables of one step on inputs x (device tensors) with buffers buf."""
+    from compressed_sparse_long_05_b300 import path as P
+    m, r, n_win = cfg["m"], cfg["r"], cfg["n_win"]
+    q0, wb, base = cfg["q_pos0"], cfg["win_base"], cfg["rope_base"]
+    kind = cfg["kind"]
+    stages = []
+    if kind == "csa_prefill":
+        stages.append(("compress", lambda: K.csa_compress(x["Ca"], x["Za"], m, Cb=x["Cb"], Zb=x["Zb"],
+                                                          out=buf.entries)))
+    if kind == "hca_prefill":
+        stages.append(("compress", lambda: K.csa_compress(x["C"], x["Z"], m, out=buf.entries)))
+    ent = buf.entries if kind.endswith("prefill") else P._entries_arg(x)
+    win = P._win_arg(x)
+    if kind.startswith("csa"):
+        qI, qI_sf, Kt, K_sf = P._indexer_args(x)
+        stages.append(("index", lambda: K.csa_index(qI, x["w"], Kt, m, q0, qI_sf=qI_sf, K_sf=K_sf,
+                                                    scores=buf.scores)))
+        stages.append(("topk", lambda: K.csa_topk(buf.scores, cfg["k"], m, q0, idx=buf.idx)))
+        stages.append(("attend", lambda: K.csa_attend(x["q"], ent, buf.idx, win, x["sink"], m, n_win,
+                                                      wb, q0, r, base, out=buf.out, ws=buf.ws)))
+    else:
+        stages.append(("attend", lambda: K.hca_attend(x["q"], ent, win, x["sink"], m, n_win, wb, q0,
+                                                      r, base, out=buf.out, ws=buf.ws)))
+    return stages
+
+
+def alloc_buffers(K, cfg, x, dev):
+    from compressed_sparse_long_05_b300 import path as P
+    buf = P.Buffers()
+    B, Tq, N, d = cfg["B"], cfg["Tq"], cfg["N"], cfg["d"]
+    kind = cfg["kind"]
+    if kind.endswith("prefill"):
+        buf.entries = torch.empty((B, N, d), dtype=x["q"].dtype, device=dev)
+    if kind.startswith("csa"):
+        buf.scores = torch.empty((B, Tq, N), dtype=torch.float32, device=dev)
+        buf.idx = torch.empty((B, Tq, cfg["k"]), dtype=torch.int32, device=dev)
+    buf.out = torch.empty_like(x["q"])
+    ent = buf.entries if kind.endswith("prefill") else P._entries_arg(x)
+    nbytes = K.attend_workspace_size(x["q"], ent, P._win_arg(x), cfg.get("k", 0), cfg["m"],
+                                     cfg["n_win"], cfg["q_pos0"], cfg["r"], not kind.startswith("csa"))
+    buf.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    return buf
+
+
+def count_kernel_nodes(step, stream):
+    """Kernels one step launches: kernel nodes of a captured graph of the step."""
+    from cuda.bindings import runtime as rt
+    g = torch.cuda.CUDAGraph(keep_graph=True)
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        for _, f in step:
+            f()
+    err, _, n = rt.cudaGraphGetNodes(g.raw_cuda_graph(), 0)
+    err, nodes, n = rt.cudaGraphGetNodes(g.raw_cuda_graph(), n)
+    kern = 0
+    for nd in nodes:
+        e2, ty = rt.cudaGraphNodeGetType(nd)
+        if ty == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel:
+            kern += 1
+    g.reset()
+    return kern
+
+
+def gpu_arm(args, cfg, rank, world):
+    import compressed_sparse_long_05_b300 as K
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    K.lib()
+    hbm_peak, tf_burst, tf_sust, peak_src = peaks()
+
+    x0 = synth.make_inputs(cfg, seed=0, device=dev)
+    wk = work(cfg)
+    step_bytes = sum(b for b, _ in wk.values())
+    copies = max(1, min(16, math.ceil(2 * L2_BYTES / max(1, step_bytes))))
+    xs = [x0] + [synth.make_inputs(cfg, seed=s, device=dev) for s in range(1, copies)]
+    bufs = [alloc_buffers(K, cfg, x, dev) for x in xs]
+    steps = [make_step(K, cfg, x, b) for x, b in zip(xs, bufs)]
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for w in range(max(3, args.warmup)):
+            for _, f in steps[w % copies]:
+                f()
+    torch.cuda.synchronize()
+    K.device_error()
+    launches_per_step = count_kernel_nodes(steps[0], stream)
+
+    # decode steps are a few microseconds: replay CUDA graphs so the host never
+    # paces the GPU.  One graph runs a whole cycle over the input copies; single
+    # step graphs cover the remainder, so exactly `steps` steps run.
+    use_graph = cfg["kind"].endswith("decode")
+    cycle, singles, inst_graphs, inst_events = None, [], [], []
+    if use_graph:
+        def capture(fns):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for f in fns:
+                    f()
+            return g
+        cycle = capture([f for c in range(copies) for _, f in steps[c]])
+        singles = [capture([f for _, f in steps[c]]) for c in range(copies)]
+        for c in range(copies):
+            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(steps[c]) + 1)]
+            gi = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gi, stream=stream, capture_error_mode="relaxed"):
+                ev[0].record()
+                for si, (_, f) in enumerate(steps[c]):
+                    f()
+                    ev[si + 1].record()
+            inst_graphs.append(gi)
+            inst_events.append(ev)
+        torch.cuda.synchronize()
+        cycle.replay()
+        for g in singles:
+            g.replay()
+        torch.cuda.synchronize()
+
+    def run_steps(n):
+        if use_graph:
+            for _ in range(n // copies):
+                cycle.replay()
+            for c in range(n % copies):
+                singles[c].replay()
+        else:
+            for s_ in range(n):
+                for _, f in steps[s_ % copies]:
+                    f()
+
+    # ---------------- timed region ----------------
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = NvmlClocks(dev.index)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with clocks, torch.cuda.stream(stream):
+        e0.record()
+        run_steps(args.steps)
+        e1.record()
+        e1.synchronize()
+    torch.cuda.synchronize()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+        torch.distributed.barrier()
+    K.device_error()
+
+    # ---------------- per-stage durations (same launches, events between stages) ----------------
+    names = [n for n, _ in steps[0]]
+    stage_ms = {n: [] for n in names}
+    reps = min(args.steps, 200) if use_graph else min(args.steps, 5)
+    with torch.cuda.stream(stream):
+        for s in range(reps):
+            if use_graph:
+                inst_graphs[s % copies].replay()
+                ev = inst_events[s % copies]
+                ev[-1].synchronize()
+                for si, n in enumerate(names):
+                    stage_ms[n].append(ev[si].elapsed_time(ev[si + 1]))
+            else:
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+                evs[0].record()
+                for si, (_, f) in enumerate(steps[s % copies]):
+                    f()
+                    evs[si + 1].record()
+                evs[-1].synchronize()
+                for si, n in enumerate(names):
+                    stage_ms[n].append(evs[si].elapsed_time(evs[si + 1]))
+    stage_avg = {n: float(np.mean(v)) for n, v in stage_ms.items()}
+
+    # ---------------- end to end through the public API, host buffers ----------------
+    e2e = e2e_leg(K, cfg, xs[0], bufs[0], stream, args, dev)
+
+    ms_step = ms_total / args.steps
+    tokens_per_step = cfg["B"] * cfg["Tq"] * world
+    value = tokens_per_step / (ms_step / 1e3)
+
+    # roofline of the stage with the largest share of the step
+    dom = max(stage_avg, key=stage_avg.get)
+    b_dom, f_dom = wk[dom]
+    if cfg["kind"].endswith("decode") or f_dom == 0:
+        achieved = b_dom / (stage_avg[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "algorithmic_bytes": b_dom, "peak_source": peak_src}
+    else:
+        achieved = f_dom / (stage_avg[dom] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": tf_sust,
+                "unit": "TFLOP/s", "frac": round(achieved / tf_sust, 4), "traffic": None,
+                "algorithmic_flops": f_dom, "peak_source": peak_src + " (sustained)"}
+    kernels = {}
+    for n in names:
+        b, f = wk[n]
+        kernels[n] = {"ms": round(stage_avg[n], 5),
+                      "share": round(stage_avg[n] / sum(stage_avg.values()), 4),
+                      "GB/s": round(b / (stage_avg[n] / 1e3) / 1e9, 1),
+                      "hbm_frac": round(b / (stage_avg[n] / 1e3) / 1e9 / hbm_peak, 4)}
+        if f:
+            tf = f / (stage_avg[n] / 1e3) / 1e12
+            kernels[n]["TFLOP/s"] = round(tf, 1)
+            kernels[n]["tensor_frac"] = round(tf / tf_sust, 4)
+    step_frac_hbm = step_bytes / (ms_step / 1e3) / 1e9 / hbm_peak
+    cfg_out = {k: cfg[k] for k in ("B", "Tq", "N", "d", "r", "n_h", "m", "n_win") if k in cfg}
+    for k in ("L", "T", "k", "H_I", "c_I"):
+        if k in cfg:
+            cfg_out[k] = cfg[k]
+    cfg_out.update({"workload": cfg["name"], "kind": cfg["kind"], "storage": cfg["dtype"],
+                    "l2": f"inputs rotate over {copies} copies (> 2x L2 per cycle)",
+                    "graph": use_graph})
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg["dtype"] != "f32" else "f32", "data": "synthetic",
+        "config": cfg_out, "roofline": roof, "step_hbm_frac": round(step_frac_hbm, 4),
+        "kernels": kernels, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    return line, xs[0]
+
+
+def e2e_leg(K, cfg, x, buf, stream, args, dev):
+    """Same metric through path.forward with per-step H2D of the step's new inputs
+    (queries, indexer queries and weights, new window row) from pinned host memory
+    and D2H of the output."""
+    from compressed_sparse_long_05_b300 import path as P
+    names = ["q"] + (["qI", "w"] if "qI" in x else (["qI_fp4", "qI_sf", "w"] if "qI_fp4" in x else []))
+    if cfg["kind"].endswith("prefill"):
+        names += [n for n in ("Ca", "Cb", "Za", "Zb", "C", "Z") if n in x]
+        names += ["win"] if "win" in x else []
+    host = {n: x[n].cpu().pin_memory() for n in names}
+    out_host = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    xd = dict(x)
+    n_steps = max(3, min(args.steps, 200 if cfg["kind"].endswith("decode") else 3))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for n, t in host.items():
+                xd[n].copy_(t, non_blocking=True)
+            P.forward(cfg, xd, buf)
+            out_host.copy_(buf.out, non_blocking=True)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_steps):
+            for n, t in host.items():
+                xd[n].copy_(t, non_blocking=True)
+            P.forward(cfg, xd, buf)
+            out_host.copy_(buf.out, non_blocking=True)
+            stream.synchronize()
+        dt = (time.perf_counter() - t0) / n_steps
+    return {"value": round(cfg["B"] * cfg["Tq"] / dt, 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_steps,
+            "api": "compressed_sparse_long_05_b300.path.forward (eager C-ABI calls)"}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle arm
+# ----------------------------------------------------------------------------
+
+
+def oracle_sample(cfg, x_np, budget_s):
+    """Runs the oracle on query rows of the workload until ~budget_s elapsed.
+
+    Returns (tokens/s, description, threads).  Prefill workloads count the
+    compression of one batch row in full plus whole query rows of the rest.
+    """
+    from oracle import pipeline as OP
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = os.cpu_count() or 1
+    kind = cfg["kind"]
+    t_start = time.perf_counter()
+    done_rows = 0
+    ent = None
+    if kind.endswith("prefill"):
+        ent = OP.entries_of(cfg, x_np, 0)
+    t_comp = time.perf_counter() - t_start
+    rows_total = cfg["Tq"]
+    rng = np.random.default_rng(0)
+    order = rng.permutation(rows_total)
+    t_rows = 0.0
+    b = 0
+    while True:
+        t0 = time.perf_counter()
+        i = int(order[done_rows % rows_total])
+        OP.run_rows(cfg, x_np, b, [i], entries=ent)
+        t_rows += time.perf_counter() - t0
+        done_rows += 1
+        if time.perf_counter() - t_start > budget_s or done_rows >= max(4 * rows_total, 100000):
+            break
+        if done_rows % rows_total == 0:
+            b = (b + 1) % cfg["B"]
+    per_row = t_rows / done_rows
+    if kind.endswith("prefill"):
+        # one full step per batch row = compression + every query row
+        t_step_per_row = t_comp + per_row * rows_total
+        tps = rows_total / t_step_per_row
+        desc = (f"compression of one {cfg['T']}-token sequence in full ({t_comp:.2f}s) + "
+                f"{done_rows} query rows of index/top-k/attend; tokens/s = T / (compress + T x per-row)")
+    else:
+        tps = 1.0 / per_row
+        desc = f"{done_rows} decode query rows (index over all N entries, top-k, attend)"
+    return tps, desc, threads
+
+
+def host_copy(x):
+    return {k: (v.float().cpu().numpy() if v.dtype in (torch.bfloat16, torch.float32)
+                else v.cpu().numpy()) for k, v in x.items()}
+
+
+def reference_arm(args, cfg, rank, world):
+    if rank != 0:
+        return None
+    x = synth.make_inputs(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    xn = host_copy(x)
+    del x
+    # the oracle is slow by design: run a bounded number of sample steps
+    # (one short warm-up, then up to 3 timed samples of ~15 s) whatever K is
+    run_steps = max(1, min(args.steps, 3))
+    per_step_budget = 15.0
+    oracle_sample(cfg, xn, 1.0)
+    vals = []
+    desc, threads = "", 1
+    for s in range(run_steps):
+        tps, desc, threads = oracle_sample(cfg, xn, per_step_budget)
+        vals.append(tps)
+    value = float(np.mean(vals))
+    tokens = cfg["B"] * cfg["Tq"]
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+            "n_gpus": world, "steps": run_steps, "steps_requested": args.steps, "warmup": 1,
+            "ms_per_step": round(tokens / value * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg["name"], "kind": cfg["kind"]},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": desc + f"; {run_steps} sample steps of ~{per_step_budget:.0f}s"},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.configs.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle CPU work")
+    args = ap.parse_args()
+    cfg = synth.get(args.workload)
+    decode = cfg["kind"].endswith("decode")
+    if args.steps is None:
+        args.steps = 20000 if decode else 10
+    if args.warmup is None:
+        args.warmup = 50 if decode else 3
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    rank = int(os.environ.get("RANK", 0))
+    if world > 1:
+        backend = "nccl" if args.impl == "native" else "gloo"
+        torch.distributed.init_process_group(backend)
+
+    if args.impl == "reference":
+        line = reference_arm(args, cfg, rank, world)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    else:
+        line, x0 = gpu_arm(args, cfg, rank, world)
+        if rank == 0:
+            if world == 1:
+                xn = host_copy(x0)
+                tps, desc, threads = oracle_sample(cfg, xn, args.cpu_budget)
+                line["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": threads,
+                                        "kind": "oracle", "sample": desc}
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
