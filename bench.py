@@ -102,53 +102,74 @@ def work(cfg):
 # ----------------------------------------------------------------------------
 
 
-class NvmlClocks:
-    """Samples SM clock and throttle reasons in a thread while the timed region runs."""
+class ClockSampler:
+    """Samples SM clocks and clock-event (throttle) reasons while the timed region runs.
 
-    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
-               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+    Uses `nvidia-smi --query-gpu ... -lms` on this process's GPU (by UUID);
+    falls back to NVML when nvidia-smi is missing.
+    """
 
-    def __init__(self, index):
-        self.ok = False
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.proc = None
+        self.err = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            self.max_mhz = None
-        self.samples, self.reasons = [], set()
-        self._stop = threading.Event()
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for name, bit in self.REASONS.items():
-                    if r & bit:
-                        self.reasons.add(name)
-            except Exception:
-                pass
-            time.sleep(0.005)
+            u = str(torch.cuda.get_device_properties(dev).uuid)
+            self.gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception as e:  # pragma: no cover
+            self.gpu_id, self.err = str(dev.index), repr(e)
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        import subprocess
+        import tempfile
+        self.out = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception as e:
+            self.err = repr(e)
         return self
 
     def __exit__(self, *a):
-        if self.ok:
-            self._stop.set()
-            self.t.join()
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
 
     def summary(self):
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples), "source": "nvml" if self.ok else "unavailable"}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            self.out.seek(0)
+            for line in self.out:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 8:
+                    continue
+                try:
+                    sm.append(float(f[0]))
+                    mx = float(f[1])
+                except ValueError:
+                    continue
+                for nm, val in zip(names, f[4:8]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        except Exception as e:
+            self.err = repr(e)
+        res = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+               "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi -lms 50"}
+        if self.err:
+            res["error"] = self.err
+        return res
 
 
 def make_step(K, cfg, x, buf):
@@ -284,7 +305,7 @@ def gpu_arm(args, cfg, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = NvmlClocks(dev.index)
+    clocks = ClockSampler(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with clocks, torch.cuda.stream(stream):

@@ -62,7 +62,8 @@ template <int CL>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   extern __shared__ __align__(16) uint32_t keys[];            // [slice]
   __shared__ uint32_t whist[TOPK_WARPS][256];
-  __shared__ uint32_t chist[2][256];                          // this CTA's histogram (double-buffered)
+  __shared__ uint32_t merged[3][256];                         // cluster histogram (used in rank 0)
+  __shared__ uint32_t hsum[256];                              // this pass's histogram over the row
   __shared__ int sh_scan[TOPK_WARPS + 1];
   __shared__ int sh_cnt[2];                                   // this CTA's (#greater, #ties)
   __shared__ uint32_t sh_sel[2];                              // selected digit, remaining k
@@ -103,6 +104,13 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
 
   uint32_t prefix = 0;          // selected high digits so far
   uint32_t krem = (uint32_t)a.k;
+  if constexpr (CL > 1) {
+    // rank 0 collects the cluster histogram; buffer (pass % 3) is written in
+    // that pass, (pass + 1) % 3 is cleared for the next one
+    if (rank == 0)
+      for (int j = tid; j < 2 * 256; j += TOPK_THREADS) (&merged[0][0])[j] = 0;
+    cluster.sync();
+  }
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
@@ -125,29 +133,35 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
       }
     }
     __syncthreads();
-    uint32_t* ch = chist[pass & 1];
-    for (int bin = tid; bin < 256; bin += TOPK_THREADS) {
-      uint32_t s = 0;
+    if constexpr (CL > 1) {
+      uint32_t* mrg = cluster.map_shared_rank(&merged[pass % 3][0], 0);
+      for (int bin = tid; bin < 256; bin += TOPK_THREADS) {
+        uint32_t s = 0;
 #pragma unroll 4
-      for (int w = 0; w < TOPK_WARPS; ++w) s += whist[w][bin];
-      ch[bin] = s;
+        for (int w = 0; w < TOPK_WARPS; ++w) s += whist[w][bin];
+        if (s) atomicAdd(mrg + bin, s);
+      }
+      if (rank == 0)
+        for (int bin = tid; bin < 256; bin += TOPK_THREADS) merged[(pass + 1) % 3][bin] = 0;
+      cluster.sync();
+      for (int bin = tid; bin < 256; bin += TOPK_THREADS) hsum[bin] = mrg[bin];
+    } else {
+      for (int bin = tid; bin < 256; bin += TOPK_THREADS) {
+        uint32_t s = 0;
+#pragma unroll 4
+        for (int w = 0; w < TOPK_WARPS; ++w) s += whist[w][bin];
+        hsum[bin] = s;
+      }
     }
-    if constexpr (CL > 1) cluster.sync(); else __syncthreads();
+    __syncthreads();
     if (wid == 0) {
-      // lane l owns bins 8l..8l+7; total over the cluster
+      // lane l owns bins 8l..8l+7
       uint32_t cnt[8];
       uint32_t part = 0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        uint32_t s = 0;
-        if constexpr (CL > 1) {
-#pragma unroll 1
-          for (int rr = 0; rr < CL; ++rr) s += cluster.map_shared_rank(ch, rr)[8 * lane + e];
-        } else {
-          s = ch[8 * lane + e];
-        }
-        cnt[e] = s;
-        part += s;
+        cnt[e] = hsum[8 * lane + e];
+        part += cnt[e];
       }
       // suffix sums from the top lane down
       uint32_t suf = part;
@@ -189,11 +203,20 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   int base_gt = 0, base_eq = 0;
   if constexpr (CL > 1) {
     cluster.sync();
-    for (int rr = 0; rr < rank; ++rr) {
-      const int* o = cluster.map_shared_rank(sh_cnt, rr);
-      base_gt += o[0];
-      base_eq += o[1];
+    // counts of the lower ranks (lane rr reads rank rr), summed across the warp
+    int g = 0, e = 0;
+    if (lane < rank) {
+      const int* o = cluster.map_shared_rank(sh_cnt, lane);
+      g = o[0];
+      e = o[1];
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, off);
+      e += __shfl_xor_sync(0xffffffffu, e, off);
+    }
+    base_gt = g;
+    base_eq = e;
   } else {
     __syncthreads();
   }
