@@ -528,8 +528,11 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.configs.WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle CPU work")
+    ap.add_argument("--set", action="append", default=[], metavar="KEY=INT",
+                    help="override a size of the workload (smaller cases for profiling)")
     args = ap.parse_args()
-    cfg = synth.get(args.workload)
+    over = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.set}
+    cfg = synth.scaled(args.workload, **over) if over else synth.get(args.workload)
     decode = cfg["kind"].endswith("decode")
     if args.steps is None:
         args.steps = 20000 if decode else 10
