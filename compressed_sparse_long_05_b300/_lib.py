@@ -42,6 +42,7 @@ _SIGS = {
     "csa_topk": [_P, _P, _I, _I, _I, _I, _I, _I, _P],
     "csa_attend": [_P, KV, _P, KV, _P, _P] + [_I] * 12 + [_F, _P, _Z, _P],
     "hca_attend": [_P, KV, KV, _P, _P] + [_I] * 11 + [_F, _P, _Z, _P],
+    "csa_attend_noalloc": [_P, KV, _P, KV, _P, _P] + [_I] * 12 + [_F, _P],
     "csa_attend_workspace_size": [_I] * 14,
     "csa_device_error": [_P],
     "csa_status_string": [_I],
@@ -172,6 +173,25 @@ def csa_attend(q, entries, idx, win, sink, m, n_win, win_base, q_pos0, r, rope_b
     _check("csa_attend", lib().csa_attend(
         _p(q), _kv(entries), _p(idx), _kv(win), _p(sink), _p(out), B, Tq, N, k, T_win, win_base,
         n_h, d, r, m, n_win, q_pos0, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
+    return out
+
+
+def csa_attend_noalloc(q, entries, idx, win, sink, m, n_win, win_base, q_pos0, r,
+                       rope_base=10000.0, out=None):
+    """csa_attend with its scratch in the library's fixed device array (no workspace).
+
+    For callers that must not allocate device memory beyond the output; see
+    include/csa.h for the size limit and the sharing rules of that array.
+    """
+    B, Tq, n_h, d = q.shape
+    _, N, _ = _rows_shape(entries)
+    _, T_win, _ = _rows_shape(win)
+    k = idx.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    _check("csa_attend_noalloc", lib().csa_attend_noalloc(
+        _p(q), _kv(entries), _p(idx), _kv(win), _p(sink), _p(out), B, Tq, N, k, T_win, win_base,
+        n_h, d, r, m, n_win, q_pos0, rope_base, _stream()))
     return out
 
 

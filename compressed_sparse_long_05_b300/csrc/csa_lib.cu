@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/csa.h"
 #include "common.cuh"
@@ -476,3 +477,59 @@ size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// csa_attend_noalloc: csa_attend for callers that cannot allocate device
+// memory.  Its scratch is one fixed array in this library's device image.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_attend_noalloc_scratch[CSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The array's
+// name in host code is only a host-side handle, so the address is looked up
+// once per device (with that device current) and cached.
+csa_status_t noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_attend_noalloc get device");
+  if (dev < 0 || dev >= kNoallocMaxDevices) return CSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attend_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_attend_noalloc scratch address");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return CSA_OK;
+}
+
+}  // namespace
+
+extern "C" csa_status_t csa_attend_noalloc(const void* q, csa_kv_t entries, const int32_t* idx,
+                                           csa_kv_t win, const float* sink, void* out, int B,
+                                           int Tq, int N, int k, int T_win, int win_base, int n_h,
+                                           int d, int r, int m, int n_win, int q_pos0,
+                                           float rope_base, void* stream) {
+  const size_t need = csa_attend_workspace_size(B, Tq, N, k, T_win, n_h, d, r, m, n_win, q_pos0,
+                                                CSA_DT_BF16, entries.dtype, 0);
+  if (need > CSA_NOALLOC_SCRATCH_BYTES) {
+    snprintf(g_cuda_msg, sizeof(g_cuda_msg),
+             "csa_attend_noalloc: these sizes need %zu scratch bytes, above the fixed %zu", need,
+             (size_t)CSA_NOALLOC_SCRATCH_BYTES);
+    return CSA_ERR_WORKSPACE;
+  }
+  void* ws = nullptr;
+  if (need > 0) {
+    const csa_status_t s = noalloc_scratch(&ws);
+    if (s != CSA_OK) return s;
+  }
+  return attend_common(q, entries, idx, win, sink, out, B, Tq, N, k, T_win, win_base, n_h, d, r,
+                       m, n_win, q_pos0, rope_base, ws, need > 0 ? (size_t)CSA_NOALLOC_SCRATCH_BYTES : 0,
+                       stream, 0);
+}

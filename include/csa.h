@@ -147,6 +147,38 @@ size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h
                                  int m, int n_win, int q_pos0, int q_dtype, int kv_dtype,
                                  int is_hca);
 
+/* ---------------------------------------------------------------------------
+ * csa_attend_noalloc — csa_attend without a caller-supplied workspace.  The
+ * pages define no such call; it exists for callers that cannot allocate
+ * device memory: code embedded in a host application or serving engine that
+ * owns every device allocation and hands this layer only its input and output
+ * buffers, and latency-critical callers that cannot take the implicit
+ * device-wide synchronisation of cudaMalloc / cudaFree.
+ *
+ * Arguments, layouts and results are those of csa_attend minus ws / ws_bytes.
+ * The scratch lives in one fixed array of CSA_NOALLOC_SCRATCH_BYTES in this
+ * library's device image: every GPU that loads the library holds it until
+ * the process exits.  This call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *   - Sizes whose scratch need (csa_attend_workspace_size) exceeds
+ *     CSA_NOALLOC_SCRATCH_BYTES return CSA_ERR_WORKSPACE before any launch
+ *     (csa_last_cuda_error() then gives both byte counts).  For scale: one
+ *     decode row per sequence at V4-Pro shape (n_h = 128, d = 512, k = 1024,
+ *     128K context) needs about 9.5 MB for 4 sequences on a 148-SM GPU.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  Nothing in it must start at zero (every scratch byte a call
+ *     reads, that call wrote first), but calls that overlap on the GPU (other
+ *     streams, other host threads) race on it: serialise them.
+ * ------------------------------------------------------------------------- */
+#define CSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+csa_status_t csa_attend_noalloc(const void* q, csa_kv_t entries, const int32_t* idx, csa_kv_t win,
+                                const float* sink, void* out, int B, int Tq, int N, int k,
+                                int T_win, int win_base, int n_h, int d, int r, int m, int n_win,
+                                int q_pos0, float rope_base, void* stream);
+
 /* Reads and clears the sticky device error word (synchronises `stream`).
  * Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE. */
 csa_status_t csa_device_error(void* stream);
