@@ -41,6 +41,47 @@ DEFAULT_WORKLOAD = "csa_decode_128k"
 L2_BYTES = 126 * 1024 * 1024
 
 
+def kernel_source_sha():
+    """First 12 hex digits of the sha256 over the kernel sources (csrc/*.cu, *.cuh)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "compressed_sparse_long_05_b300", "csrc", "*.cu*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(cfg, stage):
+    """DRAM bytes (read + write) per launch of `stage` from the committed ncu summaries.
+
+    Lines in profiles/*.md of the form
+        traffic <workload>[@T=<tokens>] <stage> <bytes> src=<sha>
+    hold the counters of one capture.  They count only while the kernel sources
+    still hash to <sha>; a capture of a shrunk prefill case (@T=...) is scaled
+    to this workload's T (q, out and the streamed inputs grow in proportion).
+    Returns (bytes or None, note).
+    """
+    import glob
+    sha = kernel_source_sha()
+    for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for line in open(f):
+            p = line.split()
+            if len(p) != 5 or p[0] != "traffic" or p[2] != stage or not p[4].startswith("src="):
+                continue
+            wl, _, at = p[1].partition("@")
+            if wl != cfg["name"].split("_T")[0] and wl != cfg["name"]:
+                continue
+            if p[4][4:] != sha:
+                return None, f"{os.path.basename(f)}: kernel sources changed since the capture"
+            nbytes = float(p[3])
+            if at:
+                k, v = at.split("=")
+                nbytes *= cfg[k] / int(v)
+                return int(nbytes), f"{os.path.basename(f)} (captured at {at}, scaled by {k})"
+            return int(nbytes), os.path.basename(f)
+    return None, "no capture of this kernel and workload"
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -355,16 +396,19 @@ def gpu_arm(args, cfg, rank, world):
     # roofline of the stage with the largest share of the step
     dom = max(stage_avg, key=stage_avg.get)
     b_dom, f_dom = wk[dom]
+    traffic, traffic_note = profiled_traffic(cfg, dom)
     if cfg["kind"].endswith("decode") or f_dom == 0:
         achieved = b_dom / (stage_avg[dom] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                "algorithmic_bytes": b_dom, "peak_source": peak_src}
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                "traffic_source": traffic_note, "algorithmic_bytes": b_dom,
+                "peak_source": peak_src + " (hbm_gbs, copy)"}
     else:
         achieved = f_dom / (stage_avg[dom] / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": tf_sust,
-                "unit": "TFLOP/s", "frac": round(achieved / tf_sust, 4), "traffic": None,
-                "algorithmic_flops": f_dom, "peak_source": peak_src + " (sustained)"}
+                "unit": "TFLOP/s", "frac": round(achieved / tf_sust, 4), "traffic": traffic,
+                "traffic_source": traffic_note, "algorithmic_flops": f_dom,
+                "algorithmic_bytes": b_dom, "peak_source": peak_src + " (bf16_tflops_sustained)"}
     kernels = {}
     for n in names:
         b, f = wk[n]
