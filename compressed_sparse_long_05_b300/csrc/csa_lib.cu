@@ -13,6 +13,7 @@
 #include "topk.cuh"
 #include "simt_f32.cuh"
 #include "index_tc.cuh"
+#include "index_fp4.cuh"
 #include "attend_tc.cuh"
 
 #include <cudaTypedefs.h>
@@ -82,6 +83,91 @@ bool tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, uint
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// 3-D byte tensor map (x fastest, 64-byte rows), 64-byte swizzle, zero fill.
+bool tmap_u8_3d_sw64(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, uint64_t z,
+                     uint64_t y_stride, uint64_t z_stride, uint32_t box_y) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {x, y, z};
+  cuuint64_t strides[2] = {y_stride, z_stride};
+  cuuint32_t box[3] = {(cuuint32_t)x, box_y, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 1-D map over `n` 8-byte elements (one element = the 8 scale bytes of a row).
+bool tmap_u64_1d(CUtensorMap* m, const void* base, uint64_t n, uint32_t box) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[1] = {n};
+  cuuint64_t strides[1] = {8};
+  cuuint32_t boxd[1] = {box};
+  cuuint32_t estr[1] = {1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 1, const_cast<void*>(base), dims, strides,
+                   boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Work split of the persistent index kernels: query groups of QT rows; when
+// there are fewer (batch row, group) pairs than SMs, the entry tiles of a
+// group are cut into chunks so that every SM streams part of K.
+csa_status_t plan_index(csa::IndexTcArgs& a, int QT, int B, int Tq, int N) {
+  a.QT = QT > Tq ? Tq : QT;
+  a.G = (Tq + a.QT - 1) / a.QT;
+  a.tiles_max = (N + csa::IDX_TILE - 1) / csa::IDX_TILE;
+  const int sms = sm_count();
+  if ((long long)B * a.G >= sms) {
+    a.chunk_tiles = a.tiles_max;
+  } else {
+    long long total = (long long)B * a.G * a.tiles_max;
+    a.chunk_tiles = (int)((total + sms - 1) / sms);
+    if (a.chunk_tiles < 1) a.chunk_tiles = 1;
+  }
+  a.chunks = (a.tiles_max + a.chunk_tiles - 1) / a.chunk_tiles;
+  long long items = (long long)B * a.G * a.chunks;
+  if (items > 0x7fffffff) return CSA_ERR_UNSUPPORTED;
+  a.items = (int)items;
+  return CSA_OK;
+}
+
+template <int H>
+csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w, const void* K,
+                              const void* K_sf, float* scores, int B, int Tq, int N, int m,
+                              int q_pos0, cudaStream_t stream) {
+  csa::IndexFp4Args fa;
+  memset(&fa, 0, sizeof(fa));
+  csa::IndexTcArgs& a = fa.t;
+  a.w = w; a.scores = scores; a.B = B; a.Tq = Tq; a.N = N; a.m = m; a.q_pos0 = q_pos0;
+  csa_status_t st = plan_index(a, 128 / H, B, Tq, N);
+  if (st != CSA_OK) return st;
+  if ((long long)B * N >= 0x7fffffffLL || (long long)B * Tq * H >= 0x7fffffffLL)
+    return CSA_ERR_UNSUPPORTED;
+  fa.sf_rows = (long long)B * N;
+  const int nqh = a.QT * H;
+  a.tmem_cols = 512;
+  CUtensorMap tmK, tmq, tmKs, tmqs;
+  if (!tmap_u8_3d_sw64(&tmK, K, csa::FP4_ROWB, N, B, csa::FP4_ROWB, (uint64_t)N * csa::FP4_ROWB,
+                       csa::IDX_TILE) ||
+      !tmap_u8_3d_sw64(&tmq, qI, csa::FP4_ROWB, (uint64_t)Tq * H, B, csa::FP4_ROWB,
+                       (uint64_t)Tq * H * csa::FP4_ROWB, nqh) ||
+      !tmap_u64_1d(&tmKs, K_sf, (uint64_t)B * N, csa::FP4_SF_BOX) ||
+      !tmap_u64_1d(&tmqs, qI_sf, (uint64_t)B * Tq * H, nqh))
+    return CSA_ERR_UNSUPPORTED;
+  const int smem = csa::IndexFp4Smem::BYTES;
+  auto kern = csa::index_fp4_kernel<H>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_index fp4 attr");
+  const int sms = sm_count();
+  const int grid = a.items < sms ? a.items : sms;
+  kern<<<grid, csa::IDX_THREADS, smem, stream>>>(tmK, tmq, tmKs, tmqs, fa);
+  CSA_CHECK_LAUNCH("csa_index fp4");
+  return CSA_OK;
 }
 
 template <int H, int C>
@@ -282,7 +368,20 @@ csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const 
       return launch_index_tc<128, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
-  (void)qI_sf; (void)K_sf;
+  if (dtype == CSA_DT_E2M1_BLOCK16) {
+    if (!qI_sf || !K_sf) return CSA_ERR_INVALID_ARG;
+    if (!aligned(qI, 16) || !aligned(K, 16) || !aligned(qI_sf, 16) || !aligned(K_sf, 16) ||
+        !aligned(w, 4) || !aligned(scores, 4))
+      return CSA_ERR_INVALID_ARG;
+    if (c != csa::FP4_C) return CSA_ERR_UNSUPPORTED;
+    if (H == 64)
+      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, S(stream));
+    if (H == 32)
+      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, S(stream));
+    if (H == 128)
+      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, S(stream));
+    return CSA_ERR_UNSUPPORTED;
+  }
   return CSA_ERR_UNSUPPORTED;
 }
 

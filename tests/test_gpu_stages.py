@@ -284,3 +284,76 @@ def test_attend_bf16_heads_64(K):
     N = 500
     _attend_case(K, B=1, Tq=3, N=N, k=128, q_pos0=4 * N - 3, T_win=140, win_base=4 * N - 140,
                  n_h=64, seed=110)
+
+
+# ----------------------------------------------------------------------------
+# index (FP4 e2m1 + e4m3 block scales, block-scaled tcgen05 path)
+# ----------------------------------------------------------------------------
+
+
+def _fp4(shape, seed, scale):
+    from synth.generate import quantise_fp4_blocks
+    g = torch.Generator().manual_seed(seed)
+    v = torch.randn(shape, generator=g) * scale
+    packed, sf = quantise_fp4_blocks(v)
+    return packed.to(DEV), sf.to(DEV)
+
+
+@pytest.mark.parametrize("B,Tq,N,H,q_pos0", [
+    (2, 1, 5000, 64, 19999),      # decode rows, ragged last tile
+    (3, 3, 1001, 64, 3999),       # odd N: scale rows of batch row 1 start on an odd row
+    (1, 300, 257, 64, 0),         # causal prefill, vis < one tile for most rows
+    (1, 7, 700, 128, 2790),       # H = 128
+    (1, 9, 640, 32, 2550),        # H = 32, four queries per group
+])
+def test_index_fp4(K, B, Tq, N, H, q_pos0):
+    m, c = 4, 128
+    q_p, q_sf = _fp4((B, Tq, H, c), 44, c ** -0.5)
+    k_p, k_sf = _fp4((B, N, c), 45, c ** -0.5)
+    w = torch.rand((B, Tq, H), generator=_gen(46), device=DEV) / H
+    s = K.csa_index(q_p, w, k_p, m, q_pos0, qI_sf=q_sf, K_sf=k_sf)
+    torch.cuda.synchronize()
+    K.device_error()
+    for b in range(B):
+        qd = O.decode_fp4_blocks(q_p[b].cpu().numpy(), q_sf[b].cpu().numpy())
+        kd = O.decode_fp4_blocks(k_p[b].cpu().numpy(), k_sf[b].cpu().numpy())
+        ref = O.index_scores(qd, f64(w[b]), kd, q_pos0 + np.arange(Tq), m)
+        got = f64(s[b])
+        for i in range(Tq):
+            assert_scores_close(got[i], ref[i], f"b={b} row {i}")
+
+
+# ----------------------------------------------------------------------------
+# attention over FP8 (e4m3 + per-row scale) / BF16-RoPE rows
+# ----------------------------------------------------------------------------
+
+
+def _mixed(rows_bf16):
+    from synth.generate import quantise_mixed_entries
+    return quantise_mixed_entries(rows_bf16.float(), 64)
+
+
+@pytest.mark.parametrize("B,Tq,N,k,split", [(2, 1, 3000, 1024, True), (1, 40, 2000, 256, False)])
+def test_attend_mixed_rows(K, B, Tq, N, k, split):
+    from tests.parity import TOL_MIXED
+    d, r, n_h, m, n_win = 512, 64, 128, 4, 128
+    q_pos0 = 4 * N - Tq
+    T_win = n_win + Tq
+    win_base = 4 * N - T_win
+    q = _rms((B, Tq, n_h, d), 120)
+    ent = _mixed(_rms((B, N, d), 121))
+    win = _mixed(_rms((B, T_win, d), 122))
+    sink = torch.randn((n_h,), generator=_gen(123), device=DEV)
+    scores = torch.rand((B, Tq, N), generator=_gen(124), device=DEV)
+    idx = K.csa_topk(scores, k, m, q_pos0)
+    out = K.csa_attend(q, ent, idx, win, sink, m, n_win, win_base, q_pos0, r)
+    torch.cuda.synchronize()
+    K.device_error()
+    for b in range(B):
+        e64 = O.decode_mixed_entries(ent[0][b].cpu().numpy(), ent[1][b].cpu().numpy(), f64(ent[2][b]))
+        w64 = O.decode_mixed_entries(win[0][b].cpu().numpy(), win[1][b].cpu().numpy(), f64(win[2][b]))
+        for i in sorted({0, Tq // 2, Tq - 1}):
+            t = q_pos0 + i
+            ref = O.csa_attend_token(f64(q[b, i]), t, e64, idx[b, i].cpu().numpy(), w64, win_base,
+                                     f64(sink), m, n_win, r, 1e4)
+            assert_close(f64(out[b, i]), ref, TOL_MIXED, TOL_MIXED, f"b={b} i={i}")
