@@ -46,7 +46,7 @@ constexpr int ATT_D = 512;
 constexpr int ATT_R = 64;
 constexpr int ATT_HG = 64;          // heads per CTA
 constexpr int ATT_TILE = 128;       // rows per tile
-constexpr int ATT_LAG = 3;          // cp.async chunk groups in flight per gather warp
+constexpr int ATT_LAG = 6;          // cp.async chunk groups in flight per gather warp
 constexpr float ATT_TAU = 8.0f;     // lazy-rescale threshold (log2 units)
 
 struct AttendTcArgs {
@@ -60,7 +60,7 @@ struct AttendTcArgs {
   const int32_t* idx;            // [B, Tq, k] or null (dense)
   const float* sink;             // [n_h]
   __nv_bfloat16* out;            // [B, Tq, n_h, 512]
-  float* part_o;                 // [items][64][512] (split mode)
+  float* part_o;                 // [items][512 dims][64 heads] (split mode)
   float* part_ml;                // [items][64][2]   (split mode)
   int B, Tq, N, k, T_win, win_base, n_h, m, n_win, q_pos0;
   int HG;                        // head groups = n_h / 64
@@ -68,6 +68,8 @@ struct AttendTcArgs {
   int chunk_rows;                // rows per chunk (multiple of 128)
   int items;                     // B * Tq * HG * nch
   int rotate_rows;               // 1 = rotate gathered rows in shared memory
+  int rel_rope;                  // 1 = rows rotated by (position - t): q and out stay unrotated
+  int tma_rows;                  // 1 = bf16 rows gathered by TMA (tile::gather4), 4-row groups
   int kv_mixed;                  // 1 = e4m3 + scale + bf16 rope rows
   float scale_log2;              // log2(e) / sqrt(d)
   RopeFreqs rf;
@@ -93,6 +95,7 @@ struct AttRow {
   int b, i, hg, c;
   long long t;
   int nsel;        // compressed rows (selected or visible)
+  int nsel4;       // row index where the window starts (nsel, rounded up to 4 for TMA groups)
   long long w0;    // first window token
   int nrows;       // nsel + window size
   int r0, r1;      // this chunk's rows [r0, r1)
@@ -113,7 +116,8 @@ CSA_DEVINL AttRow att_item(const AttendTcArgs& a, int it) {
   x.nsel = a.idx ? (int)min((long long)a.k, vis) : (int)vis;
   x.w0 = x.t - a.n_win + 1;
   if (x.w0 < 0) x.w0 = 0;
-  x.nrows = x.nsel + (int)(x.t - x.w0 + 1);
+  x.nsel4 = a.tma_rows ? ((x.nsel + 3) & ~3) : x.nsel;
+  x.nrows = x.nsel4 + (int)(x.t - x.w0 + 1);
   x.r0 = min(x.nrows, x.c * a.chunk_rows);
   x.r1 = min(x.nrows, x.r0 + a.chunk_rows);
   return x;
@@ -133,6 +137,18 @@ CSA_DEVINL void tmem_st32(uint32_t taddr, const uint32_t* r) {
 }
 CSA_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// four rows (arbitrary row coordinates) x one 128-byte box of a 2-D tensor map,
+// landing as four consecutive 128-byte rows with the map's swizzle
+CSA_DEVINL void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int r0, int r1,
+                            int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 CSA_DEVINL void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0)
@@ -141,6 +157,19 @@ CSA_DEVINL void cp_async16(uint32_t dst, const void* src, bool valid) {
 CSA_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 CSA_DEVINL void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// wait until at most n (0..7) of this thread's cp.async groups are pending
+CSA_DEVINL void cp_async_wait_n(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+  }
+}
 
 // rotate the 4 (x0, x1) pairs of one 16-byte bf16 unit; pair p uses frequency j0 + p
 CSA_DEVINL uint4 rope_unit(uint4 v, long long pos, const RopeFreqs& rf, int j0) {
@@ -196,7 +225,9 @@ CSA_DEVINL uint4 load_mixed_unit(const uint8_t* nope_row, float scale,
   return __ldg(reinterpret_cast<const uint4*>(rope_row + (unit - (ATT_D - ATT_R) / 8) * 8));
 }
 
-__global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendTcArgs a) {
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ent,
+                 const __grid_constant__ CUtensorMap tm_win, const AttendTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sE = smem + AttSmem::E;
@@ -220,6 +251,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
   uint64_t* grp_a = bar + 21;        // softmax warps: tile max partials (count 4)
   uint64_t* grp_b = bar + 22;        // softmax warps: sum partials (count 4)
   uint64_t* mma_done = bar + 23;
+  uint64_t* c7_full = bar + 24;      // [4] per gather warp: its chunk-7 rows landed (TMA, RoPE after)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttSmem::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttSmem::MISC + 4);
 
@@ -231,12 +263,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
     for (int s = 0; s < 2; ++s) { mbar_init(s_full + s, 1); mbar_init(s_free + s, 4); }
     mbar_init(p_full, 4);
     mbar_init(p_free, 1);
-    mbar_init(q_full, 4);
+    mbar_init(q_full, a.rel_rope ? 1 : 4);
     mbar_init(q_free, 1);
     mbar_init(o_free, 4);
     mbar_init(grp_a, 4);
     mbar_init(grp_b, 4);
     mbar_init(mma_done, 1);
+    for (int w = 0; w < 4; ++w) mbar_init(c7_full + w, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -248,6 +281,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
   const uint32_t TM_O = 0, TM_S = 256;     // O^T blocks at 0..255, S^T buffers at 256..383
 
   if (warp >= 4 && warp < 8) {
@@ -259,9 +293,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
       const AttRow x = att_item(a, it);
       if (x.r1 <= x.r0) continue;
       // ---- queries of this head group, RoPE at t, swizzled K-major [64 heads][512] ----
-      if (!mbar_wait(q_free, (nitem & 1) ^ 1, abort_flag)) { ok = false; break; }
-      ++nitem;
-      {
+      // (relative-RoPE mode: the MMA warp loads them unrotated by TMA)
+      if (!a.rel_rope) {
+        if (!mbar_wait(q_free, (nitem & 1) ^ 1, abort_flag)) { ok = false; break; }
+        ++nitem;
         const __nv_bfloat16* qrow0 =
             a.q + (((size_t)x.b * a.Tq + x.i) * a.n_h + (size_t)x.hg * ATT_HG + gw * 16) * ATT_D;
 #pragma unroll 4
@@ -283,6 +318,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
         // this lane's row: tile row gw*32 + lane
         const int rr = r0 + gw * 32 + lane;
         const uint8_t* src = nullptr;        // bf16 row, or e4m3 nope row
+        int trow = -1;                       // row of the entry / window tensor map (TMA mode)
         const __nv_bfloat16* rsrc = nullptr; // mixed: rope row
         float rscale = 0.f;
         long long pos = 0;
@@ -292,6 +328,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
             if (s >= a.N) { csa_flag_error(ERRBIT_BAD_INDEX); s = -1; }
             if (s >= 0) {
               const size_t row = (size_t)x.b * a.N + s;
+              trow = (int)row;
               if (a.kv_mixed) {
                 src = reinterpret_cast<const uint8_t*>(a.ent) + row * (ATT_D - ATT_R);
                 rsrc = a.ent_rope + row * ATT_R;
@@ -301,9 +338,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
               }
               pos = (long long)a.m * (s + 1) - 1;
             }
-          } else {
-            const long long tok = x.w0 + (rr - x.nsel);
+          } else if (rr >= x.nsel4) {
+            const long long tok = x.w0 + (rr - x.nsel4);
             const size_t row = (size_t)x.b * a.T_win + (size_t)(tok - a.win_base);
+            trow = (int)row;
             if (a.kv_mixed) {
               src = reinterpret_cast<const uint8_t*>(a.win) + row * (ATT_D - ATT_R);
               rsrc = a.win_rope + row * ATT_R;
@@ -318,6 +356,70 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
         {
           const uint32_t bits = __ballot_sync(0xffffffffu, src != nullptr);
           if (lane == 0) rmask[(n & 1) * 4 + gw] = bits;
+        }
+        if (a.tma_rows) {
+          // TMA: 8 groups of 4 rows per warp and 64-dim chunk.  Groups are pure
+          // (entries end at nsel4, a multiple of 4); invalid rows read row 0 of
+          // their region and are masked above.
+          const int wrow0 = r0 + gw * 32;
+          const int coord = trow >= 0 ? trow : (wrow0 + lane >= x.nsel4 ? x.b * a.T_win : x.b * a.N);
+          int cr[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) cr[j] = __shfl_sync(0xffffffffu, coord, j);
+          if (r0 == x.r0) {
+            // first tile of the item: every chunk pair is free once the last PV of
+            // the previous item is done; fetch each row's 1 KB together
+            for (int c2 = 0; c2 < 4 && ok; ++c2)
+              if (!mbar_wait(chunk_free + c2, (n & 1) ^ 1, abort_flag)) ok = false;
+            if (!ok) break;
+            if (lane == 0) {
+              for (int c = 0; c < 8; ++c)
+                mbar_arrive_expect_tx((c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, 32 * 128);
+              for (int g = 0; g < 8; ++g) {
+                const CUtensorMap* map = wrow0 + 4 * g >= x.nsel4 ? &tm_win : &tm_ent;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  tma_gather4(sE + c * 16384 + (gw * 32 + 4 * g) * 128, map,
+                              (c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, c * 64,
+                              cr[4 * g], cr[4 * g + 1], cr[4 * g + 2], cr[4 * g + 3]);
+              }
+            }
+            __syncwarp();
+          } else {
+            // later tiles: each chunk pair as soon as the PV block that read it is done
+            for (int c = 0; c < 8 && ok; ++c) {
+              if ((c & 1) == 0 && !mbar_wait(chunk_free + (c >> 1), (n & 1) ^ 1, abort_flag)) { ok = false; break; }
+              uint64_t* bar_c = (c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c;
+              if (lane == 0) {
+                mbar_arrive_expect_tx(bar_c, 32 * 128);
+                uint8_t* dst = sE + c * 16384 + gw * 32 * 128;
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                  tma_gather4(dst + g * 512, wrow0 + 4 * g >= x.nsel4 ? &tm_win : &tm_ent, bar_c, c * 64,
+                              cr[4 * g], cr[4 * g + 1], cr[4 * g + 2], cr[4 * g + 3]);
+              }
+              __syncwarp();
+            }
+            if (!ok) break;
+          }
+          if (a.rotate_rows) {
+            // RoPE of this warp's 32 rows once its chunk 7 (dims 448..511) has landed
+            if (!mbar_wait(c7_full + gw, n & 1, abort_flag)) { ok = false; break; }
+            uint8_t* c7 = sE + 7 * 16384;
+#pragma unroll 2
+            for (int k2 = 0; k2 < 8; ++k2) {
+              const int rl = k2 * 4 + (lane >> 3);
+              const int u = lane & 7;
+              const long long p = __shfl_sync(0xffffffffu, pos, rl) - (a.rel_rope ? x.t : 0);
+              const int tr = gw * 32 + rl;
+              uint4* ptr = reinterpret_cast<uint4*>(c7 + tr * 128 + ((u ^ (tr & 7)) << 4));
+              *ptr = rope_unit(*ptr, p, a.rf, u * 4);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(chunk_full + 7);
+          }
+          continue;
         }
         for (int c = 0; c < 8 && ok; ++c) {
           if ((c & 1) == 0 && !mbar_wait(chunk_free + (c >> 1), (n & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -353,6 +455,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
           }
         }
         if (!ok) break;
+        // release the remaining chunks as they land; chunk 7 (the RoPE dims) last
+        for (int c = 8 - ATT_LAG; c < 7; ++c) {
+          cp_async_wait_n(7 - c);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(chunk_full + c);
+        }
         cp_async_wait<0>();
         __syncwarp();
         if (a.rotate_rows) {
@@ -362,7 +471,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
           for (int k2 = 0; k2 < 8; ++k2) {
             const int rl = k2 * 4 + (lane >> 3);
             const int u = lane & 7;
-            const long long p = __shfl_sync(0xffffffffu, pos, rl);
+            const long long p = __shfl_sync(0xffffffffu, pos, rl) - (a.rel_rope ? x.t : 0);
             const int tr = gw * 32 + rl;
             uint4* ptr = reinterpret_cast<uint4*>(c7 + tr * 128 + ((u ^ (tr & 7)) << 4));
             *ptr = rope_unit(*ptr, p, a.rf, u * 4);
@@ -370,8 +479,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
         }
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0)
-          for (int c = 8 - ATT_LAG; c < 8; ++c) mbar_arrive(chunk_full + c);
+        if (lane == 0) mbar_arrive(chunk_full + 7);
       }
     }
   } else if (warp == 8) {
@@ -385,6 +493,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
       for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
         const AttRow x = att_item(a, it);
         if (x.r1 <= x.r0) continue;
+        if (a.rel_rope) {
+          // queries of this head group: 8 boxes of [64 heads x 64 dims], 128-byte swizzled
+          if (!mbar_wait(q_free, (nitem & 1) ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(q_full, ATT_HG * ATT_D * 2);
+          const int qrow = (x.b * a.Tq + x.i) * a.n_h + x.hg * ATT_HG;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) tma_load_3d(sQ + c * 8192, &tm_q, q_full, c * 64, qrow, 0);
+        }
         if (!mbar_wait(q_full, nitem & 1, abort_flag)) { ok = false; break; }
         const uint32_t item = nitem++;
         int j = 0;
@@ -579,27 +695,35 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
         const int dim = bk * 128 + q4 * 32 + lane;
         float c = 1.f, s = 0.f;
         const bool rope_dim = dim >= ATT_D - ATT_R;
-        if (single && rope_dim) rope_cos_sin(-x.t, a.rf.F[(dim - (ATT_D - ATT_R)) >> 1], c, s);
+        const bool rot_out = single && rope_dim && !a.rel_rope;
+        if (rot_out) rope_cos_sin(-x.t, a.rf.F[(dim - (ATT_D - ATT_R)) >> 1], c, s);
+        uint32_t r2[64];
+        if (j > 0) {
+          tmem_ld32(tmem + lane_base + TM_O + bk * ATT_HG, r2);
+          tmem_ld32(tmem + lane_base + TM_O + bk * ATT_HG + 32, r2 + 32);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) r2[e] = 0u;
+        }
 #pragma unroll
         for (int hh = 0; hh < 64; hh += 32) {
-          uint32_t r[32];
-          if (j > 0) {
-            tmem_ld32(tmem + lane_base + TM_O + bk * ATT_HG + hh, r);
-            tmem_ld_wait();
-          } else {
+          const uint32_t* r = r2 + hh;
+          if (single) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = 0u;
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float v = __uint_as_float(r[e]) * my_f[hh + e];
-            if (single) {
+            for (int e = 0; e < 32; ++e) {
+              float v = __uint_as_float(r[e]) * my_f[hh + e];
               const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
-              if (rope_dim) v = (lane & 1) ? (pv * s + v * c) : (v * c - pv * s);
+              if (rot_out) v = (lane & 1) ? (pv * s + v * c) : (v * c - pv * s);
               a.out[(orow + hh + e) * ATT_D + dim] = __float2bfloat16_rn(v);
-            } else {
-              a.part_o[((size_t)it * ATT_HG + hh + e) * ATT_D + dim] = v;
             }
+          } else {
+            // unnormalised partial, layout [item][dim][64 heads]
+            float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)it * ATT_D + dim) * ATT_HG + hh);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              dst[e >> 2] = make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                        __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
           }
         }
       }
@@ -617,53 +741,81 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attend_tc_kernel(const AttendT
 
 // ----------------------------------------------------------------------------
 // split-chunk combine: out[b,i,h,:] = sum_c 2^(m_c - M) O_c / (sum_c 2^(m_c - M) l_c
-// + 2^(z'_h log2 e - M)), then the RoPE dims rotated back by -t.
+// + 2^(z'_h log2 e - M)), then (absolute-RoPE mode) the RoPE dims rotated back by -t.
+// Partials are [chunk][dim][64 heads] f32.  One CTA per (query row, head group,
+// 8 output dims): it reads one coalesced 2 KB [8 dims x 64 heads] slice per
+// chunk and writes one 16-byte bf16 run per head.
 // ----------------------------------------------------------------------------
 struct CombineArgs {
   const float* part_o; const float* part_ml; const float* sink;
   __nv_bfloat16* out;
   int Tq, n_h, HG, nch, q_pos0;
+  int rel_rope;       // 1 = output already relative to t (no rotation)
   RopeFreqs rf;
 };
 
-__global__ void __launch_bounds__(128) attend_combine_kernel(const CombineArgs a) {
-  const int row = blockIdx.x;                   // (b * Tq + i) * n_h + h
-  const int h = row % a.n_h;
-  const int bi = row / a.n_h;
+constexpr int CMB_THREADS = 128;
+constexpr int CMB_DIMS = 8;                        // output dims per CTA
+
+__global__ void __launch_bounds__(CMB_THREADS) attend_combine_kernel(const CombineArgs a) {
+  pdl_enter();
+  extern __shared__ float cmb_w[];                 // [nch][64] chunk weights
+  __shared__ float tile[ATT_HG][CMB_DIMS + 1];
+  const int db = (blockIdx.x % (ATT_D / CMB_DIMS)) * CMB_DIMS;
+  const int unit = blockIdx.x / (ATT_D / CMB_DIMS);   // (b * Tq + i) * HG + hg
+  const int hg = unit % a.HG;
+  const int bi = unit / a.HG;
   const int i = bi % a.Tq;
-  const int hg = h / ATT_HG, hl = h % ATT_HG;
-  const size_t it0 = ((size_t)bi * a.HG + hg) * a.nch;
-  const float zs = __ldg(a.sink + h) * 1.4426950408889634f;
-  float M = zs;
-  for (int c = 0; c < a.nch; ++c) M = fmaxf(M, __ldg(a.part_ml + ((it0 + c) * ATT_HG + hl) * 2));
-  float den = exp2f(zs - M);
-  const int d0 = threadIdx.x * 4;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c = 0; c < a.nch; ++c) {
-    const float* ml = a.part_ml + ((it0 + c) * ATT_HG + hl) * 2;
-    const float mc = __ldg(ml);
-    if (mc == -INFINITY) continue;
-    const float wgt = exp2f(mc - M);
-    den += __ldg(ml + 1) * wgt;
-    const float4 o = __ldg(reinterpret_cast<const float4*>(a.part_o + ((it0 + c) * ATT_HG + hl) * ATT_D + d0));
-    acc[0] += o.x * wgt; acc[1] += o.y * wgt; acc[2] += o.z * wgt; acc[3] += o.w * wgt;
-  }
-  const float inv = 1.f / den;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) acc[e] *= inv;
-  if (d0 >= ATT_D - ATT_R) {
-    const long long t = (long long)a.q_pos0 + i;
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      float c, s;
-      rope_cos_sin(-t, a.rf.F[((d0 - (ATT_D - ATT_R)) >> 1) + p], c, s);
-      const float x0 = acc[2 * p], x1 = acc[2 * p + 1];
-      acc[2 * p] = x0 * c - x1 * s;
-      acc[2 * p + 1] = x0 * s + x1 * c;
+  const size_t it0 = (size_t)unit * a.nch;
+  const int tid = threadIdx.x;
+  if (tid < ATT_HG) {
+    const int h = tid;
+    const float* ml = a.part_ml + (it0 * ATT_HG + h) * 2;
+    const float zs = __ldg(a.sink + hg * ATT_HG + h) * 1.4426950408889634f;
+    float M = zs;
+    for (int c = 0; c < a.nch; ++c) M = fmaxf(M, __ldg(ml + (size_t)c * ATT_HG * 2));
+    float den = exp2f(zs - M);
+    for (int c = 0; c < a.nch; ++c) {
+      const float mc = __ldg(ml + (size_t)c * ATT_HG * 2);
+      if (mc != -INFINITY) den += __ldg(ml + (size_t)c * ATT_HG * 2 + 1) * exp2f(mc - M);
+    }
+    const float inv = 1.f / den;
+    for (int c = 0; c < a.nch; ++c) {
+      const float mc = __ldg(ml + (size_t)c * ATT_HG * 2);
+      cmb_w[c * ATT_HG + h] = mc == -INFINITY ? 0.f : exp2f(mc - M) * inv;
     }
   }
-  __nv_bfloat16* o = a.out + (size_t)row * ATT_D + d0;
-  *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+  __syncthreads();
+  // thread: dim db + tid / 16, heads 4 (tid % 16) .. + 3
+  const int dl = tid >> 4, hq = (tid & 15) * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* src = a.part_o + (it0 * ATT_D + db + dl) * ATT_HG + hq;
+  for (int c = 0; c < a.nch; ++c) {
+    const float4 w4 = *reinterpret_cast<const float4*>(cmb_w + c * ATT_HG + hq);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src + (size_t)c * ATT_D * ATT_HG));
+    acc.x += v.x * w4.x; acc.y += v.y * w4.y; acc.z += v.z * w4.z; acc.w += v.w * w4.w;
+  }
+  tile[hq][dl] = acc.x; tile[hq + 1][dl] = acc.y; tile[hq + 2][dl] = acc.z; tile[hq + 3][dl] = acc.w;
+  __syncthreads();
+  if (tid < ATT_HG) {
+    const int h = tid;
+    float v[CMB_DIMS];
+#pragma unroll
+    for (int k = 0; k < CMB_DIMS; ++k) v[k] = tile[h][k];
+    if (!a.rel_rope && db >= ATT_D - ATT_R) {
+      const long long t = (long long)a.q_pos0 + i;
+#pragma unroll
+      for (int p = 0; p < CMB_DIMS / 2; ++p) {
+        float cs, sn;
+        rope_cos_sin(-t, a.rf.F[((db - (ATT_D - ATT_R)) >> 1) + p], cs, sn);
+        const float x0 = v[2 * p], x1 = v[2 * p + 1];
+        v[2 * p] = x0 * cs - x1 * sn;
+        v[2 * p + 1] = x0 * sn + x1 * cs;
+      }
+    }
+    __nv_bfloat16* o = a.out + ((size_t)bi * a.n_h + (size_t)hg * ATT_HG + h) * ATT_D + db;
+    *reinterpret_cast<uint4*>(o) = f_to_bf16x8(v);
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -680,6 +832,7 @@ struct RotateArgs {
 };
 
 __global__ void __launch_bounds__(256) rope_rotate_rows_kernel(const RotateArgs a) {
+  pdl_enter();
   // one thread per 16-byte unit; 64 units per 512-dim row
   const long long u_all = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u_all >= a.rows * 64) return;

@@ -19,6 +19,14 @@ enum : unsigned int {
 
 CSA_DEVINL void csa_flag_error(unsigned int bit) { atomicOr(&g_csa_error_word, bit); }
 
+// Programmatic dependent launch.  Every kernel lets the next launch in the
+// stream start as early as possible (its prologue overlaps this grid's tail),
+// and waits for the previous grid to complete and flush before its first global
+// memory access.  Without a programmatic predecessor the wait returns at once.
+CSA_DEVINL void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+CSA_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+CSA_DEVINL void pdl_enter() { pdl_launch_dependents(); pdl_wait(); }
+
 // ----------------------------------------------------------------------------
 // numeric helpers
 // ----------------------------------------------------------------------------
@@ -61,8 +69,9 @@ CSA_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
 // uint64.  For an integer position p the rotation phase in revolutions is
 // p * F_j / 2^64 modulo 1, which unsigned 64-bit multiplication gives exactly
 // (wrap-around is the modulo).  The top bits, read as a signed fraction in
-// [-1/2, 1/2), feed sincospif, so the angle stays accurate to ~2^-24
-// revolutions at any position up to 2^40.
+// [-1/2, 1/2), give an angle in [-pi, pi) that the fast hardware sine/cosine
+// evaluate to about 1e-6 absolute, so the angle stays accurate at any position
+// up to 2^40 (plain fp32 p * theta would be off by up to 0.06 rad at 2^20).
 // ----------------------------------------------------------------------------
 struct RopeFreqs {
   unsigned long long F[64];  // one per rotated pair; r/2 <= 64
@@ -70,9 +79,9 @@ struct RopeFreqs {
 };
 
 CSA_DEVINL void rope_cos_sin(long long pos, unsigned long long F, float& c, float& s) {
-  unsigned long long ph = (unsigned long long)pos * F;
-  float rev = (float)((long long)ph >> 40) * 5.9604644775390625e-8f;  // * 2^-24
-  sincospif(2.0f * rev, &s, &c);
+  const unsigned long long ph = (unsigned long long)pos * F;
+  const float rev = (float)((long long)ph >> 40) * 5.9604644775390625e-8f;  // * 2^-24
+  __sincosf(6.283185307179586f * rev, &s, &c);
 }
 
 // ----------------------------------------------------------------------------

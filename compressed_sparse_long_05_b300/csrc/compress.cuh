@@ -49,6 +49,7 @@ struct CompressArgs {
 
 template <typename T>
 __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
+  pdl_enter();
   using V = VecTraits<T>;
   constexpr int VEC = V::N;
   const int i = blockIdx.x;            // entry

@@ -11,6 +11,7 @@
 #include "common.cuh"
 #include "compress.cuh"
 #include "topk.cuh"
+#include "topk2.cuh"
 #include "simt_f32.cuh"
 #include "index_tc.cuh"
 #include "index_fp4.cuh"
@@ -70,6 +71,42 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
+
+// Programmatic stream serialisation would let a kernel start while the previous
+// kernel in the stream finishes (every kernel here waits on the grid dependency
+// before its first global memory access, so either setting is correct).  Off:
+// measured in CUDA-graph replay of the decode and prefill steps, the early-
+// launched grids made each step slower (decode 128K: 69 vs 59 us per step).
+constexpr bool kProgrammaticLaunch = false;
+
+// Launch with an optional cluster size (and programmatic serialisation when on).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      int cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (kProgrammaticLaunch) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // 3-D bf16 tensor map (x fastest), 128-byte swizzle, zero fill out of bounds.
 bool tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, uint64_t z,
                   uint64_t y_stride_bytes, uint64_t z_stride_bytes, uint32_t box_x, uint32_t box_y) {
@@ -100,6 +137,21 @@ bool tmap_u8_3d_sw64(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, u
   return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over `rows` rows of 512 elements for tile::gather4: box of one
+// row x 64 elements (128 bytes), 128-byte swizzle.
+bool tmap_bf16_rows(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)csa::ATT_D, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)csa::ATT_D * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 1-D map over `n` 8-byte elements (one element = the 8 scale bytes of a row).
 bool tmap_u64_1d(CUtensorMap* m, const void* base, uint64_t n, uint32_t box) {
   auto enc = tmap_encoder();
@@ -122,15 +174,17 @@ csa_status_t plan_index(csa::IndexTcArgs& a, int QT, int B, int Tq, int N) {
   a.G = (Tq + a.QT - 1) / a.QT;
   a.tiles_max = (N + csa::IDX_TILE - 1) / csa::IDX_TILE;
   const int sms = sm_count();
-  if ((long long)B * a.G >= sms) {
+  const long long units = (long long)B * a.G;
+  if (units >= sms) {
     a.chunk_tiles = a.tiles_max;
   } else {
-    long long total = (long long)B * a.G * a.tiles_max;
-    a.chunk_tiles = (int)((total + sms - 1) / sms);
+    // at most `sms` items: floor(sms / units) chunks per unit, so no SM takes two
+    const long long per_unit = sms / units;
+    a.chunk_tiles = (int)((a.tiles_max + per_unit - 1) / per_unit);
     if (a.chunk_tiles < 1) a.chunk_tiles = 1;
   }
   a.chunks = (a.tiles_max + a.chunk_tiles - 1) / a.chunk_tiles;
-  long long items = (long long)B * a.G * a.chunks;
+  long long items = units * a.chunks;
   if (items > 0x7fffffff) return CSA_ERR_UNSUPPORTED;
   a.items = (int)items;
   return CSA_OK;
@@ -165,8 +219,8 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
   if (e != cudaSuccess) return cuda_fail(e, "csa_index fp4 attr");
   const int sms = sm_count();
   const int grid = a.items < sms ? a.items : sms;
-  kern<<<grid, csa::IDX_THREADS, smem, stream>>>(tmK, tmq, tmKs, tmqs, fa);
-  CSA_CHECK_LAUNCH("csa_index fp4");
+  e = launch_ex(kern, dim3(grid), dim3(csa::IDX_THREADS), smem, stream, 1, tmK, tmq, tmKs, tmqs, fa);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_index fp4 launch");
   return CSA_OK;
 }
 
@@ -175,22 +229,9 @@ csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, floa
                              int Tq, int N, int m, int q_pos0, cudaStream_t stream) {
   csa::IndexTcArgs a;
   a.w = w; a.scores = scores; a.B = B; a.Tq = Tq; a.N = N; a.m = m; a.q_pos0 = q_pos0;
-  a.QT = 256 / H;
-  if (a.QT > Tq) a.QT = Tq;
-  a.G = (Tq + a.QT - 1) / a.QT;
-  a.tiles_max = (N + csa::IDX_TILE - 1) / csa::IDX_TILE;
+  csa_status_t st = plan_index(a, 256 / H, B, Tq, N);
+  if (st != CSA_OK) return st;
   const int sms = sm_count();
-  if ((long long)B * a.G >= sms) {
-    a.chunk_tiles = a.tiles_max;
-  } else {
-    long long total = (long long)B * a.G * a.tiles_max;
-    a.chunk_tiles = (int)((total + sms - 1) / sms);
-    if (a.chunk_tiles < 1) a.chunk_tiles = 1;
-  }
-  a.chunks = (a.tiles_max + a.chunk_tiles - 1) / a.chunk_tiles;
-  long long items = (long long)B * a.G * a.chunks;
-  if (items > 0x7fffffff) return CSA_ERR_UNSUPPORTED;
-  a.items = (int)items;
   const int nqh = a.QT * H;
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * nqh)) cols <<= 1;
@@ -200,19 +241,20 @@ csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, floa
       !tmap_bf16_3d(&tmq, qI, C, (uint64_t)Tq * H, B, (uint64_t)C * 2, (uint64_t)Tq * H * C * 2,
                     64, nqh))
     return CSA_ERR_UNSUPPORTED;
-  const int smem = csa::IndexSmem<H, C>::BYTES;
+  a.stages = csa::IndexSmem<H, C>::stages_for(nqh);
+  const int smem = csa::IndexSmem<H, C>(a.stages, nqh).BYTES;
   auto kern = csa::index_tc_kernel<H, C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "csa_index tc attr");
   const int grid = a.items < sms ? a.items : sms;
-  kern<<<grid, csa::IDX_THREADS, smem, stream>>>(tmK, tmq, a);
-  CSA_CHECK_LAUNCH("csa_index tc");
+  e = launch_ex(kern, dim3(grid), dim3(csa::IDX_THREADS), smem, stream, 1, tmK, tmq, a);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_index tc launch");
   return CSA_OK;
 }
 
 // Work split and scratch layout of the tensor-core attention path.
 struct AttPlan {
-  int HG, nch, chunk_rows, items, rotate_rows;
+  int HG, nch, chunk_rows, items, rotate_rows, rel_rope;
   size_t off_part_o, off_part_ml, off_rot_ent, off_rot_win, bytes;
 };
 
@@ -228,7 +270,8 @@ AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int m, int 
   if (vis > N) vis = N;
   const long long nsel = dense ? vis : (vis < k ? vis : k);
   const long long win = t_last + 1 < n_win ? t_last + 1 : n_win;
-  const long long rows_max = nsel + win;
+  // bf16 rows are gathered by TMA in groups of 4: the window starts at nsel rounded up to 4
+  const long long rows_max = (kv_mixed ? nsel : ((nsel + 3) & ~3LL)) + win;
   const int tiles = (int)((rows_max + csa::ATT_TILE - 1) / csa::ATT_TILE);
   const long long units = (long long)B * Tq * p.HG;
   const int sms = sm_count();
@@ -244,6 +287,8 @@ AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int m, int 
   // rotate every stored row once when the queries gather far more rows than exist
   const long long gathered = (long long)B * Tq * rows_max;
   p.rotate_rows = (kv_mixed || gathered <= 2LL * B * ((long long)N + T_win)) ? 1 : 0;
+  // rows rotated in shared memory are rotated by (position - t): q and the output stay unrotated
+  p.rel_rope = p.rotate_rows;
   size_t off = 0;
   if (p.nch > 1) {
     p.off_part_o = off;
@@ -264,6 +309,69 @@ AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int m, int 
 bool tc_attend_shape(int n_h, int d, int r, int kv_dtype) {
   return d == csa::ATT_D && r == csa::ATT_R && n_h % csa::ATT_HG == 0 &&
          (kv_dtype == CSA_DT_BF16 || kv_dtype == CSA_DT_E4M3_BF16ROPE);
+}
+
+template <int NT, int CL>
+csa_status_t launch_topk2_cfg(const csa::Topk2Args& a, int rows, size_t smem, cudaStream_t st) {
+  auto kern = csa::topk2_kernel<NT, CL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_topk attr");
+  if (CL > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_topk cluster attr");
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)rows * CL);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kProgrammaticLaunch ? 2 : 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_topk launch");
+  return CSA_OK;
+}
+
+template <int NT>
+csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t smem, cudaStream_t st) {
+  switch (CL) {
+    case 1: return launch_topk2_cfg<NT, 1>(a, rows, smem, st);
+    case 2: return launch_topk2_cfg<NT, 2>(a, rows, smem, st);
+    case 4: return launch_topk2_cfg<NT, 4>(a, rows, smem, st);
+    case 8: return launch_topk2_cfg<NT, 8>(a, rows, smem, st);
+    default: return launch_topk2_cfg<NT, 16>(a, rows, smem, st);
+  }
+}
+
+// Slices of at most 16384 keys (a cluster of up to 16 CTAs per row; rows up
+// to 16 x 32768 keys), 1024 threads per CTA when few CTAs run, else 512.
+csa_status_t launch_topk2(const float* scores, int32_t* idx, int rows, int Tq, int N, int k, int m,
+                          int q_pos0, cudaStream_t st) {
+  // one CTA per row up to 32768 entries; longer rows over 8 or 16 CTAs
+  int CL = 1;
+  if (N > 32768) {
+    CL = 8;
+    while (CL < 16 && (long long)CL * 32768 < N) CL <<= 1;
+  }
+  int slice = (N + CL - 1) / CL;
+  slice = (slice + 3) & ~3;
+  if (slice < 4) slice = 4;
+  const size_t budget = 200 * 1024;
+  const size_t fixed = (size_t)csa::TK2_BINS1 * 4 * (CL > 1 ? 2 : 1) + (size_t)slice * 4;
+  if (fixed > budget) return CSA_ERR_UNSUPPORTED;
+  int cand_cap = (int)((budget - fixed) / 4);
+  if (cand_cap > slice) cand_cap = slice;
+  const size_t smem = (size_t)slice * 4 + (size_t)cand_cap * 4 + fixed - (size_t)slice * 4;
+  csa::Topk2Args a{scores, idx, Tq, N, k, m, q_pos0, slice, cand_cap};
+  if ((long long)rows * CL <= 2LL * sm_count()) return launch_topk2_nt<1024>(a, CL, rows, smem, st);
+  return launch_topk2_nt<512>(a, CL, rows, smem, st);
 }
 
 }  // namespace
@@ -330,11 +438,12 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
   dim3 grid(N, B);
   dim3 block(a.vecs * groups);
   size_t smem = (size_t)groups * a.vecs * 3 * vec * sizeof(float);
-  if (dtype == CSA_DT_BF16)
-    csa::compress_kernel<__nv_bfloat16><<<grid, block, smem, S(stream)>>>(a);
-  else
-    csa::compress_kernel<float><<<grid, block, smem, S(stream)>>>(a);
-  CSA_CHECK_LAUNCH("csa_compress");
+  {
+    cudaError_t e = dtype == CSA_DT_BF16
+                        ? launch_ex(csa::compress_kernel<__nv_bfloat16>, grid, block, smem, S(stream), 1, a)
+                        : launch_ex(csa::compress_kernel<float>, grid, block, smem, S(stream), 1, a);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_compress launch");
+  }
   return CSA_OK;
 }
 
@@ -351,8 +460,8 @@ csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const 
     csa::IndexF32Args a{reinterpret_cast<const float*>(qI), w, reinterpret_cast<const float*>(K),
                         scores, Tq, N, H, c, m, q_pos0};
     dim3 grid((N + 7) / 8, B * Tq);
-    csa::index_f32_kernel<<<grid, 256, 0, S(stream)>>>(a);
-    CSA_CHECK_LAUNCH("csa_index f32");
+    cudaError_t e = launch_ex(csa::index_f32_kernel, grid, dim3(256), 0, S(stream), 1, a);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_index f32 launch");
     return CSA_OK;
   }
   if (dtype == CSA_DT_BF16) {
@@ -394,7 +503,12 @@ csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, i
   if (!idx || (N > 0 && !scores)) return CSA_ERR_INVALID_ARG;
   if (!aligned(scores, 4) || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
   const int rows = B * Tq;
-  // cluster size: spread long rows of small batches over up to 16 SMs
+  // few long decode rows up to 32768 entries: 8-bit radix passes over a 16-CTA
+  // cluster; everything else up to 16 x 32768 entries: the candidate-filtering
+  // selector (measured faster there: many short rows, and rows past 32768)
+  if (!(N > 8192 && N <= 32768 && rows < 64) && N <= 16 * 32768)
+    return launch_topk2(scores, idx, rows, Tq, N, k, m, q_pos0, S(stream));
+  // rows longer than 16 slices of 32768 keys: 8-bit radix passes over up to 16 SMs
   int CL = 1;
   if (N > 8192 && rows < 64) CL = rows <= 9 ? 16 : 8;
   int slice = (N + CL - 1) / CL;
@@ -407,13 +521,15 @@ csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, i
   cfg.blockDim = dim3(csa::TOPK_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = S(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = kProgrammaticLaunch ? 2 : 1;
   cudaError_t e;
   switch (CL) {
     case 1:
@@ -477,8 +593,8 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
     cudaError_t e = cudaFuncSetAttribute(csa::attend_f32_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "csa_attend f32 attr");
-    csa::attend_f32_kernel<<<B * Tq, csa::ATT_F32_THREADS, smem, S(stream)>>>(a);
-    CSA_CHECK_LAUNCH("csa_attend f32");
+    e = launch_ex(csa::attend_f32_kernel, dim3(B * Tq), dim3(csa::ATT_F32_THREADS), smem, S(stream), 1, a);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_attend f32 launch");
     return CSA_OK;
   }
   if (!tc_attend_shape(n_h, d, r, ent.dtype) || ent.dtype != win.dtype) return CSA_ERR_UNSUPPORTED;
@@ -505,6 +621,9 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
   a.n_h = n_h; a.m = m; a.n_win = n_win; a.q_pos0 = q_pos0;
   a.HG = p.HG; a.nch = p.nch; a.chunk_rows = p.chunk_rows; a.items = p.items;
   a.rotate_rows = p.rotate_rows; a.kv_mixed = mixed;
+  a.rel_rope = p.rel_rope;
+  a.tma_rows = mixed ? 0 : 1;
+  if ((long long)B * N >= 0x7fffffffLL || (long long)B * T_win >= 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
   a.rf = rf;
   cudaStream_t st = S(stream);
@@ -516,35 +635,61 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
       ra.src = reinterpret_cast<const __nv_bfloat16*>(ent.data);
       ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_ent);
       ra.rows = (long long)B * N; ra.rows_per_b = N; ra.m = m; ra.base = 0;
-      csa::rope_rotate_rows_kernel<<<(unsigned)((ra.rows * 64 + 255) / 256), 256, 0, st>>>(ra);
-      CSA_CHECK_LAUNCH("csa_attend rotate entries");
+      cudaError_t e = launch_ex(csa::rope_rotate_rows_kernel, dim3((unsigned)((ra.rows * 64 + 255) / 256)),
+                                dim3(256), 0, st, 1, ra);
+      if (e != cudaSuccess) return cuda_fail(e, "csa_attend rotate entries");
       a.ent = ra.dst;
     }
     ra.src = reinterpret_cast<const __nv_bfloat16*>(win.data);
     ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_win);
     ra.rows = (long long)B * T_win; ra.rows_per_b = T_win; ra.m = 0; ra.base = win_base;
-    csa::rope_rotate_rows_kernel<<<(unsigned)((ra.rows * 64 + 255) / 256), 256, 0, st>>>(ra);
-    CSA_CHECK_LAUNCH("csa_attend rotate window");
+    {
+      cudaError_t e = launch_ex(csa::rope_rotate_rows_kernel, dim3((unsigned)((ra.rows * 64 + 255) / 256)),
+                                dim3(256), 0, st, 1, ra);
+      if (e != cudaSuccess) return cuda_fail(e, "csa_attend rotate window");
+    }
     a.win = ra.dst;
   }
   if (p.nch > 1) {
     a.part_o = reinterpret_cast<float*>(wsb + p.off_part_o);
     a.part_ml = reinterpret_cast<float*>(wsb + p.off_part_ml);
   }
+  CUtensorMap tmq, tment, tmwin;
+  memset(&tmq, 0, sizeof(tmq));
+  memset(&tment, 0, sizeof(tment));
+  memset(&tmwin, 0, sizeof(tmwin));
+  if (a.tma_rows &&
+      ((N > 0 && !tmap_bf16_rows(&tment, a.ent, (uint64_t)B * N)) ||
+       !tmap_bf16_rows(&tmwin, a.win, (uint64_t)B * T_win)))
+    return CSA_ERR_UNSUPPORTED;
+  if (a.tma_rows && N == 0) tment = tmwin;   // no entry groups exist; any valid map
+  if (p.rel_rope &&
+      !tmap_bf16_3d(&tmq, q, csa::ATT_D, (uint64_t)B * Tq * n_h, 1, (uint64_t)csa::ATT_D * 2,
+                    (uint64_t)B * Tq * n_h * csa::ATT_D * 2, 64, csa::ATT_HG))
+    return CSA_ERR_UNSUPPORTED;
   const int smem = csa::AttSmem::BYTES;
   cudaError_t e = cudaFuncSetAttribute(csa::attend_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc attr");
   const int sms = sm_count();
   const int grid = p.items < sms ? p.items : sms;
-  csa::attend_tc_kernel<<<grid, csa::ATT_THREADS, smem, st>>>(a);
-  CSA_CHECK_LAUNCH("csa_attend tc");
+  e = launch_ex(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st, 1, tmq, tment, tmwin, a);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc launch");
   if (p.nch > 1) {
     csa::CombineArgs ca;
     ca.part_o = a.part_o; ca.part_ml = a.part_ml; ca.sink = sink; ca.out = a.out;
     ca.Tq = Tq; ca.n_h = n_h; ca.HG = p.HG; ca.nch = p.nch; ca.q_pos0 = q_pos0; ca.rf = rf;
-    csa::attend_combine_kernel<<<(unsigned)((size_t)B * Tq * n_h), 128, 0, st>>>(ca);
-    CSA_CHECK_LAUNCH("csa_attend combine");
+    ca.rel_rope = p.rel_rope;
+    const size_t cmb_smem = (size_t)p.nch * csa::ATT_HG * sizeof(float);
+    if (cmb_smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(csa::attend_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)cmb_smem);
+      if (e != cudaSuccess) return cuda_fail(e, "csa_attend combine attr");
+    }
+    e = launch_ex(csa::attend_combine_kernel,
+                  dim3((unsigned)((size_t)B * Tq * p.HG * (csa::ATT_D / csa::CMB_DIMS))),
+                  dim3(csa::CMB_THREADS), cmb_smem, st, 1, ca);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_attend combine launch");
   }
   return CSA_OK;
 }

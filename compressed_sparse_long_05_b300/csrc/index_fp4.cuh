@@ -165,6 +165,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -294,17 +295,8 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           tc_fence_after();
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
           for (int qi = 0; qi < x.nq; ++qi) {
-            float acc = 0.f;
-#pragma unroll
-            for (int h0 = 0; h0 < H; h0 += 32) {
-              uint32_t r[32];
-              tmem_ld32(tbase + qi * H + h0, r);
-              tmem_ld_wait();
-              const float* wq = ws + qi * H + h0;
-#pragma unroll
-              for (int h = 0; h < 32; ++h) acc = fmaf(wq[h], fmaxf(__uint_as_float(r[h]), 0.f), acc);
-            }
-            const int vis = vis_of((long long)a.q_pos0 + x.t0 + qi, a.m, a.N);
+            const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
+            const int vis = vis32(a.q_pos0 + x.t0 + qi, a.m, a.N);
             if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
           }
           tc_fence_before();

@@ -25,7 +25,6 @@
 namespace csa {
 
 constexpr int IDX_THREADS = 192;
-constexpr int IDX_STAGES = 4;
 constexpr int IDX_TILE = 128;   // entries per tile (MMA M)
 
 struct IndexTcArgs {
@@ -35,28 +34,71 @@ struct IndexTcArgs {
   int QT;                // queries per group (QT * H <= 256)
   int G;                 // query groups per batch row
   int tiles_max;         // ceil(N / 128)
+  int stages;            // K-tile pipeline stages (bf16 kernel)
   int chunk_tiles;       // entry tiles per work item
   int chunks;            // work items per group
   int items;             // B * G * chunks
   uint32_t tmem_cols;    // allocated TMEM columns (power of 2 >= 2 * QT * H)
 };
 
+// Shared-memory layout, sized at launch: S K-tile stages (4, or 6 when the
+// query group is at most 64 rows), the query group, head weights, barriers.
 template <int H, int C>
 struct IndexSmem {
+  static constexpr int MAX_STAGES = 6;
   static constexpr int A_BYTES = IDX_TILE * C * 2;       // one K tile
-  static constexpr int B_BYTES_MAX = 256 * C * 2;        // one q group (QT*H <= 256 rows)
   static constexpr int KCH = C / 64;                     // 64-element swizzle chunks along c
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + IDX_STAGES * A_BYTES;
-  static constexpr int OFF_W = OFF_B + B_BYTES_MAX;      // float w_s[4 warps][2][256]
-  static constexpr int OFF_BAR = OFF_W + 4 * 2 * 256 * 4;
-  static constexpr int BYTES = OFF_BAR + 256 + 1024;     // + alignment slack
+  int S, OFF_B, OFF_W, OFF_BAR, BYTES;
+  __host__ __device__ IndexSmem(int stages, int nqh) {
+    S = stages;
+    OFF_B = S * A_BYTES;
+    OFF_W = OFF_B + ((nqh * C * 2 + 1023) & ~1023);      // float w_s[4 warps][2][256]
+    OFF_BAR = OFF_W + 4 * 2 * 256 * 4;
+    BYTES = OFF_BAR + 256 + 1024;                        // + alignment slack
+  }
+  static constexpr int stages_for(int nqh) {
+    return (MAX_STAGES * A_BYTES + ((nqh * C * 2 + 1023) & ~1023) + 4 * 2 * 256 * 4 + 256 + 1024 <=
+            220 * 1024) ? MAX_STAGES : 4;
+  }
 };
 
 CSA_DEVINL int vis_of(long long t, int m, int N) {
   long long v = (t + 1) / m;
   if (v < 0) v = 0;
   return (int)(v < N ? v : N);
+}
+
+// Fold the H accumulator columns of one query in this warp's 32 TMEM lanes:
+// sum_h w[h] * ReLU(D[lane][h]).  Two 32-column loads in flight before each
+// wait, four independent partial sums (the head reduction is a tree, not a
+// 64-deep dependency chain).
+template <int H>
+CSA_DEVINL float fold_heads(uint32_t taddr, const float* wq) {
+  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+  for (int h0 = 0; h0 < H; h0 += 64) {
+    constexpr int kMax = 64;
+    const int nh = (H - h0) < kMax ? (H - h0) : kMax;
+    uint32_t r[64];
+    tmem_ld32(taddr + h0, r);
+    if (nh > 32) tmem_ld32(taddr + h0 + 32, r + 32);
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < nh; h += 4) {
+      const float4 w4 = *reinterpret_cast<const float4*>(wq + h0 + h);
+      p0 = fmaf(w4.x, fmaxf(__uint_as_float(r[h]), 0.f), p0);
+      p1 = fmaf(w4.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), p1);
+      p2 = fmaf(w4.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), p2);
+      p3 = fmaf(w4.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), p3);
+    }
+  }
+  return (p0 + p1) + (p2 + p3);
+}
+
+// visible entries of the query at position t (32-bit: positions < 2^31)
+CSA_DEVINL int vis32(int t, int m, int N) {
+  const int v = (t + 1) / m;
+  return v < N ? (v < 0 ? 0 : v) : N;
 }
 
 struct IdxItem {
@@ -83,16 +125,18 @@ template <int H, int C>
 __global__ void __launch_bounds__(IDX_THREADS, 1)
 index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant__ CUtensorMap tm_q,
                 IndexTcArgs a) {
-  using L = IndexSmem<H, C>;
+  const int NQH = a.QT * H;                      // MMA N
+  const IndexSmem<H, C> L(a.stages, NQH);
+  const int S = L.S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem + L::OFF_A;
-  uint8_t* sB = smem + L::OFF_B;
-  float* w_s = reinterpret_cast<float*>(smem + L::OFF_W);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* full = bars;                         // [STAGES]
-  uint64_t* empty = bars + IDX_STAGES;           // [STAGES]
-  uint64_t* acc_full = bars + 2 * IDX_STAGES;    // [2]
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + L.OFF_B;
+  float* w_s = reinterpret_cast<float*>(smem + L.OFF_W);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.OFF_BAR);
+  uint64_t* full = bars;                         // [MAX_STAGES]
+  uint64_t* empty = bars + L.MAX_STAGES;         // [MAX_STAGES]
+  uint64_t* acc_full = bars + 2 * L.MAX_STAGES;  // [2]
   uint64_t* acc_empty = acc_full + 2;            // [2]
   uint64_t* b_full = acc_empty + 2;
   uint64_t* b_free = b_full + 1;
@@ -101,11 +145,10 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NQH = a.QT * H;                      // MMA N
   const uint32_t B_BYTES = (uint32_t)NQH * C * 2;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < IDX_STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
+    for (int s = 0; s < S; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(acc_full + s, 1); mbar_init(acc_empty + s, 4); }
     mbar_init(b_full, 1);
     mbar_init(b_free, 1);
@@ -122,6 +165,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -133,31 +177,31 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         if (x.jv <= x.j0) continue;
         const int ntl = x.jv - x.j0;
         auto load_a = [&](int j) -> bool {
-          const uint32_t st = ia % IDX_STAGES, ph = (ia / IDX_STAGES) & 1;
+          const uint32_t st = ia % S, ph = (ia / S) & 1;
           if (!mbar_wait(empty + st, ph ^ 1, abort_flag)) return false;
-          mbar_arrive_expect_tx(full + st, L::A_BYTES);
+          mbar_arrive_expect_tx(full + st, L.A_BYTES);
 #pragma unroll
-          for (int kc = 0; kc < L::KCH; ++kc)
-            tma_load_3d(sA + st * L::A_BYTES + kc * (IDX_TILE * 128), &tm_K, full + st, kc * 64,
+          for (int kc = 0; kc < L.KCH; ++kc)
+            tma_load_3d(sA + st * L.A_BYTES + kc * (IDX_TILE * 128), &tm_K, full + st, kc * 64,
                         j * IDX_TILE, x.b);
           ++ia;
           return true;
         };
         // prefetch the first tiles of this item, then swap in its query group
-        const int pre = min(ntl, IDX_STAGES);
+        const int pre = min(ntl, S);
         for (int jj = 0; jj < pre && ok; ++jj) ok = load_a(x.j0 + jj);
         if (!ok) break;
         if (nitem > 0 && !mbar_wait(b_free, (nitem - 1) & 1, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(b_full, B_BYTES);
-        for (int kc = 0; kc < L::KCH; ++kc)
+        for (int kc = 0; kc < L.KCH; ++kc)
           tma_load_3d(sB + kc * (NQH * 128), &tm_q, b_full, kc * 64, x.t0 * H, x.b);
         b_issued = true;
         ++nitem;
         for (int jj = pre; jj < ntl && ok; ++jj) ok = load_a(x.j0 + jj);
       }
       // drain copies still in flight before the CTA may exit
-      for (uint32_t k = (ia > IDX_STAGES ? ia - IDX_STAGES : 0); k < ia; ++k)
-        mbar_drain(full + (k % IDX_STAGES), (k / IDX_STAGES) & 1);
+      for (uint32_t k = (ia > (uint32_t)S ? ia - S : 0); k < ia; ++k)
+        mbar_drain(full + (k % S), (k / S) & 1);
       if (b_issued) mbar_drain(b_full, (nitem - 1) & 1);
     }
   } else if (warp == 1) {
@@ -171,12 +215,12 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         if (x.jv <= x.j0) continue;
         if (!mbar_wait(b_full, nitem & 1, abort_flag)) { ok = false; break; }
         for (int j = x.j0; j < x.jv; ++j) {
-          const uint32_t st = ia % IDX_STAGES, ph = (ia / IDX_STAGES) & 1;
+          const uint32_t st = ia % S, ph = (ia / S) & 1;
           const uint32_t buf = iacc & 1, aph = (iacc >> 1) & 1;
           if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag)) { ok = false; break; }
           if (!mbar_wait(full + st, ph, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t aBase = smem_u32(sA + st * L::A_BYTES);
+          const uint32_t aBase = smem_u32(sA + st * L.A_BYTES);
           const uint32_t bBase = smem_u32(sB);
           const uint32_t d = tmem + buf * (uint32_t)NQH;
 #pragma unroll
@@ -220,17 +264,8 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           tc_fence_after();
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
           for (int qi = 0; qi < x.nq; ++qi) {
-            float acc = 0.f;
-#pragma unroll
-            for (int h0 = 0; h0 < H; h0 += 32) {
-              uint32_t r[32];
-              tmem_ld32(tbase + qi * H + h0, r);
-              tmem_ld_wait();
-              const float* wq = ws + qi * H + h0;
-#pragma unroll
-              for (int h = 0; h < 32; ++h) acc = fmaf(wq[h], fmaxf(__uint_as_float(r[h]), 0.f), acc);
-            }
-            const int vis = vis_of((long long)a.q_pos0 + x.t0 + qi, a.m, a.N);
+            const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
+            const int vis = vis32(a.q_pos0 + x.t0 + qi, a.m, a.N);
             if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
           }
           tc_fence_before();

@@ -19,6 +19,7 @@ struct IndexF32Args {
 };
 
 __global__ void __launch_bounds__(256) index_f32_kernel(IndexF32Args a) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int row = blockIdx.y;                      // b * Tq + i
@@ -61,6 +62,7 @@ struct AttendF32Args {
 constexpr int ATT_F32_THREADS = 256;
 
 __global__ void __launch_bounds__(ATT_F32_THREADS) attend_f32_kernel(AttendF32Args a) {
+  pdl_enter();
   extern __shared__ float sm[];
   const int row = blockIdx.x;                    // b * Tq + i
   const int b = row / a.Tq, i = row % a.Tq;

@@ -60,6 +60,7 @@ CSA_DEVINL int block_excl_scan(int x, int* sh_warp, int* total) {
 
 template <int CL>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
+  pdl_enter();
   extern __shared__ __align__(16) uint32_t keys[];            // [slice]
   __shared__ uint32_t whist[TOPK_WARPS][256];
   __shared__ uint32_t merged[3][256];                         // cluster histogram (used in rank 0)

@@ -111,6 +111,10 @@ def _check_topk(scores, idx, k, m, q_pos0):
     (3, 2, 40000, 1024, 159990, 3),  # several rows, ties, ragged slices
     (1, 40, 9000, 4096, 35990, 0),   # large k
     (2, 3, 20000, 7, 79999, 1),      # every score equal: lowest indices win
+    (2, 1, 262144, 1024, 1048575, 0),   # 1M-context decode rows: 16-CTA clusters
+    (1, 2, 262144, 1024, 1048574, 2),   # ties across a 16-CTA cluster
+    (1, 1, 600000, 1024, 2399999, 0),   # beyond 16 x 32768 keys: 8-bit radix over 16 CTAs
+    (1, 3, 70001, 333, 280003, 0),      # odd N: unaligned row starts, ragged slices
 ])
 def test_topk(K, B, Tq, N, k, q_pos0, levels):
     g = _gen(21)

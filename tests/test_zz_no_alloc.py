@@ -49,9 +49,11 @@ def _decode_case(K, B, N, k, seed):
 
 
 def test_noalloc_matches_workspace_call_twice():
+    # k = 4096 splits each row set over more CTAs than one cluster holds, so the
+    # chunks merge through fp32 partials in the scratch array
     import compressed_sparse_long_05_b300 as K
-    c = _decode_case(K, B=3, N=3000, k=1024, seed=500)
-    need = K.attend_workspace_size(c["q"], c["ent"], c["win"], 1024, c["m"], c["n_win"],
+    c = _decode_case(K, B=1, N=20000, k=4096, seed=500)
+    need = K.attend_workspace_size(c["q"], c["ent"], c["win"], 4096, c["m"], c["n_win"],
                                    c["q_pos0"], c["r"], False)
     assert 0 < need <= SCRATCH_BYTES      # the case really uses scratch, and it fits
     ref = K.csa_attend(c["q"], c["ent"], c["idx"], c["win"], c["sink"], c["m"], c["n_win"],
@@ -69,9 +71,12 @@ def test_noalloc_matches_workspace_call_twice():
 def test_noalloc_second_call_other_sizes():
     # a smaller call after a larger one: stale scratch from the first must not leak in
     import compressed_sparse_long_05_b300 as K
-    big = _decode_case(K, B=4, N=5000, k=1024, seed=510)
-    small = _decode_case(K, B=1, N=700, k=256, seed=520)
-    for c, k in ((big, 1024), (small, 256)):
+    big = _decode_case(K, B=1, N=20000, k=4096, seed=510)
+    small = _decode_case(K, B=2, N=9000, k=2048, seed=520)
+    for c, k in ((big, 4096), (small, 2048)):
+        need = K.attend_workspace_size(c["q"], c["ent"], c["win"], k, c["m"], c["n_win"],
+                                       c["q_pos0"], c["r"], False)
+        assert 0 < need <= SCRATCH_BYTES
         ref = K.csa_attend(c["q"], c["ent"], c["idx"], c["win"], c["sink"], c["m"], c["n_win"],
                            c["win_base"], c["q_pos0"], c["r"])
         out = K.csa_attend_noalloc(c["q"], c["ent"], c["idx"], c["win"], c["sink"], c["m"],
@@ -84,15 +89,15 @@ def test_noalloc_second_call_other_sizes():
 def test_noalloc_rejects_sizes_beyond_the_array():
     import compressed_sparse_long_05_b300 as K
     from compressed_sparse_long_05_b300 import _lib
-    c = _decode_case(K, B=16, N=20000, k=1024, seed=530)
-    need = K.attend_workspace_size(c["q"], c["ent"], c["win"], 1024, c["m"], c["n_win"],
+    c = _decode_case(K, B=4, N=40000, k=4096, seed=530)
+    need = K.attend_workspace_size(c["q"], c["ent"], c["win"], 4096, c["m"], c["n_win"],
                                    c["q_pos0"], c["r"], False)
     assert need > SCRATCH_BYTES
     out = torch.zeros_like(c["q"])
     B, Tq, n_h, d = c["q"].shape
     st = _lib.lib().csa_attend_noalloc(
         _lib._p(c["q"]), _lib._kv(c["ent"]), _lib._p(c["idx"]), _lib._kv(c["win"]),
-        _lib._p(c["sink"]), _lib._p(out), B, Tq, c["ent"].shape[1], 1024, c["win"].shape[1],
+        _lib._p(c["sink"]), _lib._p(out), B, Tq, c["ent"].shape[1], 4096, c["win"].shape[1],
         c["win_base"], n_h, d, c["r"], c["m"], c["n_win"], c["q_pos0"], ctypes.c_float(1e4),
         _lib._stream())
     assert st == 3                      # CSA_ERR_WORKSPACE, before any launch
