@@ -60,7 +60,7 @@ struct AttendTcArgs {
   const int32_t* idx;            // [B, Tq, k] or null (dense)
   const float* sink;             // [n_h]
   __nv_bfloat16* out;            // [B, Tq, n_h, 512]
-  float* part_o;                 // [items][512 dims][64 heads] (split mode)
+  float* part_o;                 // [items][64 heads][512 dims] (split mode)
   float* part_ml;                // [items][64][2]   (split mode)
   int B, Tq, N, k, T_win, win_base, n_h, m, n_win, q_pos0;
   int HG;                        // head groups = n_h / 64
@@ -669,6 +669,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!ok) break;
       // ======================= item epilogue =======================
       const bool single = (a.nch == 1);
+      // split item and one item per CTA: the entry tile is free for staging
+      const bool stage_out = !single && (int)gridDim.x >= a.items;
       if (j > 0) {
         if (!mbar_wait(p_free, (n - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -717,14 +719,31 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               if (rot_out) v = (lane & 1) ? (pv * s + v * c) : (v * c - pv * s);
               a.out[(orow + hh + e) * ATT_D + dim] = __float2bfloat16_rn(v);
             }
-          } else {
-            // unnormalised partial, layout [item][dim][64 heads]
-            float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)it * ATT_D + dim) * ATT_HG + hh);
+          } else if (stage_out) {
+            // unnormalised partial into the staging copy of its global layout
+            // [64 heads][512 dims]: consecutive lanes write consecutive dims
+            float* st = reinterpret_cast<float*>(sE) + dim;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              dst[e >> 2] = make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                                        __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+            for (int e = 0; e < 32; ++e) st[(size_t)(hh + e) * ATT_D] = __uint_as_float(r[e]);
+          } else {
+            // unnormalised partial, layout [item][64 heads][512 dims]
+            float* dst = a.part_o + (size_t)it * ATT_HG * ATT_D + dim;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dst[(size_t)(hh + e) * ATT_D] = __uint_as_float(r[e]);
           }
+        }
+      }
+      if (stage_out) {
+        // one bulk copy of the staged 128 KB partial to global memory
+        fence_proxy_async();
+        named_bar_sync(2, 128);
+        if (threadIdx.x == 0) {
+          asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                           a.part_o + (size_t)it * ATT_D * ATT_HG),
+                       "r"(smem_u32(sE)), "r"(ATT_D * ATT_HG * 4)
+                       : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         }
       }
       tc_fence_before();
@@ -742,9 +761,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // ----------------------------------------------------------------------------
 // split-chunk combine: out[b,i,h,:] = sum_c 2^(m_c - M) O_c / (sum_c 2^(m_c - M) l_c
 // + 2^(z'_h log2 e - M)), then (absolute-RoPE mode) the RoPE dims rotated back by -t.
-// Partials are [chunk][dim][64 heads] f32.  One CTA per (query row, head group,
-// 8 output dims): it reads one coalesced 2 KB [8 dims x 64 heads] slice per
-// chunk and writes one 16-byte bf16 run per head.
+// Partials are [chunk][64 heads][512 dims] f32.  One CTA per (query row, head
+// group, 8 output dims): thread pairs read a head's 32-byte slice of every
+// chunk and write one 16-byte bf16 run.
 // ----------------------------------------------------------------------------
 struct CombineArgs {
   const float* part_o; const float* part_ml; const float* sink;
@@ -759,8 +778,7 @@ constexpr int CMB_DIMS = 8;                        // output dims per CTA
 
 __global__ void __launch_bounds__(CMB_THREADS) attend_combine_kernel(const CombineArgs a) {
   pdl_enter();
-  extern __shared__ float cmb_w[];                 // [nch][64] chunk weights
-  __shared__ float tile[ATT_HG][CMB_DIMS + 1];
+  extern __shared__ float cmb_w[];                 // [nch][64][2]: (m, l), then weights
   const int db = (blockIdx.x % (ATT_D / CMB_DIMS)) * CMB_DIMS;
   const int unit = blockIdx.x / (ATT_D / CMB_DIMS);   // (b * Tq + i) * HG + hg
   const int hg = unit % a.HG;
@@ -768,53 +786,59 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine_kernel(const Combi
   const int i = bi % a.Tq;
   const size_t it0 = (size_t)unit * a.nch;
   const int tid = threadIdx.x;
+  // every chunk's (m, l) of this unit: one contiguous run, all loads in flight
+  {
+    const float4* src = reinterpret_cast<const float4*>(a.part_ml + it0 * ATT_HG * 2);
+    float4* dst = reinterpret_cast<float4*>(cmb_w);
+    for (int e = tid; e < a.nch * ATT_HG / 2; e += CMB_THREADS) dst[e] = __ldg(src + e);
+  }
+  __syncthreads();
   if (tid < ATT_HG) {
     const int h = tid;
-    const float* ml = a.part_ml + (it0 * ATT_HG + h) * 2;
     const float zs = __ldg(a.sink + hg * ATT_HG + h) * 1.4426950408889634f;
     float M = zs;
-    for (int c = 0; c < a.nch; ++c) M = fmaxf(M, __ldg(ml + (size_t)c * ATT_HG * 2));
+    for (int c = 0; c < a.nch; ++c) M = fmaxf(M, cmb_w[(c * ATT_HG + h) * 2]);
     float den = exp2f(zs - M);
     for (int c = 0; c < a.nch; ++c) {
-      const float mc = __ldg(ml + (size_t)c * ATT_HG * 2);
-      if (mc != -INFINITY) den += __ldg(ml + (size_t)c * ATT_HG * 2 + 1) * exp2f(mc - M);
+      const float mc = cmb_w[(c * ATT_HG + h) * 2];
+      if (mc != -INFINITY) den += cmb_w[(c * ATT_HG + h) * 2 + 1] * exp2f(mc - M);
     }
     const float inv = 1.f / den;
     for (int c = 0; c < a.nch; ++c) {
-      const float mc = __ldg(ml + (size_t)c * ATT_HG * 2);
-      cmb_w[c * ATT_HG + h] = mc == -INFINITY ? 0.f : exp2f(mc - M) * inv;
+      const float mc = cmb_w[(c * ATT_HG + h) * 2];
+      cmb_w[(c * ATT_HG + h) * 2] = mc == -INFINITY ? 0.f : exp2f(mc - M) * inv;   // weight
     }
   }
   __syncthreads();
-  // thread: dim db + tid / 16, heads 4 (tid % 16) .. + 3
-  const int dl = tid >> 4, hq = (tid & 15) * 4;
+  // thread: head tid / 2, dims db + 4 (tid & 1) .. + 3
+  const int h = tid >> 1, half = tid & 1;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* src = a.part_o + (it0 * ATT_D + db + dl) * ATT_HG + hq;
+  const float* src = a.part_o + (it0 * ATT_HG + h) * ATT_D + db + 4 * half;
   for (int c = 0; c < a.nch; ++c) {
-    const float4 w4 = *reinterpret_cast<const float4*>(cmb_w + c * ATT_HG + hq);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(src + (size_t)c * ATT_D * ATT_HG));
-    acc.x += v.x * w4.x; acc.y += v.y * w4.y; acc.z += v.z * w4.z; acc.w += v.w * w4.w;
+    const float w = cmb_w[(c * ATT_HG + h) * 2];
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src + (size_t)c * ATT_HG * ATT_D));
+    acc.x += v.x * w; acc.y += v.y * w; acc.z += v.z * w; acc.w += v.w * w;
   }
-  tile[hq][dl] = acc.x; tile[hq + 1][dl] = acc.y; tile[hq + 2][dl] = acc.z; tile[hq + 3][dl] = acc.w;
-  __syncthreads();
-  if (tid < ATT_HG) {
-    const int h = tid;
-    float v[CMB_DIMS];
-#pragma unroll
-    for (int k = 0; k < CMB_DIMS; ++k) v[k] = tile[h][k];
+  float v8[CMB_DIMS];
+  v8[0] = acc.x; v8[1] = acc.y; v8[2] = acc.z; v8[3] = acc.w;
+  v8[4] = __shfl_down_sync(0xffffffffu, acc.x, 1);
+  v8[5] = __shfl_down_sync(0xffffffffu, acc.y, 1);
+  v8[6] = __shfl_down_sync(0xffffffffu, acc.z, 1);
+  v8[7] = __shfl_down_sync(0xffffffffu, acc.w, 1);
+  if (half == 0) {
     if (!a.rel_rope && db >= ATT_D - ATT_R) {
       const long long t = (long long)a.q_pos0 + i;
 #pragma unroll
       for (int p = 0; p < CMB_DIMS / 2; ++p) {
         float cs, sn;
         rope_cos_sin(-t, a.rf.F[((db - (ATT_D - ATT_R)) >> 1) + p], cs, sn);
-        const float x0 = v[2 * p], x1 = v[2 * p + 1];
-        v[2 * p] = x0 * cs - x1 * sn;
-        v[2 * p + 1] = x0 * sn + x1 * cs;
+        const float x0 = v8[2 * p], x1 = v8[2 * p + 1];
+        v8[2 * p] = x0 * cs - x1 * sn;
+        v8[2 * p + 1] = x0 * sn + x1 * cs;
       }
     }
     __nv_bfloat16* o = a.out + ((size_t)bi * a.n_h + (size_t)hg * ATT_HG + h) * ATT_D + db;
-    *reinterpret_cast<uint4*>(o) = f_to_bf16x8(v);
+    *reinterpret_cast<uint4*>(o) = f_to_bf16x8(v8);
   }
 }
 

@@ -680,7 +680,7 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
     ca.part_o = a.part_o; ca.part_ml = a.part_ml; ca.sink = sink; ca.out = a.out;
     ca.Tq = Tq; ca.n_h = n_h; ca.HG = p.HG; ca.nch = p.nch; ca.q_pos0 = q_pos0; ca.rf = rf;
     ca.rel_rope = p.rel_rope;
-    const size_t cmb_smem = (size_t)p.nch * csa::ATT_HG * sizeof(float);
+    const size_t cmb_smem = (size_t)p.nch * csa::ATT_HG * 2 * sizeof(float);
     if (cmb_smem > 48 * 1024) {
       e = cudaFuncSetAttribute(csa::attend_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)cmb_smem);
