@@ -125,6 +125,10 @@ def work(cfg):
         pairs = int(vis.sum())
         out["index"] = (B * (N * kb + Tq * H * kb + Tq * H * 4 + Tq * N * 4), 2.0 * B * pairs * H * c)
         out["topk"] = (B * (pairs * 4 + Tq * k * 4), 0.0)
+        if Tq == 1:
+            ib, ifl = out.pop("index")
+            tb, _ = out.pop("topk")
+            out["index_topk"] = (ib + tb, ifl)
         rows = np.minimum(k, vis) + win
         out["attend"] = (B * (int(rows.sum()) * rb + int(np.minimum(k, vis).sum()) * 4 +
                               2 * Tq * n_h * d * el), 4.0 * B * int(rows.sum()) * n_h * d)
@@ -227,11 +231,19 @@ def make_step(K, cfg, x, buf):
         stages.append(("compress", lambda: K.csa_compress(x["C"], x["Z"], m, out=buf.entries)))
     ent = buf.entries if kind.endswith("prefill") else P._entries_arg(x)
     win = P._win_arg(x)
-    if kind.startswith("csa"):
+    if kind.startswith("csa") and cfg["Tq"] == 1:
+        # decode: one call scores every entry and selects the top k (the index
+        # kernel also builds the selector's first histogram)
+        qI, qI_sf, Kt, K_sf = P._indexer_args(x)
+        stages.append(("index_topk", lambda: K.csa_index_topk(
+            qI, x["w"], Kt, cfg["k"], m, q0, qI_sf=qI_sf, K_sf=K_sf, scores=buf.scores,
+            idx=buf.idx, ws=buf.ws_topk)))
+    elif kind.startswith("csa"):
         qI, qI_sf, Kt, K_sf = P._indexer_args(x)
         stages.append(("index", lambda: K.csa_index(qI, x["w"], Kt, m, q0, qI_sf=qI_sf, K_sf=K_sf,
                                                     scores=buf.scores)))
         stages.append(("topk", lambda: K.csa_topk(buf.scores, cfg["k"], m, q0, idx=buf.idx)))
+    if kind.startswith("csa"):
         stages.append(("attend", lambda: K.csa_attend(x["q"], ent, buf.idx, win, x["sink"], m, n_win,
                                                       wb, q0, r, base, out=buf.out, ws=buf.ws)))
     else:
@@ -250,6 +262,9 @@ def alloc_buffers(K, cfg, x, dev):
     if kind.startswith("csa"):
         buf.scores = torch.empty((B, Tq, N), dtype=torch.float32, device=dev)
         buf.idx = torch.empty((B, Tq, cfg["k"]), dtype=torch.int32, device=dev)
+        dt = 3 if "qI_fp4" in x else 1
+        nb = K.lib().csa_index_topk_workspace_size(B, Tq, N, dt)
+        buf.ws_topk = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
     buf.out = torch.empty_like(x["q"])
     ent = buf.entries if kind.endswith("prefill") else P._entries_arg(x)
     nbytes = K.attend_workspace_size(x["q"], ent, P._win_arg(x), cfg.get("k", 0), cfg["m"],

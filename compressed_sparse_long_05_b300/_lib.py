@@ -40,6 +40,8 @@ _SIGS = {
     "csa_compress": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
     "csa_index": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
     "csa_topk": [_P, _P, _I, _I, _I, _I, _I, _I, _P],
+    "csa_index_topk": [_P, _P, _P, _P, _P, _P, _P] + [_I] * 9 + [_P, _Z, _P],
+    "csa_index_topk_workspace_size": [_I] * 4,
     "csa_attend": [_P, KV, _P, KV, _P, _P] + [_I] * 12 + [_F, _P, _Z, _P],
     "hca_attend": [_P, KV, KV, _P, _P] + [_I] * 11 + [_F, _P, _Z, _P],
     "csa_attend_noalloc": [_P, KV, _P, KV, _P, _P] + [_I] * 12 + [_F, _P],
@@ -49,7 +51,7 @@ _SIGS = {
     "csa_last_cuda_error": [],
     "csa_version": [],
 }
-_RESTYPES = {"csa_attend_workspace_size": _Z, "csa_status_string": ctypes.c_char_p,
+_RESTYPES = {"csa_attend_workspace_size": _Z, "csa_index_topk_workspace_size": _Z, "csa_status_string": ctypes.c_char_p,
              "csa_last_cuda_error": ctypes.c_char_p}
 
 
@@ -140,6 +142,26 @@ def csa_topk(scores, k, m, q_pos0, idx=None):
         idx = torch.empty((B, Tq, k), dtype=torch.int32, device=scores.device)
     _check("csa_topk", lib().csa_topk(_p(scores), _p(idx), B, Tq, N, k, m, q_pos0, _stream()))
     return idx
+
+
+def csa_index_topk(qI, w, K, k, m, q_pos0, qI_sf=None, K_sf=None, scores=None, idx=None, ws=None):
+    """Indexer scores and the top-k index sets of one call (same results as
+    csa_index then csa_topk); returns (scores, idx, ws)."""
+    fp4 = qI.dtype == torch.uint8
+    B, Tq, H = qI.shape[:3]
+    c = qI.shape[3] * (2 if fp4 else 1)
+    N = K.shape[1]
+    dt = DT_E2M1_BLOCK16 if fp4 else _dt(qI)
+    if scores is None:
+        scores = torch.empty((B, Tq, N), dtype=torch.float32, device=qI.device)
+    if idx is None:
+        idx = torch.empty((B, Tq, k), dtype=torch.int32, device=qI.device)
+    nbytes = lib().csa_index_topk_workspace_size(B, Tq, N, dt)
+    ws = _workspace(ws, nbytes, qI.device)
+    _check("csa_index_topk", lib().csa_index_topk(
+        _p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(scores), _p(idx), B, Tq, N, H, c, m, q_pos0,
+        k, dt, _p(ws) if nbytes else None, nbytes, _stream()))
+    return scores, idx, ws
 
 
 def attend_workspace_size(q, entries, win, k, m, n_win, q_pos0, r, is_hca):

@@ -193,7 +193,7 @@ csa_status_t plan_index(csa::IndexTcArgs& a, int QT, int B, int Tq, int N) {
 template <int H>
 csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w, const void* K,
                               const void* K_sf, float* scores, int B, int Tq, int N, int m,
-                              int q_pos0, cudaStream_t stream) {
+                              int q_pos0, uint32_t* hist, cudaStream_t stream) {
   csa::IndexFp4Args fa;
   memset(&fa, 0, sizeof(fa));
   csa::IndexTcArgs& a = fa.t;
@@ -203,6 +203,7 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
   if ((long long)B * N >= 0x7fffffffLL || (long long)B * Tq * H >= 0x7fffffffLL)
     return CSA_ERR_UNSUPPORTED;
   fa.sf_rows = (long long)B * N;
+  a.hist = a.QT == 1 ? hist : nullptr;
   const int nqh = a.QT * H;
   a.tmem_cols = 512;
   CUtensorMap tmK, tmq, tmKs, tmqs;
@@ -226,7 +227,7 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
 
 template <int H, int C>
 csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, float* scores, int B,
-                             int Tq, int N, int m, int q_pos0, cudaStream_t stream) {
+                             int Tq, int N, int m, int q_pos0, uint32_t* hist, cudaStream_t stream) {
   csa::IndexTcArgs a;
   a.w = w; a.scores = scores; a.B = B; a.Tq = Tq; a.N = N; a.m = m; a.q_pos0 = q_pos0;
   csa_status_t st = plan_index(a, 256 / H, B, Tq, N);
@@ -241,8 +242,9 @@ csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, floa
       !tmap_bf16_3d(&tmq, qI, C, (uint64_t)Tq * H, B, (uint64_t)C * 2, (uint64_t)Tq * H * C * 2,
                     64, nqh))
     return CSA_ERR_UNSUPPORTED;
-  a.stages = csa::IndexSmem<H, C>::stages_for(nqh);
-  const int smem = csa::IndexSmem<H, C>(a.stages, nqh).BYTES;
+  a.hist = a.QT == 1 ? hist : nullptr;
+  a.stages = csa::IndexSmem<H, C>::stages_for(nqh, a.hist != nullptr);
+  const int smem = csa::IndexSmem<H, C>(a.stages, nqh, a.hist != nullptr).BYTES;
   auto kern = csa::index_tc_kernel<H, C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "csa_index tc attr");
@@ -311,9 +313,9 @@ bool tc_attend_shape(int n_h, int d, int r, int kv_dtype) {
          (kv_dtype == CSA_DT_BF16 || kv_dtype == CSA_DT_E4M3_BF16ROPE);
 }
 
-template <int NT, int CL>
+template <int NT, int CL, int BITS1>
 csa_status_t launch_topk2_cfg(const csa::Topk2Args& a, int rows, size_t smem, cudaStream_t st) {
-  auto kern = csa::topk2_kernel<NT, CL>;
+  auto kern = csa::topk2_kernel<NT, CL, BITS1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "csa_topk attr");
   if (CL > 8) {
@@ -339,39 +341,47 @@ csa_status_t launch_topk2_cfg(const csa::Topk2Args& a, int rows, size_t smem, cu
   return CSA_OK;
 }
 
-template <int NT>
+template <int NT, int BITS1>
 csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t smem, cudaStream_t st) {
   switch (CL) {
-    case 1: return launch_topk2_cfg<NT, 1>(a, rows, smem, st);
-    case 2: return launch_topk2_cfg<NT, 2>(a, rows, smem, st);
-    case 4: return launch_topk2_cfg<NT, 4>(a, rows, smem, st);
-    case 8: return launch_topk2_cfg<NT, 8>(a, rows, smem, st);
-    default: return launch_topk2_cfg<NT, 16>(a, rows, smem, st);
+    case 1: return launch_topk2_cfg<NT, 1, BITS1>(a, rows, smem, st);
+    case 2: return launch_topk2_cfg<NT, 2, BITS1>(a, rows, smem, st);
+    case 4: return launch_topk2_cfg<NT, 4, BITS1>(a, rows, smem, st);
+    case 8: return launch_topk2_cfg<NT, 8, BITS1>(a, rows, smem, st);
+    default: return launch_topk2_cfg<NT, 16, BITS1>(a, rows, smem, st);
   }
 }
 
-// Slices of at most 16384 keys (a cluster of up to 16 CTAs per row; rows up
-// to 16 x 32768 keys), 1024 threads per CTA when few CTAs run, else 512.
+// One CTA per row up to 32768 entries, longer rows over a cluster of 8 or 16
+// CTAs (rows up to 16 x 32768 entries); 1024 threads per CTA when few CTAs
+// run, else 512.  `hist` (optional): per-row histograms of the first
+// IDX_HBITS key bits of the visible scores, built by the index kernel.
 csa_status_t launch_topk2(const float* scores, int32_t* idx, int rows, int Tq, int N, int k, int m,
-                          int q_pos0, cudaStream_t st) {
-  // one CTA per row up to 32768 entries; longer rows over 8 or 16 CTAs
+                          int q_pos0, const uint32_t* hist, cudaStream_t st) {
   int CL = 1;
   if (N > 32768) {
     CL = 8;
     while (CL < 16 && (long long)CL * 32768 < N) CL <<= 1;
+  } else if (hist && N > 8192 && (long long)rows * 8 <= 2LL * sm_count()) {
+    CL = 8;   // few decode rows: spread the sweeps over 8 CTAs (measured faster than 1 or 16)
   }
   int slice = (N + CL - 1) / CL;
   slice = (slice + 3) & ~3;
   if (slice < 4) slice = 4;
+  const int bits1 = hist ? csa::IDX_HBITS : csa::TK2_BITS1;
+  const bool merge = CL > 1 && !hist;
   const size_t budget = 200 * 1024;
-  const size_t fixed = (size_t)csa::TK2_BINS1 * 4 * (CL > 1 ? 2 : 1) + (size_t)slice * 4;
+  const size_t fixed = csa::topk2_smem_bytes(slice, 0, bits1, merge);
   if (fixed > budget) return CSA_ERR_UNSUPPORTED;
   int cand_cap = (int)((budget - fixed) / 4);
   if (cand_cap > slice) cand_cap = slice;
-  const size_t smem = (size_t)slice * 4 + (size_t)cand_cap * 4 + fixed - (size_t)slice * 4;
-  csa::Topk2Args a{scores, idx, Tq, N, k, m, q_pos0, slice, cand_cap};
-  if ((long long)rows * CL <= 2LL * sm_count()) return launch_topk2_nt<1024>(a, CL, rows, smem, st);
-  return launch_topk2_nt<512>(a, CL, rows, smem, st);
+  const size_t smem = csa::topk2_smem_bytes(slice, cand_cap, bits1, merge);
+  csa::Topk2Args a{scores, idx, Tq, N, k, m, q_pos0, slice, cand_cap, hist};
+  const bool wide = (long long)rows * CL <= 2LL * sm_count();
+  if (hist) return wide ? launch_topk2_nt<1024, csa::IDX_HBITS>(a, CL, rows, smem, st)
+                        : launch_topk2_nt<512, csa::IDX_HBITS>(a, CL, rows, smem, st);
+  return wide ? launch_topk2_nt<1024, csa::TK2_BITS1>(a, CL, rows, smem, st)
+              : launch_topk2_nt<512, csa::TK2_BITS1>(a, CL, rows, smem, st);
 }
 
 }  // namespace
@@ -448,9 +458,9 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
 }
 
 // ---------------------------------------------------------------------------
-csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
-                       const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
-                       int m, int q_pos0, int dtype, void* stream) {
+static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w, const void* K,
+                              const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
+                              int m, int q_pos0, int dtype, uint32_t* hist, void* stream) {
   if (B < 0 || Tq < 0 || N < 0 || H <= 0 || c <= 0 || m <= 0 || q_pos0 < 0)
     return CSA_ERR_INVALID_ARG;
   if (B == 0 || Tq == 0 || N == 0) return CSA_OK;
@@ -468,13 +478,13 @@ csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const 
     if (!aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4) || !aligned(scores, 4))
       return CSA_ERR_INVALID_ARG;
     if (H == 64 && c == 128)
-      return launch_index_tc<64, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
+      return launch_index_tc<64, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, hist, S(stream));
     if (H == 64 && c == 64)
-      return launch_index_tc<64, 64>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
+      return launch_index_tc<64, 64>(qI, w, K, scores, B, Tq, N, m, q_pos0, hist, S(stream));
     if (H == 32 && c == 128)
-      return launch_index_tc<32, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
+      return launch_index_tc<32, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, hist, S(stream));
     if (H == 128 && c == 128)
-      return launch_index_tc<128, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, S(stream));
+      return launch_index_tc<128, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, hist, S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
   if (dtype == CSA_DT_E2M1_BLOCK16) {
@@ -484,14 +494,52 @@ csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const 
       return CSA_ERR_INVALID_ARG;
     if (c != csa::FP4_C) return CSA_ERR_UNSUPPORTED;
     if (H == 64)
-      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, S(stream));
+      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, hist, S(stream));
     if (H == 32)
-      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, S(stream));
+      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, hist, S(stream));
     if (H == 128)
-      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, S(stream));
+      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, hist, S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
   return CSA_ERR_UNSUPPORTED;
+}
+
+csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
+                       const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
+                       int m, int q_pos0, int dtype, void* stream) {
+  return index_impl(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, H, c, m, q_pos0, dtype, nullptr, stream);
+}
+
+// ---------------------------------------------------------------------------
+static bool index_topk_fused(int B, int Tq, int N, int dtype) {
+  return B > 0 && Tq == 1 && N > 0 && N <= 16 * 32768 &&
+         (dtype == CSA_DT_BF16 || dtype == CSA_DT_E2M1_BLOCK16);
+}
+
+size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype) {
+  if (!index_topk_fused(B, Tq, N, dtype)) return 0;
+  return (size_t)B * Tq * csa::IDX_HBINS * sizeof(uint32_t);
+}
+
+csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, const void* K,
+                            const void* K_sf, float* scores, int32_t* idx, int B, int Tq, int N,
+                            int H, int c, int m, int q_pos0, int k, int dtype, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (k < 1 || k > 4096) return CSA_ERR_INVALID_ARG;
+  if (!index_topk_fused(B, Tq, N, dtype)) {
+    csa_status_t st = csa_index(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, H, c, m, q_pos0, dtype, stream);
+    if (st != CSA_OK) return st;
+    return csa_topk(scores, idx, B, Tq, N, k, m, q_pos0, stream);
+  }
+  if (!idx || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
+  const size_t need = csa_index_topk_workspace_size(B, Tq, N, dtype);
+  if (!ws || ws_bytes < need || !aligned(ws, 16)) return CSA_ERR_WORKSPACE;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws);
+  cudaError_t e = cudaMemsetAsync(hist, 0, need, S(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "csa_index_topk histogram clear");
+  csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, H, c, m, q_pos0, dtype, hist, stream);
+  if (st != CSA_OK) return st;
+  return launch_topk2(scores, idx, B * Tq, Tq, N, k, m, q_pos0, hist, S(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -507,7 +555,7 @@ csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, i
   // cluster; everything else up to 16 x 32768 entries: the candidate-filtering
   // selector (measured faster there: many short rows, and rows past 32768)
   if (!(N > 8192 && N <= 32768 && rows < 64) && N <= 16 * 32768)
-    return launch_topk2(scores, idx, rows, Tq, N, k, m, q_pos0, S(stream));
+    return launch_topk2(scores, idx, rows, Tq, N, k, m, q_pos0, nullptr, S(stream));
   // rows longer than 16 slices of 32768 keys: 8-bit radix passes over up to 16 SMs
   int CL = 1;
   if (N > 8192 && rows < 64) CL = rows <= 9 ? 16 : 8;

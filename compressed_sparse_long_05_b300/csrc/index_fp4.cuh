@@ -43,7 +43,8 @@ struct IndexFp4Smem {
   static constexpr int OFF_RAW_A = OFF_ATOM_B + 1024;        // [STAGES][RAW_PITCH]
   static constexpr int OFF_RAW_B = OFF_RAW_A + FP4_STAGES * RAW_PITCH;  // <= 128 x 8 B
   static constexpr int OFF_W = OFF_RAW_B + 1024;             // float w_s[4 warps][2][256]
-  static constexpr int OFF_BAR = OFF_W + 4 * 2 * 256 * 4;
+  static constexpr int OFF_HIST = OFF_W + 4 * 2 * 256 * 4;  // [4 warps][IDX_HBINS] u32
+  static constexpr int OFF_BAR = OFF_HIST + 4 * IDX_HBINS * 4;
   static constexpr int BYTES = OFF_BAR + 256 + 1024;         // + alignment slack
 };
 
@@ -277,6 +278,11 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q4 = warp & 3;
+    uint32_t* wh = reinterpret_cast<uint32_t*>(smem + L::OFF_HIST) + q4 * IDX_HBINS;
+    if (a.hist) {
+      for (int b = lane; b < IDX_HBINS; b += 32) wh[b] = 0;
+      __syncwarp();
+    }
     uint32_t iacc = 0, nitem = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
@@ -298,6 +304,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
             const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
             const int vis = vis32(a.q_pos0 + x.t0 + qi, a.m, a.N);
             if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
+            if (a.hist) hist_add(wh, acc, s < vis);
           }
           tc_fence_before();
           __syncwarp();
@@ -308,6 +315,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
             if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
         }
       }
+      if (a.hist && ok) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
     }
   }
 

@@ -39,7 +39,31 @@ struct IndexTcArgs {
   int chunks;            // work items per group
   int items;             // B * G * chunks
   uint32_t tmem_cols;    // allocated TMEM columns (power of 2 >= 2 * QT * H)
+  uint32_t* hist;        // optional [B * Tq][IDX_HBINS] key-digit histograms (QT == 1), zeroed
 };
+
+// Key-digit histogram of the scores, built in the index epilogue for the
+// top-k selector: bin = top IDX_HBITS bits of the order-preserving key.
+constexpr int IDX_HBITS = 11;
+constexpr int IDX_HBINS = 1 << IDX_HBITS;
+
+// One warp's visible scores of one tile into its shared histogram.
+CSA_DEVINL void hist_add(uint32_t* wh, float score, bool visible) {
+  const uint32_t am = __ballot_sync(0xffffffffu, visible);
+  if (visible) {
+    const uint32_t dig = float_to_key(score) >> (32 - IDX_HBITS);
+    const uint32_t peers = __match_any_sync(am, dig);
+    if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(wh + dig, (uint32_t)__popc(peers));
+  }
+}
+// One warp adds its shared histogram into the row's global one and clears it.
+CSA_DEVINL void hist_flush(uint32_t* wh, uint32_t* gh) {
+  for (int b = threadIdx.x & 31; b < IDX_HBINS; b += 32) {
+    const uint32_t c = wh[b];
+    if (c) { atomicAdd(gh + b, c); wh[b] = 0; }
+  }
+  __syncwarp();
+}
 
 // Shared-memory layout, sized at launch: S K-tile stages (4, or 6 when the
 // query group is at most 64 rows), the query group, head weights, barriers.
@@ -48,17 +72,20 @@ struct IndexSmem {
   static constexpr int MAX_STAGES = 6;
   static constexpr int A_BYTES = IDX_TILE * C * 2;       // one K tile
   static constexpr int KCH = C / 64;                     // 64-element swizzle chunks along c
-  int S, OFF_B, OFF_W, OFF_BAR, BYTES;
-  __host__ __device__ IndexSmem(int stages, int nqh) {
+  static constexpr int HIST_BYTES = 4 * IDX_HBINS * 4;   // one histogram per epilogue warp
+  int S, OFF_B, OFF_W, OFF_HIST, OFF_BAR, BYTES;
+  __host__ __device__ IndexSmem(int stages, int nqh, bool hist) {
     S = stages;
     OFF_B = S * A_BYTES;
     OFF_W = OFF_B + ((nqh * C * 2 + 1023) & ~1023);      // float w_s[4 warps][2][256]
-    OFF_BAR = OFF_W + 4 * 2 * 256 * 4;
+    OFF_HIST = OFF_W + 4 * 2 * 256 * 4;
+    OFF_BAR = OFF_HIST + (hist ? HIST_BYTES : 0);
     BYTES = OFF_BAR + 256 + 1024;                        // + alignment slack
   }
-  static constexpr int stages_for(int nqh) {
-    return (MAX_STAGES * A_BYTES + ((nqh * C * 2 + 1023) & ~1023) + 4 * 2 * 256 * 4 + 256 + 1024 <=
-            220 * 1024) ? MAX_STAGES : 4;
+  static int stages_for(int nqh, bool hist) {
+    for (int s = MAX_STAGES; s > 4; --s)
+      if (IndexSmem(s, nqh, hist).BYTES <= 224 * 1024) return s;
+    return 4;
   }
 };
 
@@ -126,7 +153,7 @@ __global__ void __launch_bounds__(IDX_THREADS, 1)
 index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant__ CUtensorMap tm_q,
                 IndexTcArgs a) {
   const int NQH = a.QT * H;                      // MMA N
-  const IndexSmem<H, C> L(a.stages, NQH);
+  const IndexSmem<H, C> L(a.stages, NQH, a.hist != nullptr);
   const int S = L.S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -244,6 +271,11 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q4 = warp & 3;                       // TMEM lane quarter of this warp
+    uint32_t* wh = reinterpret_cast<uint32_t*>(smem + L.OFF_HIST) + q4 * IDX_HBINS;
+    if (a.hist) {
+      for (int b = lane; b < IDX_HBINS; b += 32) wh[b] = 0;
+      __syncwarp();
+    }
     uint32_t iacc = 0, nitem = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
@@ -267,6 +299,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
             const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
             const int vis = vis32(a.q_pos0 + x.t0 + qi, a.m, a.N);
             if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
+            if (a.hist) hist_add(wh, acc, s < vis);
           }
           tc_fence_before();
           __syncwarp();
@@ -277,6 +310,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
             if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
         }
       }
+      if (a.hist && ok) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
     }
   }
 

@@ -25,9 +25,8 @@
 namespace csa {
 namespace cg2 = cooperative_groups;
 
-constexpr int TK2_BITS1 = 12;
-constexpr int TK2_BINS1 = 1 << TK2_BITS1;     // first digit: key bits 31..20
-constexpr int TK2_SHIFT1 = 32 - TK2_BITS1;
+constexpr int TK2_BITS1 = 12;                 // first digit when the kernel builds its histogram
+constexpr int TK2_MAXBINS = 1 << TK2_BITS1;
 
 struct Topk2Args {
   const float* scores;
@@ -35,12 +34,13 @@ struct Topk2Args {
   int Tq, N, k, m, q_pos0;
   int slice;      // keys per CTA (multiple of 4)
   int cand_cap;   // candidate capacity per CTA
+  const uint32_t* hist;   // optional [rows][2^BITS1] first-digit histograms of the visible scores
 };
 
-// dynamic shared memory: keys[slice] | cand[cand_cap] | hist1[BINS1] | (CL > 1) merged1[BINS1]
-template <int CL>
-__host__ __device__ constexpr size_t topk2_smem_bytes(int slice, int cand_cap) {
-  return (size_t)slice * 4 + (size_t)cand_cap * 4 + TK2_BINS1 * 4 + (CL > 1 ? TK2_BINS1 * 4 : 0);
+// dynamic shared memory: keys[slice] | cand[cand_cap] | hist1[2^BITS1] | merged1[2^BITS1]
+// (merged1 only when a cluster builds the histogram itself)
+__host__ __device__ constexpr size_t topk2_smem_bytes(int slice, int cand_cap, int bits1, bool merge) {
+  return (size_t)slice * 4 + (size_t)cand_cap * 4 + ((size_t)4 << bits1) * (merge ? 2 : 1);
 }
 
 // Exclusive prefix over the block of one int per thread (NT threads); returns
@@ -74,10 +74,13 @@ CSA_DEVINL int tk2_block_scan(int x, int* sh, int* total) {
   return r;
 }
 
-template <int NT, int CL>
+template <int NT, int CL, int BITS1>
 __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   pdl_enter();
   constexpr int NW = NT / 32;
+  constexpr int BINS1 = 1 << BITS1;
+  constexpr int SHIFT1 = 32 - BITS1;
+  const bool hist_in = a.hist != nullptr;
   extern __shared__ __align__(16) uint32_t tk_smem[];
   __shared__ uint32_t hist2[3][128];          // candidate-pass histograms (rank 0 merges)
   __shared__ int sh_scan[NW + 1];
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   uint32_t* keys = tk_smem;
   uint32_t* cand = keys + a.slice;
   uint32_t* hist1 = cand + a.cand_cap;
-  uint32_t* merged1 = hist1 + TK2_BINS1;               // CL > 1 only (rank 0's is the merge target)
+  uint32_t* merged1 = hist1 + BINS1;                   // cluster-built histograms only (rank 0 merges)
 
   const int lo = min(vis, rank * a.slice);
   const int hi = min(vis, lo + a.slice);
@@ -115,9 +118,14 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   const int seg = (((n + NW - 1) / NW) + 31) & ~31;
   const int s0 = min(n, wid * seg), s1 = min(n, s0 + seg);
 
-  for (int j = tid; j < TK2_BINS1; j += NT) hist1[j] = 0;
-  if (CL > 1 && rank == 0)
-    for (int j = tid; j < TK2_BINS1; j += NT) merged1[j] = 0;
+  if (hist_in) {
+    const uint32_t* gh = a.hist + (size_t)row * BINS1;
+    for (int j = tid; j < BINS1; j += NT) hist1[j] = __ldg(gh + j);
+  } else {
+    for (int j = tid; j < BINS1; j += NT) hist1[j] = 0;
+    if (CL > 1 && rank == 0)
+      for (int j = tid; j < BINS1; j += NT) merged1[j] = 0;
+  }
   if (tid < 3 * 128) (&hist2[0][0])[tid] = 0;
   if (tid == 0) sh_cand_n = 0;
   if constexpr (CL > 1) cluster.sync();
@@ -145,29 +153,30 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
         key = float_to_key(__uint_as_float(keys[j]));
         keys[j] = key;
       }
+      if (hist_in) continue;                          // the index kernel built the histogram
       const uint32_t am = __ballot_sync(0xffffffffu, act);
       if (act) {
-        const uint32_t dig = key >> TK2_SHIFT1;
+        const uint32_t dig = key >> SHIFT1;
         const uint32_t peers = __match_any_sync(am, dig);
         if (lane == __ffs(peers) - 1) atomicAdd(&hist1[dig], (uint32_t)__popc(peers));
       }
     }
   }
   __syncthreads();
-  if constexpr (CL > 1) {
+  if (CL > 1 && !hist_in) {
     uint32_t* dst = cluster.map_shared_rank(merged1, 0);
-    for (int b = tid; b < TK2_BINS1; b += NT) {
+    for (int b = tid; b < BINS1; b += NT) {
       const uint32_t c = hist1[b];
       if (c) atomicAdd(dst + b, c);
     }
     cluster.sync();
-    for (int b = tid; b < TK2_BINS1; b += NT) hist1[b] = dst[b];
+    for (int b = tid; b < BINS1; b += NT) hist1[b] = dst[b];
     __syncthreads();
   }
 
   // ---- 2. threshold bin: suffix counts over the first digit ----
   {
-    constexpr int PER = TK2_BINS1 / NT;               // bins per thread (>= 2)
+    constexpr int PER = BINS1 / NT;                   // bins per thread (>= 2)
     const int rt = NT - 1 - tid;                      // thread rt holds the highest bins first
     uint32_t c[PER];
     int part = 0;
@@ -202,7 +211,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   {
     // count this slice's b1 keys first (capacity check), then copy
     int mine = 0;
-    for (int j = s0 + lane; j < s1; j += 32) mine += (keys[j] >> TK2_SHIFT1) == b1;
+    for (int j = s0 + lane; j < s1; j += 32) mine += (keys[j] >> SHIFT1) == b1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
     if (lane == 0) atomicAdd(&sh_cand_n, mine);
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
       for (int j0 = s0; j0 < s1; j0 += 32) {
         const int j = j0 + lane;
         const uint32_t key = j < s1 ? keys[j] : 0u;
-        const bool in = j < s1 && (key >> TK2_SHIFT1) == b1;
+        const bool in = j < s1 && (key >> SHIFT1) == b1;
         const uint32_t bm = __ballot_sync(0xffffffffu, in);
         if (bm) {
           int base = 0;
@@ -232,12 +241,13 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   const int list_n = cand_ok ? ncand : n;
 
   // ---- 4. three radix passes over the candidates (or the b1-filtered slice) ----
-  uint32_t prefix = b1 << TK2_SHIFT1;
-  uint32_t pmask = 0xffffffffu << TK2_SHIFT1;
+  uint32_t prefix = b1 << SHIFT1;
+  uint32_t pmask = 0xffffffffu << SHIFT1;
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
-    const int sh = pass == 0 ? 13 : (pass == 1 ? 6 : 0);   // digits: bits 19..13, 12..6, 5..0
-    const int wd = pass == 2 ? 6 : 7;
+    // the SHIFT1 (20 or 21) remaining bits as digits of 7, 7 and 6 or 7 bits
+    const int sh = pass == 0 ? SHIFT1 - 7 : (pass == 1 ? SHIFT1 - 14 : 0);
+    const int wd = pass == 2 ? SHIFT1 - 14 : 7;
     const uint32_t dmask = (1u << wd) - 1u;
     uint32_t* h = hist2[pass];
     for (int j0 = 0; j0 < list_n; j0 += NT) {

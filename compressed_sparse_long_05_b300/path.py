@@ -26,6 +26,7 @@ class Buffers:
         self.idx = None
         self.out = None
         self.ws = None
+        self.ws_topk = None
 
 
 def _entries_arg(x):
@@ -63,9 +64,9 @@ def forward(cfg: dict, x: dict, buf: Buffers | None = None):
     win = _win_arg(x)
     if kind.startswith("csa"):
         qI, qI_sf, K, K_sf = _indexer_args(x)
-        buf.scores = L.csa_index(qI, x["w"], K, m, q_pos0, qI_sf=qI_sf, K_sf=K_sf,
-                                 scores=buf.scores)
-        buf.idx = L.csa_topk(buf.scores, cfg["k"], m, q_pos0, idx=buf.idx)
+        buf.scores, buf.idx, buf.ws_topk = L.csa_index_topk(
+            qI, x["w"], K, cfg["k"], m, q_pos0, qI_sf=qI_sf, K_sf=K_sf, scores=buf.scores,
+            idx=buf.idx, ws=buf.ws_topk)
         if buf.ws is None:
             n = L.attend_workspace_size(x["q"], entries, win, cfg["k"], m, n_win, q_pos0, r, False)
             buf.ws = L._workspace(None, n, x["q"].device)

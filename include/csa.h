@@ -92,7 +92,8 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
  *   dtype E2M1_BLOCK16: qI [B, Tq, H, c/2] bytes, qI_sf [B, Tq, H, c/16] bytes,
  *                       K [B, N, c/2] bytes, K_sf [B, N, c/16] bytes.
  *   w: [B, Tq, H] float32.  scores: [B, Tq, N] float32 (every element written).
- *   BF16 / E2M1 need H in {16,32,64,128}, c in {64,128}; F32 any H, c <= 256.
+ *   BF16 needs (H, c) in {(64,128), (64,64), (32,128), (128,128)}; E2M1 needs
+ *   H in {32,64,128}, c == 128; F32 any H, c <= 256.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
                        const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
@@ -108,6 +109,24 @@ csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const 
  * ------------------------------------------------------------------------- */
 csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, int k, int m,
                       int q_pos0, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_index_topk — csa_index followed by csa_topk in one call, with the same
+ * results (scores and index sets identical to the two separate calls).  For
+ * one query row per batch row (decode) in BF16 or E2M1_BLOCK16, the index
+ * kernel also counts each visible score's top 11 order-preserving key bits
+ * into a per-row histogram, so the selector starts from the threshold bin
+ * instead of building that histogram itself (§2.3.1 "Lightning Indexer" and
+ * "top-k selector").  Other shapes run the two stages unchanged.
+ *   ws / ws_bytes: scratch of csa_index_topk_workspace_size(B, Tq, N, dtype)
+ *   bytes (16-byte aligned; may be NULL when that size is 0).  The call clears
+ *   it on the stream before use; nothing in it must be initialised.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, const void* K,
+                            const void* K_sf, float* scores, int32_t* idx, int B, int Tq, int N,
+                            int H, int c, int m, int q_pos0, int k, int dtype, void* ws,
+                            size_t ws_bytes, void* stream);
+size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype);
 
 /* ---------------------------------------------------------------------------
  * csa_attend — shared-KV multi-query core attention (§2.3.1 "Shared KV MQA",

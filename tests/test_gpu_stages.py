@@ -361,3 +361,36 @@ def test_attend_mixed_rows(K, B, Tq, N, k, split):
             ref = O.csa_attend_token(f64(q[b, i]), t, e64, idx[b, i].cpu().numpy(), w64, win_base,
                                      f64(sink), m, n_win, r, 1e4)
             assert_close(f64(out[b, i]), ref, TOL_MIXED, TOL_MIXED, f"b={b} i={i}")
+
+
+# ----------------------------------------------------------------------------
+# index + top-k in one call (decode rows: histogram built by the index kernel)
+# ----------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("fmt,B,N,k", [
+    ("bf16", 3, 32768, 1024),       # 128K-context decode rows, one CTA per row
+    ("bf16", 2, 700, 1024),         # every visible entry selected (vis < k)
+    ("bf16", 1, 5001, 333),         # odd N
+    ("fp4", 2, 262144, 1024),       # 1M-context decode rows over an 8-CTA cluster
+    ("fp4", 1, 40001, 512),         # past 32768: cluster of 8, ragged slices
+])
+def test_index_topk_fused_matches_separate_calls(K, fmt, B, N, k):
+    m, H, c = 4, 64, 128
+    q_pos0 = 4 * N - 1
+    w = torch.rand((B, 1, H), generator=_gen(47), device=DEV) / H
+    if fmt == "bf16":
+        qI = _randn((B, 1, H, c), torch.bfloat16, 48, scale=c ** -0.5)
+        Kt = _randn((B, N, c), torch.bfloat16, 49, scale=c ** -0.5)
+        q_sf = k_sf = None
+    else:
+        qI, q_sf = _fp4((B, 1, H, c), 48, c ** -0.5)
+        Kt, k_sf = _fp4((B, N, c), 49, c ** -0.5)
+    s_ref = K.csa_index(qI, w, Kt, m, q_pos0, qI_sf=q_sf, K_sf=k_sf)
+    i_ref = K.csa_topk(s_ref, k, m, q_pos0)
+    s, i, _ = K.csa_index_topk(qI, w, Kt, k, m, q_pos0, qI_sf=q_sf, K_sf=k_sf)
+    torch.cuda.synchronize()
+    K.device_error()
+    assert torch.equal(s, s_ref)
+    assert torch.equal(i, i_ref)
+    _check_topk(s, i, k, m, q_pos0)
