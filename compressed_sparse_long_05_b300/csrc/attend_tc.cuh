@@ -26,15 +26,26 @@
 // bf16 and the row sums use the same rounded values.
 //
 // Warp roles (288 threads): warps 0-3 softmax / epilogue (one TMEM lane
-// quarter each), warps 4-7 gather (cp.async, 32 rows each, plus the RoPE of
-// the query and, unless the rows come pre-rotated, of the gathered rows),
-// warp 8 TMEM owner + MMA issuer.  Gathering chunk c of tile n+1 waits only
-// for the PV block that read it in tile n, so loads overlap the tail of PV.
+// quarter each), warps 4-7 gather (32 rows each), warp 8 TMEM owner + MMA
+// issuer.
+//   - bf16 rows are gathered by TMA tile::gather4 (four arbitrary rows x one
+//     128-byte box per instruction, landing already swizzled); the entries end
+//     at a multiple of 4 rows so every 4-row group comes from one tensor.
+//   - FP8 / BF16-RoPE rows are copied with cp.async (all of a tile at once)
+//     and widened to bf16 in place.
+//   - RoPE: when many query rows share few stored rows (prefill), every stored
+//     row is rotated once up front at its absolute position and the query is
+//     rotated at t (output rotated back at -t).  Otherwise (decode) each
+//     gathered row is rotated in shared memory by (position - t), so the query
+//     (loaded unrotated by TMA) and the output need no rotation.
+//   - The first tile of an item fetches each row's 1 KB together; later tiles
+//     refill each chunk pair as soon as the PV block that read it is done.
 //
 // A single-chunk item finishes in the kernel: divide by the softmax
-// denominator plus exp(sink), rotate the RoPE dims back by -t, store bf16.
+// denominator plus exp(sink), rotate the RoPE dims back if needed, store bf16.
 // A multi-chunk item (decode: few query rows, many rows each) stores its
-// unnormalised O^T, running max and denominator for attend_combine_kernel.
+// unnormalised O (staged in shared memory, one bulk copy when the CTA has one
+// item), running max and denominator for attend_combine_kernel.
 #pragma once
 #include <cuda_fp8.h>
 #include "tc.cuh"
@@ -46,7 +57,6 @@ constexpr int ATT_D = 512;
 constexpr int ATT_R = 64;
 constexpr int ATT_HG = 64;          // heads per CTA
 constexpr int ATT_TILE = 128;       // rows per tile
-constexpr int ATT_LAG = 6;          // cp.async chunk groups in flight per gather warp
 constexpr float ATT_TAU = 8.0f;     // lazy-rescale threshold (log2 units)
 
 struct AttendTcArgs {
@@ -157,19 +167,6 @@ CSA_DEVINL void cp_async16(uint32_t dst, const void* src, bool valid) {
 CSA_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 CSA_DEVINL void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-// wait until at most n (0..7) of this thread's cp.async groups are pending
-CSA_DEVINL void cp_async_wait_n(int n) {
-  switch (n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    case 6: cp_async_wait<6>(); break;
-    default: cp_async_wait<7>(); break;
-  }
-}
 
 // rotate the 4 (x0, x1) pairs of one 16-byte bf16 unit; pair p uses frequency j0 + p
 CSA_DEVINL uint4 rope_unit(uint4 v, long long pos, const RopeFreqs& rf, int j0) {
@@ -205,24 +202,19 @@ CSA_DEVINL void warp_reduce_scatter64(float* x, int lane) {
   }
 }
 
-// gather one 16-byte unit of a mixed-precision row (dims 8u..8u+7 of 512)
-CSA_DEVINL uint4 load_mixed_unit(const uint8_t* nope_row, float scale,
-                                 const __nv_bfloat16* rope_row, int unit) {
-  if (unit < (ATT_D - ATT_R) / 8) {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(nope_row + unit * 8));
-    float f[8];
-    const __nv_fp8x2_storage_t* p2 = reinterpret_cast<const __nv_fp8x2_storage_t*>(&raw);
+// eight e4m3 bytes times the row scale -> eight bf16 (one 16-byte unit)
+CSA_DEVINL uint4 e4m3x8_to_bf16(uint2 raw, float scale) {
+  float f[8];
+  const __nv_fp8x2_storage_t* p2 = reinterpret_cast<const __nv_fp8x2_storage_t*>(&raw);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(p2[e], __NV_E4M3);
-      __half2 h2 = *reinterpret_cast<__half2*>(&hr);
-      float2 v = __half22float2(h2);
-      f[2 * e] = v.x * scale;
-      f[2 * e + 1] = v.y * scale;
-    }
-    return f_to_bf16x8(f);
+  for (int e = 0; e < 4; ++e) {
+    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(p2[e], __NV_E4M3);
+    __half2 h2 = *reinterpret_cast<__half2*>(&hr);
+    float2 v = __half22float2(h2);
+    f[2 * e] = v.x * scale;
+    f[2 * e + 1] = v.y * scale;
   }
-  return __ldg(reinterpret_cast<const uint4*>(rope_row + (unit - (ATT_D - ATT_R) / 8) * 8));
+  return f_to_bf16x8(f);
 }
 
 __global__ void __launch_bounds__(ATT_THREADS, 1)
@@ -421,50 +413,58 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
           continue;
         }
-        for (int c = 0; c < 8 && ok; ++c) {
-          if ((c & 1) == 0 && !mbar_wait(chunk_free + (c >> 1), (n & 1) ^ 1, abort_flag)) { ok = false; break; }
-          uint8_t* dst_chunk = sE + c * 16384;
+        // ---- FP8 / BF16-RoPE rows (kv_mixed) ----
+        // Every copy of the tile goes out at once: the 64 e4m3 bytes of each
+        // 64-dim chunk (0..6) land in the upper half of the row's 128-byte
+        // slot, the RoPE dims (chunk 7) land as bf16 in place.  The e4m3 bytes
+        // are then widened to bf16 in place (times the row scale).
+        for (int c2 = 0; c2 < 4 && ok; ++c2)
+          if (!mbar_wait(chunk_free + c2, (n & 1) ^ 1, abort_flag)) ok = false;
+        if (!ok) break;
+#pragma unroll 1
+        for (int c = 0; c < 7; ++c) {
 #pragma unroll
-          for (int k2 = 0; k2 < 8; ++k2) {
-            const int rl = k2 * 4 + (lane >> 3);           // row within this warp's 32
-            const int u = lane & 7;
+          for (int k = 0; k < 4; ++k) {
+            const int rl = (k * 32 + lane) >> 2, u4 = lane & 3;
             const uint8_t* s_row = reinterpret_cast<const uint8_t*>(
                 __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src), rl));
-            const int tr = gw * 32 + rl;                   // tile row
-            const uint32_t dst = smem_u32(dst_chunk + tr * 128 + ((u ^ (tr & 7)) << 4));
-            if (!a.kv_mixed) {
-              cp_async16(dst, s_row ? s_row + c * 128 + u * 16 : reinterpret_cast<const uint8_t*>(a.q),
-                         s_row != nullptr);
-            } else {
-              const __nv_bfloat16* r_row = reinterpret_cast<const __nv_bfloat16*>(
-                  __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rsrc), rl));
-              const float sc = __shfl_sync(0xffffffffu, rscale, rl);
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (s_row) v = load_mixed_unit(s_row, sc, r_row, c * 8 + u);
-              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
-                           "r"(v.z), "r"(v.w)
-                           : "memory");
-            }
-          }
-          cp_async_commit();
-          if (c >= ATT_LAG) {
-            cp_async_wait<ATT_LAG>();
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(chunk_full + (c - ATT_LAG));
+            const uint32_t dst = smem_u32(sE + c * 16384 + (gw * 32 + rl) * 128 + 64 + u4 * 16);
+            cp_async16(dst, s_row ? s_row + c * 64 + u4 * 16 : reinterpret_cast<const uint8_t*>(a.q),
+                       s_row != nullptr);
           }
         }
-        if (!ok) break;
-        // release the remaining chunks as they land; chunk 7 (the RoPE dims) last
-        for (int c = 8 - ATT_LAG; c < 7; ++c) {
-          cp_async_wait_n(7 - c);
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(chunk_full + c);
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) {
+          const int rl = k2 * 4 + (lane >> 3), u = lane & 7;
+          const uint8_t* r_row = reinterpret_cast<const uint8_t*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rsrc), rl));
+          const int tr = gw * 32 + rl;
+          const uint32_t dst = smem_u32(sE + 7 * 16384 + tr * 128 + ((u ^ (tr & 7)) << 4));
+          cp_async16(dst, r_row ? r_row + u * 16 : reinterpret_cast<const uint8_t*>(a.q), r_row != nullptr);
         }
+        cp_async_commit();
         cp_async_wait<0>();
         __syncwarp();
-        if (a.rotate_rows) {
+#pragma unroll 1
+        for (int c = 0; c < 7; ++c) {
+          uint2 raw[8];
+#pragma unroll
+          for (int k2 = 0; k2 < 8; ++k2) {
+            const int tr = gw * 32 + k2 * 4 + (lane >> 3);
+            raw[k2] = *reinterpret_cast<const uint2*>(sE + c * 16384 + tr * 128 + 64 + (lane & 7) * 8);
+          }
+          __syncwarp();                                // every row's bytes read before any is overwritten
+#pragma unroll
+          for (int k2 = 0; k2 < 8; ++k2) {
+            const int rl = k2 * 4 + (lane >> 3), u = lane & 7;
+            const float sc = __shfl_sync(0xffffffffu, rscale, rl);
+            const int tr = gw * 32 + rl;
+            *reinterpret_cast<uint4*>(sE + c * 16384 + tr * 128 + ((u ^ (tr & 7)) << 4)) =
+                e4m3x8_to_bf16(raw[k2], sc);
+          }
+          __syncwarp();
+        }
+        {
           // RoPE of this warp's 32 rows: chunk 7 holds dims 448..511
           uint8_t* c7 = sE + 7 * 16384;
 #pragma unroll 2
@@ -479,7 +479,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(chunk_full + 7);
+        if (lane == 0)
+          for (int c = 0; c < 8; ++c) mbar_arrive(chunk_full + c);
       }
     }
   } else if (warp == 8) {

@@ -206,6 +206,7 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
   a.hist = a.QT == 1 ? hist : nullptr;
   const int nqh = a.QT * H;
   a.tmem_cols = 512;
+  a.nbuf = 4 * nqh <= 256 ? 4 : 2;   // accumulators in columns [0, 256); scale factors above
   CUtensorMap tmK, tmq, tmKs, tmqs;
   if (!tmap_u8_3d_sw64(&tmK, K, csa::FP4_ROWB, N, B, csa::FP4_ROWB, (uint64_t)N * csa::FP4_ROWB,
                        csa::IDX_TILE) ||
@@ -234,8 +235,11 @@ csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, floa
   if (st != CSA_OK) return st;
   const int sms = sm_count();
   const int nqh = a.QT * H;
+  // four accumulator buffers when they fit: the epilogue of one tile overlaps
+  // the MMAs of the next three
+  a.nbuf = 4 * nqh <= 512 ? 4 : 2;
   uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * nqh)) cols <<= 1;
+  while (cols < (uint32_t)(a.nbuf * nqh)) cols <<= 1;
   a.tmem_cols = cols;
   CUtensorMap tmK, tmq;
   if (!tmap_bf16_3d(&tmK, K, C, N, B, (uint64_t)C * 2, (uint64_t)N * C * 2, 64, csa::IDX_TILE) ||

@@ -45,7 +45,9 @@ struct IndexFp4Smem {
   static constexpr int OFF_W = OFF_RAW_B + 1024;             // float w_s[4 warps][2][256]
   static constexpr int OFF_HIST = OFF_W + 4 * 2 * 256 * 4;  // [4 warps][IDX_HBINS] u32
   static constexpr int OFF_BAR = OFF_HIST + 4 * IDX_HBINS * 4;
-  static constexpr int BYTES = OFF_BAR + 256 + 1024;         // + alignment slack
+  static constexpr int BAR_BYTES = 512;                      // 2 * STAGES + 8 + 3 barriers, flags
+  static constexpr int BYTES = OFF_BAR + BAR_BYTES + 1024;   // + alignment slack
+  static_assert((2 * FP4_STAGES + 11) * 8 + 8 <= BAR_BYTES, "barrier region");
 };
 
 // Instruction descriptor, kind::mxf4nvf4: A and B e2m1, K-major, ue4m3 scales, D f32.
@@ -133,9 +135,9 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* full = bars;                         // [STAGES]
   uint64_t* empty = bars + FP4_STAGES;           // [STAGES]
-  uint64_t* acc_full = bars + 2 * FP4_STAGES;    // [2]
-  uint64_t* acc_empty = acc_full + 2;            // [2]
-  uint64_t* b_full = acc_empty + 2;
+  uint64_t* acc_full = bars + 2 * FP4_STAGES;  // [nbuf <= 4]
+  uint64_t* acc_empty = acc_full + 4;            // [nbuf <= 4]
+  uint64_t* b_full = acc_empty + 4;
   uint64_t* b_free = b_full + 1;
   uint64_t* mma_done = b_free + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -148,7 +150,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < FP4_STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(acc_full + s, 1); mbar_init(acc_empty + s, 4); }
+    for (int s = 0; s < 4; ++s) { mbar_init(acc_full + s, 1); mbar_init(acc_empty + s, 4); }
     mbar_init(b_full, 1);
     mbar_init(b_free, 1);
     mbar_init(mma_done, 1);
@@ -236,7 +238,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
       }
       for (int j = x.j0; j < x.jv; ++j) {
         const uint32_t st = ia % FP4_STAGES, ph = (ia / FP4_STAGES) & 1;
-        const uint32_t buf = iacc & 1, aph = (iacc >> 1) & 1;
+        const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(acc_empty + buf, aph ^ 1, abort_flag))) { ok = false; break; }
         if (!__all_sync(0xffffffffu, mbar_wait(full + st, ph, abort_flag))) { ok = false; break; }
         {
@@ -296,7 +298,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
         const int s = j * IDX_TILE + q4 * 32 + lane;
         float* srow = a.scores + ((size_t)x.b * a.Tq + x.t0) * a.N + s;
         if (j < x.jv) {
-          const uint32_t buf = iacc & 1, aph = (iacc >> 1) & 1;
+          const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
           if (!mbar_wait(acc_full + buf, aph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;

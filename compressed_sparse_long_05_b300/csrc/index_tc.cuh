@@ -38,7 +38,8 @@ struct IndexTcArgs {
   int chunk_tiles;       // entry tiles per work item
   int chunks;            // work items per group
   int items;             // B * G * chunks
-  uint32_t tmem_cols;    // allocated TMEM columns (power of 2 >= 2 * QT * H)
+  uint32_t tmem_cols;    // allocated TMEM columns (power of 2 >= nbuf * QT * H)
+  int nbuf;              // accumulator buffers in tensor memory (2 or 4)
   uint32_t* hist;        // optional [B * Tq][IDX_HBINS] key-digit histograms (QT == 1), zeroed
 };
 
@@ -163,9 +164,9 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.OFF_BAR);
   uint64_t* full = bars;                         // [MAX_STAGES]
   uint64_t* empty = bars + L.MAX_STAGES;         // [MAX_STAGES]
-  uint64_t* acc_full = bars + 2 * L.MAX_STAGES;  // [2]
-  uint64_t* acc_empty = acc_full + 2;            // [2]
-  uint64_t* b_full = acc_empty + 2;
+  uint64_t* acc_full = bars + 2 * L.MAX_STAGES;  // [nbuf <= 4]
+  uint64_t* acc_empty = acc_full + 4;            // [nbuf <= 4]
+  uint64_t* b_full = acc_empty + 4;
   uint64_t* b_free = b_full + 1;
   uint64_t* mma_done = b_free + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -176,7 +177,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(acc_full + s, 1); mbar_init(acc_empty + s, 4); }
+    for (int s = 0; s < 4; ++s) { mbar_init(acc_full + s, 1); mbar_init(acc_empty + s, 4); }
     mbar_init(b_full, 1);
     mbar_init(b_free, 1);
     mbar_init(mma_done, 1);
@@ -243,7 +244,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         if (!mbar_wait(b_full, nitem & 1, abort_flag)) { ok = false; break; }
         for (int j = x.j0; j < x.jv; ++j) {
           const uint32_t st = ia % S, ph = (ia / S) & 1;
-          const uint32_t buf = iacc & 1, aph = (iacc >> 1) & 1;
+          const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
           if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag)) { ok = false; break; }
           if (!mbar_wait(full + st, ph, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -291,7 +292,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         const int s = j * IDX_TILE + q4 * 32 + lane;
         float* srow = a.scores + ((size_t)x.b * a.Tq + x.t0) * a.N + s;
         if (j < x.jv) {
-          const uint32_t buf = iacc & 1, aph = (iacc >> 1) & 1;
+          const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
           if (!mbar_wait(acc_full + buf, aph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
