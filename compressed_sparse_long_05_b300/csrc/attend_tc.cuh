@@ -244,6 +244,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint64_t* grp_b = bar + 22;        // softmax warps: sum partials (count 4)
   uint64_t* mma_done = bar + 23;
   uint64_t* c7_full = bar + 24;      // [4] per gather warp: its chunk-7 rows landed (TMA, RoPE after)
+  uint64_t* q_ready = bar + 28;      // absolute-RoPE mode: q rotated at t -> MMA (count 4)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttSmem::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttSmem::MISC + 4);
 
@@ -255,7 +256,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int s = 0; s < 2; ++s) { mbar_init(s_full + s, 1); mbar_init(s_free + s, 4); }
     mbar_init(p_full, 4);
     mbar_init(p_free, 1);
-    mbar_init(q_full, a.rel_rope ? 1 : 4);
+    mbar_init(q_full, 1);
+    mbar_init(q_ready, 4);
     mbar_init(q_free, 1);
     mbar_init(o_free, 4);
     mbar_init(grp_a, 4);
@@ -284,27 +286,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
       const AttRow x = att_item(a, it);
       if (x.r1 <= x.r0) continue;
-      // ---- queries of this head group, RoPE at t, swizzled K-major [64 heads][512] ----
-      // (relative-RoPE mode: the MMA warp loads them unrotated by TMA)
-      if (!a.rel_rope) {
-        if (!mbar_wait(q_free, (nitem & 1) ^ 1, abort_flag)) { ok = false; break; }
-        ++nitem;
-        const __nv_bfloat16* qrow0 =
-            a.q + (((size_t)x.b * a.Tq + x.i) * a.n_h + (size_t)x.hg * ATT_HG + gw * 16) * ATT_D;
-#pragma unroll 4
-        for (int k2 = 0; k2 < 32; ++k2) {
-          const int u_all = k2 * 32 + lane;          // 0..1023 over 16 heads x 64 units
-          const int hl = u_all >> 6, ur = u_all & 63;
-          const int c = ur >> 3, u = ur & 7;
-          uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow0 + (size_t)hl * ATT_D + ur * 8));
-          if (c == 7) v = rope_unit(v, x.t, a.rf, u * 4);
-          const int h = gw * 16 + hl;
-          *reinterpret_cast<uint4*>(sQ + c * 8192 + h * 128 + ((u ^ (h & 7)) << 4)) = v;
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(q_full);
-      }
       // ---- tiles ----
       for (int r0 = x.r0; r0 < x.r1 && ok; r0 += ATT_TILE, ++n) {
         // this lane's row: tile row gw*32 + lane
@@ -377,6 +358,21 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               }
             }
             __syncwarp();
+            if (!a.rel_rope) {
+              // absolute-RoPE mode: rotate this warp's 16 heads of the TMA-loaded
+              // queries (chunk 7 = dims 448..511) at t, then release them to the MMA
+              if (!mbar_wait(q_full, nitem & 1, abort_flag)) { ok = false; break; }
+              ++nitem;
+#pragma unroll
+              for (int k2 = 0; k2 < 4; ++k2) {
+                const int h = gw * 16 + k2 * 4 + (lane >> 3), u = lane & 7;
+                uint4* ptr = reinterpret_cast<uint4*>(sQ + 7 * 8192 + h * 128 + ((u ^ (h & 7)) << 4));
+                *ptr = rope_unit(*ptr, x.t, a.rf, u * 4);
+              }
+              fence_proxy_async();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(q_ready);
+            }
           } else {
             // later tiles: each chunk pair as soon as the PV block that read it is done
             for (int c = 0; c < 8 && ok; ++c) {
@@ -494,7 +490,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
         const AttRow x = att_item(a, it);
         if (x.r1 <= x.r0) continue;
-        if (a.rel_rope) {
+        {
           // queries of this head group: 8 boxes of [64 heads x 64 dims], 128-byte swizzled
           if (!mbar_wait(q_free, (nitem & 1) ^ 1, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(q_full, ATT_HG * ATT_D * 2);
@@ -502,7 +498,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
           for (int c = 0; c < 8; ++c) tma_load_3d(sQ + c * 8192, &tm_q, q_full, c * 64, qrow, 0);
         }
-        if (!mbar_wait(q_full, nitem & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(a.rel_rope ? q_full : q_ready, nitem & 1, abort_flag)) { ok = false; break; }
         const uint32_t item = nitem++;
         int j = 0;
         for (int r0 = x.r0; r0 < x.r1; r0 += ATT_TILE, ++n, ++j) {

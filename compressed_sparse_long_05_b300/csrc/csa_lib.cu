@@ -710,15 +710,14 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
   memset(&tmq, 0, sizeof(tmq));
   memset(&tment, 0, sizeof(tment));
   memset(&tmwin, 0, sizeof(tmwin));
+  if (!tmap_bf16_3d(&tmq, q, csa::ATT_D, (uint64_t)B * Tq * n_h, 1, (uint64_t)csa::ATT_D * 2,
+                    (uint64_t)B * Tq * n_h * csa::ATT_D * 2, 64, csa::ATT_HG))
+    return CSA_ERR_UNSUPPORTED;
   if (a.tma_rows &&
       ((N > 0 && !tmap_bf16_rows(&tment, a.ent, (uint64_t)B * N)) ||
        !tmap_bf16_rows(&tmwin, a.win, (uint64_t)B * T_win)))
     return CSA_ERR_UNSUPPORTED;
   if (a.tma_rows && N == 0) tment = tmwin;   // no entry groups exist; any valid map
-  if (p.rel_rope &&
-      !tmap_bf16_3d(&tmq, q, csa::ATT_D, (uint64_t)B * Tq * n_h, 1, (uint64_t)csa::ATT_D * 2,
-                    (uint64_t)B * Tq * n_h * csa::ATT_D * 2, 64, csa::ATT_HG))
-    return CSA_ERR_UNSUPPORTED;
   const int smem = csa::AttSmem::BYTES;
   cudaError_t e = cudaFuncSetAttribute(csa::attend_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
