@@ -217,6 +217,13 @@ class ClockSampler:
         return res
 
 
+def max_over_ranks(value, device):
+    """The largest of every rank's value (all ranks get it): the slowest rank's time counts."""
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def make_step(K, cfg, x, buf):
     """Stage callables of one step on inputs x (device tensors) with buffers buf."""
     from compressed_sparse_long_05_b300 import path as P
@@ -372,9 +379,7 @@ def gpu_arm(args, cfg, rank, world):
     torch.cuda.synchronize()
     ms_total = e0.elapsed_time(e1)
     if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
+        ms_total = max_over_ranks(ms_total, dev)
         torch.distributed.barrier()
     K.device_error()
 
@@ -556,8 +561,8 @@ def reference_arm(args, cfg, rank, world):
     # the oracle is slow by design: run a bounded number of sample steps
     # (one short warm-up, then up to 3 timed samples of ~15 s) whatever K is
     run_steps = max(1, min(args.steps, 3))
-    per_step_budget = 15.0
-    oracle_sample(cfg, xn, 1.0)
+    per_step_budget = args.cpu_budget
+    oracle_sample(cfg, xn, min(1.0, per_step_budget))
     vals = []
     desc, threads = "", 1
     for s in range(run_steps):
