@@ -14,7 +14,8 @@ __device__ unsigned int g_csa_error_word;
 enum : unsigned int {
   ERRBIT_TIMEOUT = 1u,      // a bounded mbarrier wait gave up
   ERRBIT_BAD_INDEX = 2u,    // an index list held an entry >= N
-  ERRBIT_TMEM = 4u          // tensor-memory allocation returned an unusable address
+  ERRBIT_TMEM = 4u,         // tensor-memory allocation returned an unusable address
+  ERRBIT_HIST = 8u          // a key-digit histogram disagreed with the scores it describes
 };
 
 CSA_DEVINL void csa_flag_error(unsigned int bit) { atomicOr(&g_csa_error_word, bit); }

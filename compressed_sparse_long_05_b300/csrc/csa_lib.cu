@@ -206,7 +206,9 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
   a.hist = a.QT == 1 ? hist : nullptr;
   const int nqh = a.QT * H;
   a.tmem_cols = 512;
-  a.nbuf = 4 * nqh <= 256 ? 4 : 2;   // accumulators in columns [0, 256); scale factors above
+  // accumulator buffers in columns [0, 256), scale factors above; the two
+  // epilogue groups take alternate buffers
+  a.nbuf = 4 * nqh <= 256 ? 4 : 2;
   CUtensorMap tmK, tmq, tmKs, tmqs;
   if (!tmap_u8_3d_sw64(&tmK, K, csa::FP4_ROWB, N, B, csa::FP4_ROWB, (uint64_t)N * csa::FP4_ROWB,
                        csa::IDX_TILE) ||
@@ -221,7 +223,7 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
   if (e != cudaSuccess) return cuda_fail(e, "csa_index fp4 attr");
   const int sms = sm_count();
   const int grid = a.items < sms ? a.items : sms;
-  e = launch_ex(kern, dim3(grid), dim3(csa::IDX_THREADS), smem, stream, 1, tmK, tmq, tmKs, tmqs, fa);
+  e = launch_ex(kern, dim3(grid), dim3(csa::FP4_THREADS), smem, stream, 1, tmK, tmq, tmKs, tmqs, fa);
   if (e != cudaSuccess) return cuda_fail(e, "csa_index fp4 launch");
   return CSA_OK;
 }

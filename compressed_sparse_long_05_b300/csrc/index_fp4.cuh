@@ -17,17 +17,26 @@
 // tensor-memory scale atoms (row r = 32g + i of a 128-row block at byte
 // 16 i + 4 g + k for the k-th 16-element block of the MMA's K range) ->
 // tcgen05.cp into tensor memory (32x128b, replicated to the four lane
-// quarters).  fp32 accumulators are double-buffered in tensor memory; the
-// epilogue folds the heads with ReLU * w exactly as the bf16 kernel does.
+// quarters).  fp32 accumulators rotate through up to four tensor-memory
+// buffers; the epilogue folds the heads with ReLU * w exactly as the bf16
+// kernel does.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + scale
-// rearrangement + MMA issuer, warps 2-5 epilogue.
+// Warp roles (384 threads), each step of the per-tile chain on its own warps so
+// that no step's latency sits inside another's loop:
+//   warp 0      TMA producer (K tile + its scale rows, 12 stages),
+//   warp 1      TMEM owner; one lane issues the MMAs,
+//   warps 2, 3  scale rearrangement (raw rows -> atoms -> tcgen05.cp into
+//               tensor memory) of alternate tiles, running ahead of the MMA,
+//   warps 4-11  epilogue, two groups of four warps (one per TMEM lane
+//               quarter) taking alternate tiles.
 #pragma once
 #include "index_tc.cuh"
 
 namespace csa {
 
-constexpr int FP4_STAGES = 8;
+constexpr int FP4_STAGES = 12;
+constexpr int FP4_THREADS = 384;
+constexpr int FP4_EPI_WARP0 = 4;           // first epilogue warp (warps 2, 3 rearrange scales)
 constexpr int FP4_C = 128;                  // indexer dim (elements)
 constexpr int FP4_ROWB = FP4_C / 2;         // packed bytes per row
 constexpr int FP4_SF_BOX = 130;             // uint64 scale rows per stage load (128 + 2 for alignment)
@@ -42,12 +51,13 @@ struct IndexFp4Smem {
   static constexpr int OFF_ATOM_B = OFF_ATOM_A + FP4_STAGES * 1024;   // [2][512]
   static constexpr int OFF_RAW_A = OFF_ATOM_B + 1024;        // [STAGES][RAW_PITCH]
   static constexpr int OFF_RAW_B = OFF_RAW_A + FP4_STAGES * RAW_PITCH;  // <= 128 x 8 B
-  static constexpr int OFF_W = OFF_RAW_B + 1024;             // float w_s[4 warps][2][256]
-  static constexpr int OFF_HIST = OFF_W + 4 * 2 * 256 * 4;  // [4 warps][IDX_HBINS] u32
+  static constexpr int OFF_W = OFF_RAW_B + 1024;             // float w_s[8 warps][2][256]
+  static constexpr int OFF_HIST = OFF_W + 8 * 2 * 256 * 4;  // [4 lane quarters][IDX_HBINS] u32
   static constexpr int OFF_BAR = OFF_HIST + 4 * IDX_HBINS * 4;
-  static constexpr int BAR_BYTES = 512;                      // 2 * STAGES + 8 + 3 barriers, flags
+  static constexpr int NBAR = 3 * FP4_STAGES + 8 + 7;        // stage, accumulator, item barriers
+  static constexpr int BAR_BYTES = 512;
   static constexpr int BYTES = OFF_BAR + BAR_BYTES + 1024;   // + alignment slack
-  static_assert((2 * FP4_STAGES + 11) * 8 + 8 <= BAR_BYTES, "barrier region");
+  static_assert(NBAR * 8 + 8 <= BAR_BYTES, "barrier region");
 };
 
 // Instruction descriptor, kind::mxf4nvf4: A and B e2m1, K-major, ue4m3 scales, D f32.
@@ -117,7 +127,7 @@ struct IndexFp4Args {
 };
 
 template <int H>
-__global__ void __launch_bounds__(IDX_THREADS, 1)
+__global__ void __launch_bounds__(FP4_THREADS, 1)
 index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_Ksf, const __grid_constant__ CUtensorMap tm_qsf,
                  IndexFp4Args fa) {
@@ -133,33 +143,49 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
   uint8_t* rawB = smem + L::OFF_RAW_B;
   float* w_s = reinterpret_cast<float*>(smem + L::OFF_W);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* full = bars;                         // [STAGES]
-  uint64_t* empty = bars + FP4_STAGES;           // [STAGES]
-  uint64_t* acc_full = bars + 2 * FP4_STAGES;  // [nbuf <= 4]
-  uint64_t* acc_empty = acc_full + 4;            // [nbuf <= 4]
-  uint64_t* b_full = acc_empty + 4;
-  uint64_t* b_free = b_full + 1;
+  uint64_t* full = bars;                          // [STAGES] K tile + scale rows landed (TMA)
+  uint64_t* sf_ready = bars + FP4_STAGES;         // [STAGES] scale atoms of the stage in tensor memory (commit)
+  uint64_t* empty = bars + 2 * FP4_STAGES;        // [STAGES] MMA read the stage (commit)
+  uint64_t* acc_full = bars + 3 * FP4_STAGES;     // [nbuf <= 4] accumulator written (commit)
+  uint64_t* acc_empty = acc_full + 4;             // [nbuf <= 4] read by the owning epilogue group
+  uint64_t* b_full = acc_empty + 4;               // query group + its scale rows landed (TMA)
+  uint64_t* b_ready = b_full + 1;                 // query scale atoms in tensor memory (commit)
+  uint64_t* b_free = b_ready + 1;                 // every MMA of the item done (commit)
   uint64_t* mma_done = b_free + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* epi_sync = mma_done + 1;              // the 8 epilogue warps at an item's end (count 8)
+  uint64_t* cp_done = epi_sync + 1;               // [2] each scale warp's last copies (commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cp_done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NQH = a.QT * H;                      // MMA N (<= 128)
-  // tensor-memory columns: accumulators [0, 2*NQH), A scales, B scales
+  const int NQH = a.QT * H;                       // MMA N (<= 128)
+  // tensor-memory columns: accumulators [0, nbuf*NQH) within [0, 256), A scales, B scales
   const uint32_t TM_SFA = 256, TM_SFB = 256 + FP4_STAGES * 8;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < FP4_STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
+    for (int s = 0; s < FP4_STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(sf_ready + s, 1);
+      mbar_init(empty + s, 1);
+    }
     for (int s = 0; s < 4; ++s) { mbar_init(acc_full + s, 1); mbar_init(acc_empty + s, 4); }
     mbar_init(b_full, 1);
+    mbar_init(b_ready, 1);
     mbar_init(b_free, 1);
     mbar_init(mma_done, 1);
+    mbar_init(epi_sync, 8);
+    mbar_init(cp_done, 1);
+    mbar_init(cp_done + 1, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
+  }
+  if (a.hist) {
+    uint32_t* h = reinterpret_cast<uint32_t*>(smem + L::OFF_HIST);
+    for (int b = threadIdx.x; b < 4 * IDX_HBINS; b += blockDim.x) h[b] = 0;
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_K); prefetch_tmap(&tm_q); prefetch_tmap(&tm_Ksf); prefetch_tmap(&tm_qsf);
@@ -219,43 +245,24 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
       if (b_issued) mbar_drain(b_full, (nitem - 1) & 1);
     }
   } else if (warp == 1) {
-    // ---------------- scale atoms + MMA issuer (whole warp) ----------------
-    uint32_t ia = 0, iacc = 0, nitem = 0;
-    bool ok = true;
-    const uint32_t idesc = idesc_mxf4(IDX_TILE, NQH);
-    for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
-      const IdxItem x = idx_item(a, it);
-      if (x.jv <= x.j0) continue;
-      // every lane waits and the warp votes, so all 32 lanes leave together on a timeout
-      if (!__all_sync(0xffffffffu, mbar_wait(b_full, nitem & 1, abort_flag))) { ok = false; break; }
-      build_scale_atoms(rawB, atomB, NQH, lane);
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        tc_fence_after();
-        tmem_cp_32x128b_x4(tmem + TM_SFB, sdesc_atom(smem_u32(atomB)));
-        tmem_cp_32x128b_x4(tmem + TM_SFB + 4, sdesc_atom(smem_u32(atomB + 512)));
-      }
-      for (int j = x.j0; j < x.jv; ++j) {
-        const uint32_t st = ia % FP4_STAGES, ph = (ia / FP4_STAGES) & 1;
-        const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(acc_empty + buf, aph ^ 1, abort_flag))) { ok = false; break; }
-        if (!__all_sync(0xffffffffu, mbar_wait(full + st, ph, abort_flag))) { ok = false; break; }
-        {
-          const long long r0 = (long long)x.b * a.N + (long long)j * IDX_TILE;
-          const uint8_t* raw = rawA + st * L::RAW_PITCH + (r0 & 1) * 8;
-          const int nrows = (int)min((long long)IDX_TILE, (long long)a.N - (long long)j * IDX_TILE);
-          build_scale_atoms(raw, atomA + st * 1024, nrows, lane);
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
+    // ---------------- MMA issuer (one lane) ----------------
+    if (lane == 0) {
+      uint32_t ia = 0, iacc = 0, nitem = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_mxf4(IDX_TILE, NQH);
+      const uint32_t bBase = smem_u32(sB);
+      for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+        const IdxItem x = idx_item(a, it);
+        if (x.jv <= x.j0) continue;
+        if (!mbar_wait(b_ready, nitem & 1, abort_flag)) { ok = false; break; }
+        for (int j = x.j0; j < x.jv; ++j) {
+          const uint32_t st = ia % FP4_STAGES, ph = (ia / FP4_STAGES) & 1;
+          const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
+          if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(sf_ready + st, ph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfa = tmem + TM_SFA + st * 8;
-          tmem_cp_32x128b_x4(sfa, sdesc_atom(smem_u32(atomA + st * 1024)));
-          tmem_cp_32x128b_x4(sfa + 4, sdesc_atom(smem_u32(atomA + st * 1024 + 512)));
           const uint32_t aBase = smem_u32(sA + st * L::A_BYTES);
-          const uint32_t bBase = smem_u32(sB);
           const uint32_t d = tmem + buf * (uint32_t)NQH;
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
@@ -263,33 +270,78 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
                       sfa + kk * 4, tmem + TM_SFB + kk * 4, kk > 0 ? 1u : 0u);
           umma_commit(empty + st);
           umma_commit(acc_full + buf);
+          ++ia;
+          ++iacc;
         }
-        __syncwarp();
-        ++ia;
-        ++iacc;
+        if (!ok) break;
+        umma_commit(b_free);
+        ++nitem;
       }
-      if (lane == 0) umma_commit(b_free);
-      __syncwarp();
-      ++nitem;
-    }
-    if (lane == 0) {
       umma_commit(mma_done);
       mbar_drain(mma_done, 0);
     }
-    __syncwarp();
-  } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const int q4 = warp & 3;
-    uint32_t* wh = reinterpret_cast<uint32_t*>(smem + L::OFF_HIST) + q4 * IDX_HBINS;
-    if (a.hist) {
-      for (int b = lane; b < IDX_HBINS; b += 32) wh[b] = 0;
-      __syncwarp();
-    }
-    uint32_t iacc = 0, nitem = 0;
+  } else if (warp < FP4_EPI_WARP0) {
+    // ---------------- scale rearrangement (whole warps; warp 2 even tiles, warp 3 odd) ----------------
+    const uint32_t sw = warp - 2;
+    uint32_t ia = 0, nitem = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
       const IdxItem x = idx_item(a, it);
-      float* ws = w_s + ((q4 * 2) + (nitem & 1)) * 256;
+      if (x.jv <= x.j0) continue;
+      if (sw == 0) {
+        // every lane waits and the warp votes, so all 32 lanes leave together on a timeout
+        if (!__all_sync(0xffffffffu, mbar_wait(b_full, nitem & 1, abort_flag))) { ok = false; break; }
+        build_scale_atoms(rawB, atomB, NQH, lane);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          // these warps also move the atoms into tensor memory; the commit tells the
+          // MMA lane when the copies are done
+          tc_fence_after();
+          tmem_cp_32x128b_x4(tmem + TM_SFB, sdesc_atom(smem_u32(atomB)));
+          tmem_cp_32x128b_x4(tmem + TM_SFB + 4, sdesc_atom(smem_u32(atomB + 512)));
+          umma_commit(b_ready);
+        }
+        __syncwarp();
+      }
+      for (int j = x.j0; j < x.jv; ++j, ++ia) {
+        if ((ia & 1) != sw) continue;
+        const uint32_t st = ia % FP4_STAGES, ph = (ia / FP4_STAGES) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(full + st, ph, abort_flag))) { ok = false; break; }
+        const long long r0 = (long long)x.b * a.N + (long long)j * IDX_TILE;
+        const uint8_t* raw = rawA + st * L::RAW_PITCH + (r0 & 1) * 8;
+        const int nrows = (int)min((long long)IDX_TILE, (long long)a.N - (long long)j * IDX_TILE);
+        build_scale_atoms(raw, atomA + st * 1024, nrows, lane);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sfa = tmem + TM_SFA + st * 8;
+          tmem_cp_32x128b_x4(sfa, sdesc_atom(smem_u32(atomA + st * 1024)));
+          tmem_cp_32x128b_x4(sfa + 4, sdesc_atom(smem_u32(atomA + st * 1024 + 512)));
+          umma_commit(sf_ready + st);
+        }
+        __syncwarp();
+      }
+      ++nitem;
+    }
+    // every tensor-memory copy this warp issued is done before the CTA frees tensor memory
+    if (lane == 0) {
+      umma_commit(cp_done + sw);
+      mbar_drain(cp_done + sw, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 4..11: two groups, alternate tiles) ----------------
+    const int ew = warp - FP4_EPI_WARP0;             // 0..7
+    const int grp = ew >> 2;                         // tiles with iacc % 2 == grp
+    const int q4 = warp & 3;                         // TMEM lane quarter this warp may access
+    uint32_t* wh = reinterpret_cast<uint32_t*>(smem + L::OFF_HIST) + q4 * IDX_HBINS;   // shared by both groups
+    uint32_t iacc = 0, nitem = 0, nsync = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+      const IdxItem x = idx_item(a, it);
+      float* ws = w_s + ((ew * 2) + (nitem & 1)) * 256;
       for (int e = lane; e < x.nq * H; e += 32)
         ws[e] = __ldg(a.w + ((size_t)x.b * a.Tq + x.t0) * H + e);
       __syncwarp();
@@ -298,7 +350,10 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
         const int s = j * IDX_TILE + q4 * 32 + lane;
         float* srow = a.scores + ((size_t)x.b * a.Tq + x.t0) * a.N + s;
         if (j < x.jv) {
+          const uint32_t mine = (iacc & 1) == (uint32_t)grp;
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
+          ++iacc;
+          if (!mine) continue;
           if (!mbar_wait(acc_full + buf, aph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
@@ -311,13 +366,26 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + buf);
-          ++iacc;
-        } else {
+        } else if ((j & 1) == grp) {
           for (int qi = 0; qi < x.nq; ++qi)
             if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
         }
       }
-      if (a.hist && ok) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
+      if (a.hist) {
+        // both groups have added this item's scores: one group flushes (and clears)
+        // the shared per-quarter histograms; the next item's adds wait for that.
+        // Bounded waits: a warp that gave up still arrives, and the flag ends the rest.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_sync);
+        const bool s1 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
+        ++nsync;
+        if (ok && s1 && grp == 0) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_sync);
+        const bool s2 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
+        ++nsync;
+        if (!s1 || !s2) ok = false;
+      }
     }
   }
 

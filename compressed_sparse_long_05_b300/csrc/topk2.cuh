@@ -127,7 +127,11 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
       for (int j = tid; j < BINS1; j += NT) merged1[j] = 0;
   }
   if (tid < 3 * 128) (&hist2[0][0])[tid] = 0;
-  if (tid == 0) sh_cand_n = 0;
+  if (tid == 0) {
+    sh_cand_n = 0;
+    sh_sel[0] = 0xffffffffu;                          // no threshold bin found (yet)
+    sh_sel[1] = 0u;
+  }
   if constexpr (CL > 1) cluster.sync();
   else __syncthreads();
 
@@ -201,6 +205,15 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
       }
     }
     __syncthreads();
+  }
+  if (sh_sel[0] == 0xffffffffu) {
+    // the histogram holds fewer than k keys: it does not describe these scores
+    // (only a broken caller-side histogram gets here).  Flag it and leave the
+    // row empty rather than select from a wrong threshold.
+    if (tid == 0 && rank == 0) csa_flag_error(ERRBIT_HIST);
+    for (int j = rank * NT + tid; j < a.k; j += CL * NT) orow[j] = -1;
+    if constexpr (CL > 1) cluster.sync();             // no rank leaves while peers may map its memory
+    return;
   }
   const uint32_t b1 = sh_sel[0];
   uint32_t krem = sh_sel[1];
@@ -359,7 +372,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
     const bool take = j < s1 && (key > T || (key == T && e_lt < q_eq));
     if (take) {
       const int pos = g_lt + min(q_eq, e_lt);
-      if (pos < a.k) orow[pos] = lo + j;
+      if (pos >= 0 && pos < a.k) orow[pos] = lo + j;
     }
     gt_before += __popc(gm);
     eq_before += __popc(em);

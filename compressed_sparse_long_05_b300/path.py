@@ -79,3 +79,48 @@ def forward(cfg: dict, x: dict, buf: Buffers | None = None):
         buf.out = L.hca_attend(x["q"], entries, win, x["sink"], m, n_win, win_base, q_pos0, r,
                                base, out=buf.out, ws=buf.ws)
     return buf.out
+
+
+class GraphForward:
+    """A layer forward replayed as one CUDA graph, host transfers included.
+
+    For a decode loop whose per-step work is tens of microseconds, launching
+    each stage from Python costs more than the stages.  This captures, once:
+    the copy of every name in ``host_inputs`` from its pinned host buffer into
+    the device input, every stage of :func:`forward`, and the copy of the
+    output back into a pinned host tensor.  Each call then replays the graph
+    and waits for it.  The caller refreshes ``self.host[name]`` in place
+    between calls (the graph reads those exact buffers) and reads the returned
+    host output before the next call overwrites it.
+
+    ``x`` holds the device inputs the graph reads and writes; they and the
+    buffers stay owned by this object for its lifetime.
+    """
+
+    def __init__(self, cfg: dict, x: dict, host_inputs, stream=None):
+        import torch
+        self.cfg = cfg
+        self.x = dict(x)
+        self.host = {n: self.x[n].cpu().pin_memory() for n in host_inputs}
+        self.buf = Buffers()
+        self.stream = stream or torch.cuda.Stream()
+        with torch.cuda.stream(self.stream):
+            forward(cfg, self.x, self.buf)          # sizes every buffer before capture
+        self.out_host = torch.empty(self.buf.out.shape, dtype=self.buf.out.dtype).pin_memory()
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream, capture_error_mode="relaxed"):
+            for n, t in self.host.items():
+                self.x[n].copy_(t, non_blocking=True)
+            forward(cfg, self.x, self.buf)
+            self.out_host.copy_(self.buf.out, non_blocking=True)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
+        self.d2h_bytes = self.out_host.numel() * self.out_host.element_size()
+
+    def __call__(self):
+        """Runs one forward on the current host inputs; returns the pinned host output."""
+        import torch
+        with torch.cuda.stream(self.stream):      # replay() launches on the current stream
+            self.graph.replay()
+        self.stream.synchronize()
+        return self.out_host

@@ -374,6 +374,8 @@ def test_attend_mixed_rows(K, B, Tq, N, k, split):
     ("bf16", 1, 5001, 333),         # odd N
     ("fp4", 2, 262144, 1024),       # 1M-context decode rows over an 8-CTA cluster
     ("fp4", 1, 40001, 512),         # past 32768: cluster of 8, ragged slices
+    ("fp4", 200, 3000, 512),        # more rows than SMs: CTAs flush two rows' histograms
+    ("bf16", 200, 3000, 512),
 ])
 def test_index_topk_fused_matches_separate_calls(K, fmt, B, N, k):
     m, H, c = 4, 64, 128
