@@ -336,26 +336,30 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           // their region and are masked above.
           const int wrow0 = r0 + gw * 32;
           const int coord = trow >= 0 ? trow : (wrow0 + lane >= x.nsel4 ? x.b * a.T_win : x.b * a.N);
-          int cr[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) cr[j] = __shfl_sync(0xffffffffu, coord, j);
+          // lane g (< 8) issues the copies of row group g (rows 4g..4g+3 of this warp):
+          // eight issuing lanes keep more gathers in flight than one
+          const int g8 = lane & 7;
+          const int cr0 = __shfl_sync(0xffffffffu, coord, 4 * g8);
+          const int cr1 = __shfl_sync(0xffffffffu, coord, 4 * g8 + 1);
+          const int cr2 = __shfl_sync(0xffffffffu, coord, 4 * g8 + 2);
+          const int cr3 = __shfl_sync(0xffffffffu, coord, 4 * g8 + 3);
+          const CUtensorMap* gmap = wrow0 + 4 * g8 >= x.nsel4 ? &tm_win : &tm_ent;
           if (r0 == x.r0) {
             // first tile of the item: every chunk pair is free once the last PV of
             // the previous item is done; fetch each row's 1 KB together
             for (int c2 = 0; c2 < 4 && ok; ++c2)
               if (!mbar_wait(chunk_free + c2, (n & 1) ^ 1, abort_flag)) ok = false;
             if (!ok) break;
-            if (lane == 0) {
+            if (lane == 0)
               for (int c = 0; c < 8; ++c)
                 mbar_arrive_expect_tx((c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, 32 * 128);
-              for (int g = 0; g < 8; ++g) {
-                const CUtensorMap* map = wrow0 + 4 * g >= x.nsel4 ? &tm_win : &tm_ent;
+            __syncwarp();
+            if (lane < 8) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                  tma_gather4(sE + c * 16384 + (gw * 32 + 4 * g) * 128, map,
-                              (c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, c * 64,
-                              cr[4 * g], cr[4 * g + 1], cr[4 * g + 2], cr[4 * g + 3]);
-              }
+              for (int c = 0; c < 8; ++c)
+                tma_gather4(sE + c * 16384 + (gw * 32 + 4 * g8) * 128, gmap,
+                            (c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, c * 64,
+                            cr0, cr1, cr2, cr3);
             }
             __syncwarp();
             if (!a.rel_rope) {
@@ -375,16 +379,18 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
           } else {
             // later tiles: each chunk pair as soon as the PV block that read it is done
-            for (int c = 0; c < 8 && ok; ++c) {
-              if ((c & 1) == 0 && !mbar_wait(chunk_free + (c >> 1), (n & 1) ^ 1, abort_flag)) { ok = false; break; }
-              uint64_t* bar_c = (c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c;
-              if (lane == 0) {
-                mbar_arrive_expect_tx(bar_c, 32 * 128);
-                uint8_t* dst = sE + c * 16384 + gw * 32 * 128;
+            for (int c2 = 0; c2 < 4 && ok; ++c2) {
+              if (!mbar_wait(chunk_free + c2, (n & 1) ^ 1, abort_flag)) { ok = false; break; }
+              if (lane == 0)
+                for (int c = 2 * c2; c < 2 * c2 + 2; ++c)
+                  mbar_arrive_expect_tx((c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, 32 * 128);
+              __syncwarp();
+              if (lane < 8) {
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                  tma_gather4(dst + g * 512, wrow0 + 4 * g >= x.nsel4 ? &tm_win : &tm_ent, bar_c, c * 64,
-                              cr[4 * g], cr[4 * g + 1], cr[4 * g + 2], cr[4 * g + 3]);
+                for (int c = 2 * c2; c < 2 * c2 + 2; ++c)
+                  tma_gather4(sE + c * 16384 + (gw * 32 + 4 * g8) * 128, gmap,
+                              (c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, c * 64,
+                              cr0, cr1, cr2, cr3);
               }
               __syncwarp();
             }
