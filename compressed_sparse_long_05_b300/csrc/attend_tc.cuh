@@ -28,9 +28,10 @@
 // Warp roles (288 threads): warps 0-3 softmax / epilogue (one TMEM lane
 // quarter each), warps 4-7 gather (32 rows each), warp 8 TMEM owner + MMA
 // issuer.
-//   - bf16 rows are gathered by TMA tile::gather4 (four arbitrary rows x one
-//     128-byte box per instruction, landing already swizzled); the entries end
-//     at a multiple of 4 rows so every 4-row group comes from one tensor.
+//   - bf16 rows are copied with cp.async, 16 bytes per lane straight into the
+//     swizzled tile; each lane's copies of a 64-dim chunk arrive on that
+//     chunk's barrier as they land (measured faster than TMA tile::gather4,
+//     which this tile layout also allows).
 //   - FP8 / BF16-RoPE rows are copied with cp.async (all of a tile at once)
 //     and widened to bf16 in place.
 //   - RoPE: when many query rows share few stored rows (prefill), every stored
@@ -79,7 +80,6 @@ struct AttendTcArgs {
   int items;                     // B * Tq * HG * nch
   int rotate_rows;               // 1 = rotate gathered rows in shared memory
   int rel_rope;                  // 1 = rows rotated by (position - t): q and out stay unrotated
-  int tma_rows;                  // 1 = bf16 rows gathered by TMA (tile::gather4), 4-row groups
   int kv_mixed;                  // 1 = e4m3 + scale + bf16 rope rows
   float scale_log2;              // log2(e) / sqrt(d)
   RopeFreqs rf;
@@ -105,7 +105,6 @@ struct AttRow {
   int b, i, hg, c;
   long long t;
   int nsel;        // compressed rows (selected or visible)
-  int nsel4;       // row index where the window starts (nsel, rounded up to 4 for TMA groups)
   long long w0;    // first window token
   int nrows;       // nsel + window size
   int r0, r1;      // this chunk's rows [r0, r1)
@@ -126,8 +125,7 @@ CSA_DEVINL AttRow att_item(const AttendTcArgs& a, int it) {
   x.nsel = a.idx ? (int)min((long long)a.k, vis) : (int)vis;
   x.w0 = x.t - a.n_win + 1;
   if (x.w0 < 0) x.w0 = 0;
-  x.nsel4 = a.tma_rows ? ((x.nsel + 3) & ~3) : x.nsel;
-  x.nrows = x.nsel4 + (int)(x.t - x.w0 + 1);
+  x.nrows = x.nsel + (int)(x.t - x.w0 + 1);
   x.r0 = min(x.nrows, x.c * a.chunk_rows);
   x.r1 = min(x.nrows, x.r0 + a.chunk_rows);
   return x;
@@ -147,24 +145,17 @@ CSA_DEVINL void tmem_st32(uint32_t taddr, const uint32_t* r) {
 }
 CSA_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// four rows (arbitrary row coordinates) x one 128-byte box of a 2-D tensor map,
-// landing as four consecutive 128-byte rows with the map's swizzle
-CSA_DEVINL void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int r0, int r1,
-                            int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
 CSA_DEVINL void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0)
                : "memory");
 }
 CSA_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrive on `bar` once every cp.async this thread issued so far has landed (the
+// barrier's pending count is raised by one until then).
+CSA_DEVINL void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 template <int N>
 CSA_DEVINL void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
@@ -218,8 +209,7 @@ CSA_DEVINL uint4 e4m3x8_to_bf16(uint2 raw, float scale) {
 }
 
 __global__ void __launch_bounds__(ATT_THREADS, 1)
-attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ent,
-                 const __grid_constant__ CUtensorMap tm_win, const AttendTcArgs a) {
+attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sE = smem + AttSmem::E;
@@ -243,8 +233,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint64_t* grp_a = bar + 21;        // softmax warps: tile max partials (count 4)
   uint64_t* grp_b = bar + 22;        // softmax warps: sum partials (count 4)
   uint64_t* mma_done = bar + 23;
-  uint64_t* c7_full = bar + 24;      // [4] per gather warp: its chunk-7 rows landed (TMA, RoPE after)
-  uint64_t* q_ready = bar + 28;      // absolute-RoPE mode: q rotated at t -> MMA (count 4)
+  uint64_t* q_ready = bar + 24;      // absolute-RoPE mode: q rotated at t -> MMA (count 4)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttSmem::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttSmem::MISC + 4);
 
@@ -263,7 +252,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     mbar_init(grp_a, 4);
     mbar_init(grp_b, 4);
     mbar_init(mma_done, 1);
-    for (int w = 0; w < 4; ++w) mbar_init(c7_full + w, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -291,7 +279,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // this lane's row: tile row gw*32 + lane
         const int rr = r0 + gw * 32 + lane;
         const uint8_t* src = nullptr;        // bf16 row, or e4m3 nope row
-        int trow = -1;                       // row of the entry / window tensor map (TMA mode)
         const __nv_bfloat16* rsrc = nullptr; // mixed: rope row
         float rscale = 0.f;
         long long pos = 0;
@@ -301,7 +288,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (s >= a.N) { csa_flag_error(ERRBIT_BAD_INDEX); s = -1; }
             if (s >= 0) {
               const size_t row = (size_t)x.b * a.N + s;
-              trow = (int)row;
               if (a.kv_mixed) {
                 src = reinterpret_cast<const uint8_t*>(a.ent) + row * (ATT_D - ATT_R);
                 rsrc = a.ent_rope + row * ATT_R;
@@ -311,10 +297,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               }
               pos = (long long)a.m * (s + 1) - 1;
             }
-          } else if (rr >= x.nsel4) {
-            const long long tok = x.w0 + (rr - x.nsel4);
+          } else {
+            const long long tok = x.w0 + (rr - x.nsel);
             const size_t row = (size_t)x.b * a.T_win + (size_t)(tok - a.win_base);
-            trow = (int)row;
             if (a.kv_mixed) {
               src = reinterpret_cast<const uint8_t*>(a.win) + row * (ATT_D - ATT_R);
               rsrc = a.win_rope + row * ATT_R;
@@ -330,37 +315,39 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const uint32_t bits = __ballot_sync(0xffffffffu, src != nullptr);
           if (lane == 0) rmask[(n & 1) * 4 + gw] = bits;
         }
-        if (a.tma_rows) {
-          // TMA: 8 groups of 4 rows per warp and 64-dim chunk.  Groups are pure
-          // (entries end at nsel4, a multiple of 4); invalid rows read row 0 of
-          // their region and are masked above.
-          const int wrow0 = r0 + gw * 32;
-          const int coord = trow >= 0 ? trow : (wrow0 + lane >= x.nsel4 ? x.b * a.T_win : x.b * a.N);
-          // lane g (< 8) issues the copies of row group g (rows 4g..4g+3 of this warp):
-          // eight issuing lanes keep more gathers in flight than one
-          const int g8 = lane & 7;
-          const int cr0 = __shfl_sync(0xffffffffu, coord, 4 * g8);
-          const int cr1 = __shfl_sync(0xffffffffu, coord, 4 * g8 + 1);
-          const int cr2 = __shfl_sync(0xffffffffu, coord, 4 * g8 + 2);
-          const int cr3 = __shfl_sync(0xffffffffu, coord, 4 * g8 + 3);
-          const CUtensorMap* gmap = wrow0 + 4 * g8 >= x.nsel4 ? &tm_win : &tm_ent;
+        if (!a.kv_mixed) {
+          // bf16 rows by cp.async: lane l copies 16-byte granule (l & 7) of rows
+          // (l >> 3) + 4k, k < 8, of this warp's 32, straight into the swizzled tile.
+          // Each lane's copies of chunk c arrive on the chunk's barrier when they land
+          // (the barrier's pending count rises by one per lane until then); rows
+          // without a source are zero-filled and masked above.
+          const uint8_t* rsrc8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            rsrc8[k] = reinterpret_cast<const uint8_t*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src), (lane >> 3) + 4 * k));
+          auto cp_chunk = [&](int c) {
+            const int u = lane & 7;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int tr = gw * 32 + (lane >> 3) + 4 * k;
+              const uint8_t* sp = rsrc8[k];
+              cp_async16(smem_u32(sE + c * 16384 + tr * 128 + ((u ^ (tr & 7)) << 4)),
+                         sp ? sp + c * 128 + u * 16 : reinterpret_cast<const uint8_t*>(a.q), sp != nullptr);
+            }
+            if (!(c == 7 && a.rotate_rows)) {        // chunk 7 is released after its RoPE below
+              cp_async_mbar_arrive(chunk_full + c);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(chunk_full + c);
+            }
+          };
           if (r0 == x.r0) {
             // first tile of the item: every chunk pair is free once the last PV of
             // the previous item is done; fetch each row's 1 KB together
             for (int c2 = 0; c2 < 4 && ok; ++c2)
               if (!mbar_wait(chunk_free + c2, (n & 1) ^ 1, abort_flag)) ok = false;
             if (!ok) break;
-            if (lane == 0)
-              for (int c = 0; c < 8; ++c)
-                mbar_arrive_expect_tx((c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, 32 * 128);
-            __syncwarp();
-            if (lane < 8) {
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                tma_gather4(sE + c * 16384 + (gw * 32 + 4 * g8) * 128, gmap,
-                            (c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, c * 64,
-                            cr0, cr1, cr2, cr3);
-            }
+            for (int c = 0; c < 8; ++c) cp_chunk(c);
             __syncwarp();
             if (!a.rel_rope) {
               // absolute-RoPE mode: rotate this warp's 16 heads of the TMA-loaded
@@ -381,24 +368,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // later tiles: each chunk pair as soon as the PV block that read it is done
             for (int c2 = 0; c2 < 4 && ok; ++c2) {
               if (!mbar_wait(chunk_free + c2, (n & 1) ^ 1, abort_flag)) { ok = false; break; }
-              if (lane == 0)
-                for (int c = 2 * c2; c < 2 * c2 + 2; ++c)
-                  mbar_arrive_expect_tx((c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, 32 * 128);
-              __syncwarp();
-              if (lane < 8) {
-#pragma unroll
-                for (int c = 2 * c2; c < 2 * c2 + 2; ++c)
-                  tma_gather4(sE + c * 16384 + (gw * 32 + 4 * g8) * 128, gmap,
-                              (c == 7 && a.rotate_rows) ? c7_full + gw : chunk_full + c, c * 64,
-                              cr0, cr1, cr2, cr3);
-              }
-              __syncwarp();
+              cp_chunk(2 * c2);
+              cp_chunk(2 * c2 + 1);
             }
             if (!ok) break;
           }
           if (a.rotate_rows) {
             // RoPE of this warp's 32 rows once its chunk 7 (dims 448..511) has landed
-            if (!mbar_wait(c7_full + gw, n & 1, abort_flag)) { ok = false; break; }
+            cp_async_commit();                        // wait for every copy this lane issued
+            cp_async_wait<0>();
+            __syncwarp();
             uint8_t* c7 = sE + 7 * 16384;
 #pragma unroll 2
             for (int k2 = 0; k2 < 8; ++k2) {

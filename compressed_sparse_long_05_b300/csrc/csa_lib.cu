@@ -137,21 +137,6 @@ bool tmap_u8_3d_sw64(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, u
   return r == CUDA_SUCCESS;
 }
 
-// 2-D bf16 map over `rows` rows of 512 elements for tile::gather4: box of one
-// row x 64 elements (128 bytes), 128-byte swizzle.
-bool tmap_bf16_rows(CUtensorMap* m, const void* base, uint64_t rows) {
-  auto enc = tmap_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)csa::ATT_D, rows};
-  cuuint64_t strides[1] = {(cuuint64_t)csa::ATT_D * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // 1-D map over `n` 8-byte elements (one element = the 8 scale bytes of a row).
 bool tmap_u64_1d(CUtensorMap* m, const void* base, uint64_t n, uint32_t box) {
   auto enc = tmap_encoder();
@@ -278,8 +263,7 @@ AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int m, int 
   if (vis > N) vis = N;
   const long long nsel = dense ? vis : (vis < k ? vis : k);
   const long long win = t_last + 1 < n_win ? t_last + 1 : n_win;
-  // bf16 rows are gathered by TMA in groups of 4: the window starts at nsel rounded up to 4
-  const long long rows_max = (kv_mixed ? nsel : ((nsel + 3) & ~3LL)) + win;
+  const long long rows_max = nsel + win;
   const int tiles = (int)((rows_max + csa::ATT_TILE - 1) / csa::ATT_TILE);
   const long long units = (long long)B * Tq * p.HG;
   const int sms = sm_count();
@@ -676,7 +660,6 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
   a.HG = p.HG; a.nch = p.nch; a.chunk_rows = p.chunk_rows; a.items = p.items;
   a.rotate_rows = p.rotate_rows; a.kv_mixed = mixed;
   a.rel_rope = p.rel_rope;
-  a.tma_rows = mixed ? 0 : 1;
   if ((long long)B * N >= 0x7fffffffLL || (long long)B * T_win >= 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
   a.rf = rf;
@@ -708,25 +691,18 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
     a.part_o = reinterpret_cast<float*>(wsb + p.off_part_o);
     a.part_ml = reinterpret_cast<float*>(wsb + p.off_part_ml);
   }
-  CUtensorMap tmq, tment, tmwin;
+  CUtensorMap tmq;
   memset(&tmq, 0, sizeof(tmq));
-  memset(&tment, 0, sizeof(tment));
-  memset(&tmwin, 0, sizeof(tmwin));
   if (!tmap_bf16_3d(&tmq, q, csa::ATT_D, (uint64_t)B * Tq * n_h, 1, (uint64_t)csa::ATT_D * 2,
                     (uint64_t)B * Tq * n_h * csa::ATT_D * 2, 64, csa::ATT_HG))
     return CSA_ERR_UNSUPPORTED;
-  if (a.tma_rows &&
-      ((N > 0 && !tmap_bf16_rows(&tment, a.ent, (uint64_t)B * N)) ||
-       !tmap_bf16_rows(&tmwin, a.win, (uint64_t)B * T_win)))
-    return CSA_ERR_UNSUPPORTED;
-  if (a.tma_rows && N == 0) tment = tmwin;   // no entry groups exist; any valid map
   const int smem = csa::AttSmem::BYTES;
   cudaError_t e = cudaFuncSetAttribute(csa::attend_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc attr");
   const int sms = sm_count();
   const int grid = p.items < sms ? p.items : sms;
-  e = launch_ex(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st, 1, tmq, tment, tmwin, a);
+  e = launch_ex(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st, 1, tmq, a);
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc launch");
   if (p.nch > 1) {
     csa::CombineArgs ca;
