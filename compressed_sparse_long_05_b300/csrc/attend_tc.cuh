@@ -44,10 +44,17 @@
 //
 // A single-chunk item finishes in the kernel: divide by the softmax
 // denominator plus exp(sink), rotate the RoPE dims back if needed, store bf16.
-// A multi-chunk item (decode: few query rows, many rows each) stores its
-// unnormalised O (staged in shared memory, one bulk copy when the CTA has one
-// item), running max and denominator for attend_combine_kernel.
+// A multi-chunk item (decode: few query rows, many rows each) keeps its
+// unnormalised O and its running max and denominator, and the chunks merge by
+// log-sum-exp, in one of two ways:
+//   - cluster merge: the chunks of a (query row, head group) run as one thread-
+//     block cluster, each staging its O (fp32 [64 heads][512 dims]) and (max,
+//     sum) in its own shared memory; every CTA then merges its share of the
+//     outputs from all chunks' shared memory over DSMEM and stores bf16;
+//   - otherwise O goes to global memory (one bulk copy of the staged tile when
+//     the CTA has one item) and attend_combine_kernel merges.
 #pragma once
+#include <cooperative_groups.h>
 #include <cuda_fp8.h>
 #include "tc.cuh"
 
@@ -81,6 +88,7 @@ struct AttendTcArgs {
   int rotate_rows;               // 1 = rotate gathered rows in shared memory
   int rel_rope;                  // 1 = rows rotated by (position - t): q and out stay unrotated
   int kv_mixed;                  // 1 = e4m3 + scale + bf16 rope rows
+  int cl_reduce;                 // 1 = the nch chunks of a head group are one cluster and merge over DSMEM
   float scale_log2;              // log2(e) / sqrt(d)
   RopeFreqs rf;
 };
@@ -93,7 +101,10 @@ struct AttSmem {
   static constexpr int SUMP = MAXP + 2 * 4 * 64 * 4;       // [2][4][64] f32
   static constexpr int MROW = SUMP + 2 * 4 * 64 * 4;       // [4 warps][64] f32 running max
   static constexpr int FAC = MROW + 4 * 64 * 4;            // [4][64] f32 rescale factors
-  static constexpr int RMASK = FAC + 4 * 64 * 4;          // [2 tiles][4 warps] u32 row-valid bits
+  static constexpr int ML = FAC + 4 * 64 * 4;              // [64][2] f32 this chunk's (max, sum) (cluster merge)
+  static constexpr int WTS = ML + 64 * 2 * 4;              // [16 chunks][64] f32 merge weights (cluster merge)
+  static constexpr int INVD = WTS + 16 * 64 * 4;           // [64] f32 1 / denominator (cluster merge)
+  static constexpr int RMASK = INVD + 64 * 4;             // [2 tiles][4 warps] u32 row-valid bits
   static constexpr int BAR = RMASK + 64;
   static constexpr int NBAR = 32;
   static constexpr int MISC = BAR + NBAR * 8;
@@ -206,6 +217,71 @@ CSA_DEVINL uint4 e4m3x8_to_bf16(uint2 raw, float scale) {
     f[2 * e + 1] = v.y * scale;
   }
   return f_to_bf16x8(f);
+}
+
+// Cluster merge of a head group's chunks (one item per CTA; cluster rank = chunk).
+// Every CTA has staged its unnormalised O [64 heads][512 dims] f32 at sE and its
+// per-head (max, sum) at AttSmem::ML.  CTA c computes outputs [c*8192/nch,
+// (c+1)*8192/nch) of the 8192 float4 columns: out = sum_c 2^(m_c - M) O_c /
+// (sum_c 2^(m_c - M) l_c + 2^(z' log2 e - M)), reading every chunk's shared
+// memory over DSMEM (relative-RoPE mode: the output needs no rotation).
+CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint8_t* sE) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int nch = a.nch;
+  const int crank = (int)cl.block_rank();
+  const AttRow x = att_item(a, blockIdx.x);
+  float* ml = reinterpret_cast<float*>(smem + AttSmem::ML);
+  float* wts = reinterpret_cast<float*>(smem + AttSmem::WTS);
+  float* invd = reinterpret_cast<float*>(smem + AttSmem::INVD);
+  cl.sync();                                          // every chunk's O and (max, sum) staged
+  if (threadIdx.x < ATT_HG) {
+    const int h = threadIdx.x;
+    float M = -INFINITY;
+    for (int c = 0; c < nch; ++c) M = fmaxf(M, cl.map_shared_rank(ml, c)[2 * h]);
+    const float zs = __ldg(a.sink + x.hg * ATT_HG + h) * 1.4426950408889634f;
+    M = fmaxf(M, zs);
+    float den = exp2f(zs - M);
+    for (int c = 0; c < nch; ++c) {
+      const float* p = cl.map_shared_rank(ml, c);
+      const float w = exp2f(p[2 * h] - M);           // 0 for a chunk with no valid row (max -inf)
+      wts[c * ATT_HG + h] = w;
+      den += w * p[2 * h + 1];
+    }
+    invd[h] = 1.f / den;
+  }
+  __syncthreads();
+  const float4* srcs[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    srcs[c] = c < nch ? reinterpret_cast<const float4*>(cl.map_shared_rank(sE, c)) : nullptr;
+  const size_t orow = ((size_t)x.b * a.Tq + x.i) * a.n_h + (size_t)x.hg * ATT_HG;
+  const int q0 = crank * (ATT_HG * ATT_D / 4) / nch, q1 = (crank + 1) * (ATT_HG * ATT_D / 4) / nch;
+  for (int q = q0 + (int)threadIdx.x; q < q1; q += (int)blockDim.x) {
+    const int h = q >> 7;                             // 128 float4 columns per head
+    float4 v[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      if (c < nch) v[c] = srcs[c][q];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      if (c < nch) {
+        const float w = wts[c * ATT_HG + h];
+        acc.x = fmaf(w, v[c].x, acc.x);
+        acc.y = fmaf(w, v[c].y, acc.y);
+        acc.z = fmaf(w, v[c].z, acc.z);
+        acc.w = fmaf(w, v[c].w, acc.w);
+      }
+    const float s = invd[h];
+    __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * s, acc.y * s);
+    __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * s, acc.w * s);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+    *reinterpret_cast<uint2*>(a.out + (orow + h) * ATT_D + (q & 127) * 4) = pk;
+  }
+  cl.sync();                                          // no CTA leaves while peers read its memory
 }
 
 __global__ void __launch_bounds__(ATT_THREADS, 1)
@@ -668,7 +744,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
           my_f[h] = exp2f(m_run[e] - M) / den;
         } else {
           my_f[h] = 1.f;
-          float* ml = a.part_ml + ((size_t)it * ATT_HG + h) * 2;
+          float* ml = a.cl_reduce ? reinterpret_cast<float*>(smem + AttSmem::ML) + h * 2
+                                  : a.part_ml + ((size_t)it * ATT_HG + h) * 2;
           if (q4 == 0) { ml[0] = m_run[e]; ml[1] = l_run[e]; }
         }
       }
@@ -715,7 +792,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
           }
         }
       }
-      if (stage_out) {
+      if (stage_out && !a.cl_reduce) {
         // one bulk copy of the staged 128 KB partial to global memory
         fence_proxy_async();
         named_bar_sync(2, 128);
@@ -737,6 +814,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (a.cl_reduce) attend_cluster_merge(a, smem, sE);
   if (warp == 8) tmem_dealloc(tmem, 512);
 }
 

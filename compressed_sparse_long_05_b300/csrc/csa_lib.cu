@@ -247,11 +247,54 @@ csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, floa
 
 // Work split and scratch layout of the tensor-core attention path.
 struct AttPlan {
-  int HG, nch, chunk_rows, items, rotate_rows, rel_rope;
+  int HG, nch, chunk_rows, items, rotate_rows, rel_rope, cl_reduce;
   size_t off_part_o, off_part_ml, off_rot_ent, off_rot_win, bytes;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Co-resident clusters of `cl` attention CTAs on the current device (0 when the
+// query fails), cached per device and size.
+int attend_max_clusters(int cl) {
+  static std::mutex mu;
+  static int cache_dev = -1;
+  static int cache[17];
+  int dev = 0;
+  if (cl < 2 || cl > 16 || cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache_dev != dev) {
+    for (int i = 0; i <= 16; ++i) cache[i] = -1;
+    cache_dev = dev;
+  }
+  if (cache[cl] < 0) {
+    int n = 0;
+    bool ok = cudaFuncSetAttribute(csa::attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   csa::AttSmem::BYTES) == cudaSuccess;
+    if (ok && cl > 8)
+      ok = cudaFuncSetAttribute(csa::attend_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+           cudaSuccess;
+    if (ok) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)cl);
+      cfg.blockDim = dim3(csa::ATT_THREADS);
+      cfg.dynamicSmemBytes = csa::AttSmem::BYTES;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = cl;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      ok = cudaOccupancyMaxActiveClusters(&n, csa::attend_tc_kernel, &cfg) == cudaSuccess;
+    }
+    if (!ok) {
+      cudaGetLastError();   // clear the sticky-free error of a failed query
+      n = 0;
+    }
+    cache[cl] = n;
+  }
+  return cache[cl];
+}
 
 AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int m, int n_win, int q_pos0,
                     int dense, int kv_mixed) {
@@ -281,8 +324,11 @@ AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int m, int 
   p.rotate_rows = (kv_mixed || gathered <= 2LL * B * ((long long)N + T_win)) ? 1 : 0;
   // rows rotated in shared memory are rotated by (position - t): q and the output stay unrotated
   p.rel_rope = p.rotate_rows;
+  // the chunks of each head group merge inside a cluster when they all run at once
+  p.cl_reduce = (p.nch > 1 && p.nch <= 16 && p.items <= sms && p.rel_rope &&
+                 attend_max_clusters(p.nch) >= p.items / p.nch) ? 1 : 0;
   size_t off = 0;
-  if (p.nch > 1) {
+  if (p.nch > 1 && !p.cl_reduce) {
     p.off_part_o = off;
     off = align256(off + (size_t)p.items * csa::ATT_HG * csa::ATT_D * sizeof(float));
     p.off_part_ml = off;
@@ -659,6 +705,7 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
   a.n_h = n_h; a.m = m; a.n_win = n_win; a.q_pos0 = q_pos0;
   a.HG = p.HG; a.nch = p.nch; a.chunk_rows = p.chunk_rows; a.items = p.items;
   a.rotate_rows = p.rotate_rows; a.kv_mixed = mixed;
+  a.cl_reduce = p.cl_reduce;
   a.rel_rope = p.rel_rope;
   if ((long long)B * N >= 0x7fffffffLL || (long long)B * T_win >= 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
@@ -687,7 +734,7 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
     }
     a.win = ra.dst;
   }
-  if (p.nch > 1) {
+  if (p.nch > 1 && !p.cl_reduce) {
     a.part_o = reinterpret_cast<float*>(wsb + p.off_part_o);
     a.part_ml = reinterpret_cast<float*>(wsb + p.off_part_ml);
   }
@@ -702,9 +749,14 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc attr");
   const int sms = sm_count();
   const int grid = p.items < sms ? p.items : sms;
-  e = launch_ex(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st, 1, tmq, a);
+  if (p.cl_reduce && p.nch > 8) {
+    e = cudaFuncSetAttribute(csa::attend_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_attend cluster attr");
+  }
+  e = launch_ex(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st,
+                p.cl_reduce ? p.nch : 1, tmq, a);
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc launch");
-  if (p.nch > 1) {
+  if (p.nch > 1 && !p.cl_reduce) {
     csa::CombineArgs ca;
     ca.part_o = a.part_o; ca.part_ml = a.part_ml; ca.sink = sink; ca.out = a.out;
     ca.Tq = Tq; ca.n_h = n_h; ca.HG = p.HG; ca.nch = p.nch; ca.q_pos0 = q_pos0; ca.rf = rf;
