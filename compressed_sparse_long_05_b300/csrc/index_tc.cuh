@@ -13,8 +13,10 @@
 // ReLU * w into QT scores per entry: the head reduction never leaves
 // registers, and each warp stores 32 consecutive scores per query.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
-// issuer, warps 2-5 epilogue (one TMEM lane quarter each).
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
+// issuer, warps 2-9 epilogue in two groups of four (one warp per TMEM lane
+// quarter) that take alternate tiles, so the fold of one tile overlaps the
+// next tile's.
 //
 // Work items are (batch row b, query group g, chunk of entry tiles), dealt
 // round-robin to persistent CTAs.  Tiles past the last entry any query of the
@@ -24,7 +26,7 @@
 
 namespace csa {
 
-constexpr int IDX_THREADS = 192;
+constexpr int IDX_THREADS = 320;
 constexpr int IDX_TILE = 128;   // entries per tile (MMA M)
 
 struct IndexTcArgs {
@@ -78,8 +80,8 @@ struct IndexSmem {
   __host__ __device__ IndexSmem(int stages, int nqh, bool hist) {
     S = stages;
     OFF_B = S * A_BYTES;
-    OFF_W = OFF_B + ((nqh * C * 2 + 1023) & ~1023);      // float w_s[4 warps][2][256]
-    OFF_HIST = OFF_W + 4 * 2 * 256 * 4;
+    OFF_W = OFF_B + ((nqh * C * 2 + 1023) & ~1023);      // float w_s[8 warps][256]
+    OFF_HIST = OFF_W + 8 * 256 * 4;
     OFF_BAR = OFF_HIST + (hist ? HIST_BYTES : 0);
     BYTES = OFF_BAR + 256 + 1024;                        // + alignment slack
   }
@@ -169,7 +171,8 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   uint64_t* b_full = acc_empty + 4;
   uint64_t* b_free = b_full + 1;
   uint64_t* mma_done = b_free + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* epi_sync = mma_done + 1;             // the 8 epilogue warps at an item's end (count 8)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_sync + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -181,12 +184,17 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
     mbar_init(b_full, 1);
     mbar_init(b_free, 1);
     mbar_init(mma_done, 1);
+    mbar_init(epi_sync, 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, a.tmem_cols);
     tmem_relinquish();
+  }
+  if (a.hist) {
+    uint32_t* h = reinterpret_cast<uint32_t*>(smem + L.OFF_HIST);
+    for (int b = threadIdx.x; b < 4 * IDX_HBINS; b += blockDim.x) h[b] = 0;
   }
   if (warp == 0 && lane == 0) { prefetch_tmap(&tm_K); prefetch_tmap(&tm_q); }
   tc_fence_before();
@@ -270,29 +278,30 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
       mbar_drain(mma_done, 0);
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..9: two groups, alternate tiles) ----------------
+    const int ew = warp - 2;                       // 0..7
+    const int grp = ew >> 2;                       // tiles with iacc % 2 == grp
     const int q4 = warp & 3;                       // TMEM lane quarter of this warp
-    uint32_t* wh = reinterpret_cast<uint32_t*>(smem + L.OFF_HIST) + q4 * IDX_HBINS;
-    if (a.hist) {
-      for (int b = lane; b < IDX_HBINS; b += 32) wh[b] = 0;
-      __syncwarp();
-    }
-    uint32_t iacc = 0, nitem = 0;
+    uint32_t* wh = reinterpret_cast<uint32_t*>(smem + L.OFF_HIST) + q4 * IDX_HBINS;   // shared by both groups
+    uint32_t iacc = 0, nsync = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
       const IdxItem x = idx_item(a, it);
       // this warp's own copy of the group's head weights (no cross-warp barrier,
       // so a warp that stops on a timed-out wait cannot strand the others)
-      float* ws = w_s + ((q4 * 2) + (nitem & 1)) * 256;
+      float* ws = w_s + ew * 256;
+      __syncwarp();                                // the previous item's reads are done
       for (int e = lane; e < x.nq * H; e += 32)
         ws[e] = __ldg(a.w + ((size_t)x.b * a.Tq + x.t0) * H + e);
       __syncwarp();
-      ++nitem;
       for (int j = x.j0; j < x.j1; ++j) {
         const int s = j * IDX_TILE + q4 * 32 + lane;
         float* srow = a.scores + ((size_t)x.b * a.Tq + x.t0) * a.N + s;
         if (j < x.jv) {
+          const uint32_t mine = (iacc & 1) == (uint32_t)grp;
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
+          ++iacc;
+          if (!mine) continue;
           if (!mbar_wait(acc_full + buf, aph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
@@ -305,13 +314,26 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + buf);
-          ++iacc;
-        } else {
+        } else if ((j & 1) == grp) {
           for (int qi = 0; qi < x.nq; ++qi)
             if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
         }
       }
-      if (a.hist && ok) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
+      if (a.hist) {
+        // both groups have added this item's scores: one group flushes (and clears)
+        // the shared per-quarter histograms; the next item's adds wait for that.
+        // Bounded waits: a warp that gave up still arrives, and the flag ends the rest.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_sync);
+        const bool s1 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
+        ++nsync;
+        if (ok && s1 && grp == 0) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_sync);
+        const bool s2 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
+        ++nsync;
+        if (!s1 || !s2) ok = false;
+      }
     }
   }
 
