@@ -271,7 +271,7 @@ def alloc_buffers(K, cfg, x, dev):
         buf.idx = torch.empty((B, Tq, cfg["k"]), dtype=torch.int32, device=dev)
         dt = 3 if "qI_fp4" in x else 1
         nb = K.lib().csa_index_topk_workspace_size(B, Tq, N, dt)
-        buf.ws_topk = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        buf.ws_topk = torch.zeros(max(nb, 256), dtype=torch.uint8, device=dev)   # histograms start zero
     buf.out = torch.empty_like(x["q"])
     ent = buf.entries if kind.endswith("prefill") else P._entries_arg(x)
     nbytes = K.attend_workspace_size(x["q"], ent, P._win_arg(x), cfg.get("k", 0), cfg["m"],

@@ -146,7 +146,11 @@ def csa_topk(scores, k, m, q_pos0, idx=None):
 
 def csa_index_topk(qI, w, K, k, m, q_pos0, qI_sf=None, K_sf=None, scores=None, idx=None, ws=None):
     """Indexer scores and the top-k index sets of one call (same results as
-    csa_index then csa_topk); returns (scores, idx, ws)."""
+    csa_index then csa_topk); returns (scores, idx, ws).
+
+    ``ws`` (returned for reuse) must be zero-filled before its first call: a new
+    one is allocated zeroed, and every successful call leaves it zero.  After a
+    failed call pass ``ws=None`` (or zero it) again."""
     fp4 = qI.dtype == torch.uint8
     B, Tq, H = qI.shape[:3]
     c = qI.shape[3] * (2 if fp4 else 1)
@@ -157,7 +161,7 @@ def csa_index_topk(qI, w, K, k, m, q_pos0, qI_sf=None, K_sf=None, scores=None, i
     if idx is None:
         idx = torch.empty((B, Tq, k), dtype=torch.int32, device=qI.device)
     nbytes = lib().csa_index_topk_workspace_size(B, Tq, N, dt)
-    ws = _workspace(ws, nbytes, qI.device)
+    ws = _workspace(ws, nbytes, qI.device, zero=True)   # histograms start zero; calls leave them zero
     _check("csa_index_topk", lib().csa_index_topk(
         _p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(scores), _p(idx), B, Tq, N, H, c, m, q_pos0,
         k, dt, _p(ws) if nbytes else None, nbytes, _stream()))
@@ -173,11 +177,11 @@ def attend_workspace_size(q, entries, win, k, m, n_win, q_pos0, r, is_hca):
                                            _dt(q), kv_dt, 1 if is_hca else 0)
 
 
-def _workspace(ws, nbytes, device):
+def _workspace(ws, nbytes, device, zero=False):
     if nbytes == 0:
         return ws
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        ws = (torch.zeros if zero else torch.empty)(nbytes, dtype=torch.uint8, device=device)
     return ws
 
 

@@ -393,7 +393,7 @@ csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t s
 // run, else 512.  `hist` (optional): per-row histograms of the first
 // IDX_HBITS key bits of the visible scores, built by the index kernel.
 csa_status_t launch_topk2(const float* scores, int32_t* idx, int rows, int Tq, int N, int k, int m,
-                          int q_pos0, const uint32_t* hist, cudaStream_t st) {
+                          int q_pos0, uint32_t* hist, cudaStream_t st) {
   int CL = 1;
   if (N > 32768) {
     CL = 8;
@@ -570,9 +570,9 @@ csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, c
   if (!idx || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
   const size_t need = csa_index_topk_workspace_size(B, Tq, N, dtype);
   if (!ws || ws_bytes < need || !aligned(ws, 16)) return CSA_ERR_WORKSPACE;
+  // the histograms start zero (caller's first use) and the selector clears each
+  // row's after reading it, so no clearing pass runs here
   uint32_t* hist = reinterpret_cast<uint32_t*>(ws);
-  cudaError_t e = cudaMemsetAsync(hist, 0, need, S(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "csa_index_topk histogram clear");
   csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, H, c, m, q_pos0, dtype, hist, stream);
   if (st != CSA_OK) return st;
   return launch_topk2(scores, idx, B * Tq, Tq, N, k, m, q_pos0, hist, S(stream));

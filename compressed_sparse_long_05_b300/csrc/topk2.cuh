@@ -34,7 +34,8 @@ struct Topk2Args {
   int Tq, N, k, m, q_pos0;
   int slice;      // keys per CTA (multiple of 4)
   int cand_cap;   // candidate capacity per CTA
-  const uint32_t* hist;   // optional [rows][2^BITS1] first-digit histograms of the visible scores
+  uint32_t* hist;         // optional [rows][2^BITS1] first-digit histograms of the visible scores;
+                          // each row's is cleared once read (left zero for the next call)
 };
 
 // dynamic shared memory: keys[slice] | cand[cand_cap] | hist1[2^BITS1] | merged1[2^BITS1]
@@ -103,6 +104,8 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
 
   if (vis <= a.k) {                                   // every visible entry is selected
     for (int j = rank * NT + tid; j < a.k; j += CL * NT) orow[j] = j < vis ? j : -1;
+    if (hist_in)                                      // leave the histogram zero for the next call
+      for (int j = rank * NT + tid; j < BINS1; j += CL * NT) a.hist[(size_t)row * BINS1 + j] = 0u;
     return;
   }
 
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
 
   if (hist_in) {
     const uint32_t* gh = a.hist + (size_t)row * BINS1;
-    for (int j = tid; j < BINS1; j += NT) hist1[j] = __ldg(gh + j);
+    for (int j = tid; j < BINS1; j += NT) hist1[j] = gh[j];
   } else {
     for (int j = tid; j < BINS1; j += NT) hist1[j] = 0;
     if (CL > 1 && rank == 0)
@@ -134,6 +137,12 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   }
   if constexpr (CL > 1) cluster.sync();
   else __syncthreads();
+  if (hist_in) {
+    // every rank holds its copy: clear this rank's share of the row's histogram
+    // so that the workspace is zero again for the next call
+    uint32_t* gh = a.hist + (size_t)row * BINS1;
+    for (int j = rank * (BINS1 / CL) + tid; j < (rank + 1) * (BINS1 / CL); j += NT) gh[j] = 0u;
+  }
 
   // ---- 1. load the slice (every copy in flight at once), then keys + first-digit histogram ----
   {

@@ -119,8 +119,11 @@ csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, i
  * instead of building that histogram itself (§2.3.1 "Lightning Indexer" and
  * "top-k selector").  Other shapes run the two stages unchanged.
  *   ws / ws_bytes: scratch of csa_index_topk_workspace_size(B, Tq, N, dtype)
- *   bytes (16-byte aligned; may be NULL when that size is 0).  The call clears
- *   it on the stream before use; nothing in it must be initialised.
+ *   bytes (16-byte aligned; may be NULL when that size is 0).  It holds the
+ *   per-row histograms and must be ZERO-FILLED before its first use; every call
+ *   that returns CSA_OK and leaves the device error word clear leaves it zero
+ *   again (the selector clears each histogram after reading it), so a decode
+ *   loop zero-fills it once.  After a failed call, zero-fill it again.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, const void* K,
                             const void* K_sf, float* scores, int32_t* idx, int B, int Tq, int N,

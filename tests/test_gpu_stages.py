@@ -396,3 +396,29 @@ def test_index_topk_fused_matches_separate_calls(K, fmt, B, N, k):
     assert torch.equal(s, s_ref)
     assert torch.equal(i, i_ref)
     _check_topk(s, i, k, m, q_pos0)
+
+
+@pytest.mark.parametrize("fmt,B,N", [("bf16", 3, 32768), ("bf16", 2, 700), ("fp4", 2, 40001)])
+def test_index_topk_workspace_left_zero(K, fmt, B, N):
+    # the histograms in the workspace start zero and every call leaves them zero,
+    # so repeated calls on one workspace agree with the first
+    m, H, c, k = 4, 64, 128, 1024
+    q_pos0 = 4 * N - 1
+    w = torch.rand((B, 1, H), generator=_gen(57), device=DEV) / H
+    if fmt == "bf16":
+        qI = _randn((B, 1, H, c), torch.bfloat16, 58, scale=c ** -0.5)
+        Kt = _randn((B, N, c), torch.bfloat16, 59, scale=c ** -0.5)
+        q_sf = k_sf = None
+    else:
+        qI, q_sf = _fp4((B, 1, H, c), 58, c ** -0.5)
+        Kt, k_sf = _fp4((B, N, c), 59, c ** -0.5)
+    s0, i0, ws = K.csa_index_topk(qI, w, Kt, k, m, q_pos0, qI_sf=q_sf, K_sf=k_sf)
+    torch.cuda.synchronize()
+    K.device_error()
+    assert ws is not None and int(ws.count_nonzero()) == 0
+    for _ in range(2):
+        s, i, ws = K.csa_index_topk(qI, w, Kt, k, m, q_pos0, qI_sf=q_sf, K_sf=k_sf, ws=ws)
+        torch.cuda.synchronize()
+        K.device_error()
+        assert torch.equal(s, s0) and torch.equal(i, i0)
+        assert int(ws.count_nonzero()) == 0
