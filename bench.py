@@ -576,11 +576,13 @@ def reference_arm(args, cfg, rank, world):
     x = synth.make_inputs(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
     xn = host_copy(x)
     del x
-    # the oracle is slow by design: run a bounded number of sample steps
-    # (one short warm-up, then up to 3 timed samples of ~15 s) whatever K is
+    # the oracle is slow by design: W short warm-up samples (at least 3, ~0.2 s
+    # each), then up to 3 timed samples of --cpu-budget seconds whatever K is
     run_steps = max(1, min(args.steps, 3))
     per_step_budget = args.cpu_budget
-    oracle_sample(cfg, xn, min(1.0, per_step_budget))
+    warm = max(3, args.warmup)
+    for _ in range(warm):
+        oracle_sample(cfg, xn, min(0.2, per_step_budget))
     vals = []
     desc, threads = "", 1
     for s in range(run_steps):
@@ -589,7 +591,7 @@ def reference_arm(args, cfg, rank, world):
     value = float(np.mean(vals))
     tokens = cfg["B"] * cfg["Tq"]
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
-            "n_gpus": world, "steps": run_steps, "steps_requested": args.steps, "warmup": 1,
+            "n_gpus": world, "steps": run_steps, "steps_requested": args.steps, "warmup": warm,
             "ms_per_step": round(tokens / value * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg["name"], "kind": cfg["kind"]},
