@@ -1,6 +1,6 @@
 """Workload shapes for the CSA / HCA forward path.
 
-Each workload is a plain dict of sizes.  The five named workloads follow the
+Each workload is a plain dict of sizes.  The five main workloads follow the
 shapes the DeepSeek-V4 report gives for V4-Pro (Chinese translation,
 blog.uika.cn, §4.2.1 model settings table: m=4, n_h^I=64, c^I=128, top-k 1024,
 m'=128, n_h=128, c=512, n_win=128; §2.3.3: RoPE on the last 64 dims) and a tiny
@@ -40,6 +40,16 @@ WORKLOADS = {
     "csa_decode_1m_mixed": dict(
         kind="csa_decode", dtype="mixed", B=8, L=1048576, m=4, d=512, r=64,
         n_h=128, H_I=64, c_I=128, k=1024, n_win=128, w_scale=1.0 / 64,
+        qk_scale=128 ** -0.5),
+    # V4-Flash attention shape (same report, §4.2.1: n_h=64, top-k 512; m, the
+    # indexer, c and the window as Pro), decode and prefill at the Pro sizes
+    "csa_decode_flash_128k": dict(
+        kind="csa_decode", dtype="bf16", B=4, L=131072, m=4, d=512, r=64,
+        n_h=64, H_I=64, c_I=128, k=512, n_win=128, w_scale=1.0 / 64,
+        qk_scale=128 ** -0.5),
+    "csa_prefill_flash_32k": dict(
+        kind="csa_prefill", dtype="bf16", B=1, T=32768, m=4, d=512, r=64,
+        n_h=64, H_I=64, c_I=128, k=512, n_win=128, w_scale=1.0 / 64,
         qk_scale=128 ** -0.5),
 }
 

@@ -136,3 +136,12 @@ def test_csa_decode_1m_mixed_full(K):
     # all 8 sequences run; two are checked row by row (each oracle row decodes
     # and scores 262,144 FP4 keys in float64)
     _check_workload(K, "csa_decode_1m_mixed", batch_rows=[0, 7])
+
+
+def test_csa_decode_flash_128k_full(K):
+    # V4-Flash attention shape: one 64-head group, top-k 512
+    _check_workload(K, "csa_decode_flash_128k")
+
+
+def test_csa_prefill_flash_32k_full(K):
+    _check_workload(K, "csa_prefill_flash_32k")

@@ -31,6 +31,20 @@ def test_pro_shapes_match_printed_table():
     assert synth.get("csa_decode_1m_mixed")["L"] == g["context_1m"]
 
 
+def test_flash_shapes_match_printed_table():
+    g = json.load(open(GOLDEN))
+    fl = g["flash"]
+    for name in ("csa_decode_flash_128k", "csa_prefill_flash_32k"):
+        c = synth.get(name)
+        assert (c["m"], c["H_I"], c["c_I"], c["k"], c["n_h"], c["d"], c["n_win"], c["r"]) == (
+            fl["m"], fl["n_h_I"], fl["c_I"], fl["top_k"], fl["n_h"], fl["c"], fl["n_win"],
+            g["rope_dims"])
+    # the Flash decode differs from the Pro decode only in heads and top-k
+    pro, fla = synth.get("csa_decode_128k"), synth.get("csa_decode_flash_128k")
+    diff = {k for k in pro if pro[k] != fla.get(k)}
+    assert diff == {"n_h", "k", "name"}
+
+
 def test_mixed_storage_halves_the_entry_bytes():
     g = json.load(open(GOLDEN))
     c = synth.scaled("csa_decode_1m_mixed", L=1024, B=1)
