@@ -124,3 +124,76 @@ class GraphForward:
             self.graph.replay()
         self.stream.synchronize()
         return self.out_host
+
+
+class PipelinedForward:
+    """A stream of independent layer forwards (e.g. prefill requests) with the
+    host transfers overlapped with compute.
+
+    Two device copies of every input in ``host_inputs`` and of the output
+    alternate between steps: step s copies its inputs host -> device on one
+    stream, runs every stage of :func:`forward` on a second once they are in,
+    and copies its output device -> host on a third, so that step s's compute
+    overlaps step s+1's upload and step s-1's download.  Each step still
+    moves its own inputs and output across PCIe.
+
+    ``submit(host)`` queues one step whose inputs are the pinned host tensors
+    ``host`` (same names, shapes and dtypes as ``x``); it returns the pinned
+    host output buffer that step fills, valid after ``wait(step)``.  Outputs
+    alternate between two host buffers, so read a step's output before
+    submitting step + 2, and leave a step's host inputs unchanged until
+    ``wait(step)`` returns.
+    """
+
+    def __init__(self, cfg: dict, x: dict, host_inputs):
+        import torch
+        self.cfg = cfg
+        self.names = list(host_inputs)
+        self.sets = []
+        for _ in range(2):
+            xs = dict(x)
+            for n in self.names:
+                xs[n] = torch.empty_like(x[n])
+            self.sets.append((xs, Buffers()))
+        self.s_in = torch.cuda.Stream()
+        self.s_run = torch.cuda.Stream()
+        self.s_out = torch.cuda.Stream()
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of the set landed
+        self.ev_run = [torch.cuda.Event() for _ in range(2)]     # compute of the set done
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]     # output of the set read back
+        self.out_host = [None, None]
+        self.step = 0
+        for xs, buf in self.sets:                                 # size every buffer once
+            with torch.cuda.stream(self.s_run):
+                forward(cfg, xs, buf)
+        torch.cuda.synchronize()
+        self.out_host = [torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+                         for _, buf in self.sets]
+
+    def submit(self, host: dict):
+        import torch
+        i = self.step % 2
+        xs, buf = self.sets[i]
+        if self.step >= 2:
+            # the set's previous compute must be done before its inputs are overwritten
+            self.s_in.wait_event(self.ev_run[i])
+        with torch.cuda.stream(self.s_in):
+            for n in self.names:
+                xs[n].copy_(host[n], non_blocking=True)
+            self.ev_in[i].record(self.s_in)
+        self.s_run.wait_event(self.ev_in[i])
+        if self.step >= 2:
+            self.s_run.wait_event(self.ev_out[i])                 # its output was read back
+        with torch.cuda.stream(self.s_run):
+            forward(self.cfg, xs, buf)
+            self.ev_run[i].record(self.s_run)
+        self.s_out.wait_event(self.ev_run[i])
+        with torch.cuda.stream(self.s_out):
+            self.out_host[i].copy_(buf.out, non_blocking=True)
+            self.ev_out[i].record(self.s_out)
+        self.step += 1
+        return self.out_host[i]
+
+    def wait(self, step: int):
+        """Blocks until step ``step``'s output is in its host buffer."""
+        self.ev_out[step % 2].synchronize()
