@@ -81,6 +81,36 @@ def forward(cfg: dict, x: dict, buf: Buffers | None = None):
     return buf.out
 
 
+def compress_entry(i: int, m: int, Ca, Za, Cb=None, Zb=None, Ba=None, Bb=None):
+    """Compressed entry i alone, for each batch row: the entry a decode step adds
+    to the cache when block i closes (DeepSeek-V4 report, Chinese translation,
+    blog.uika.cn, §3.6.1: raw tokens wait in a buffer until their block is full).
+
+    Ca, Za (and Cb, Zb for CSA) are [B, T, d] raw-token buffers holding at least
+    tokens [m*(i-1), m*(i+1)) (CSA) or [m*i, m*(i+1)) (HCA).  Entry i of the
+    overlapped compression depends only on the a-rows of block i and the b-rows
+    of block i-1, so ``csa_compress`` over the two-block window [m*(i-1),
+    m*(i+1)) yields it as the window's entry 1 (entry 0 of the window is not
+    entry i-1 and is discarded); i = 0 and HCA take the one block.  Returns a
+    [B, d] view of the kernel's output.
+    """
+    import torch
+    B, T, d = Ca.shape
+    overlap = Cb is not None
+    lo = m * (i - 1) if (overlap and i > 0) else m * i
+    hi = m * (i + 1)
+    if i < 0 or hi > T:
+        raise ValueError(f"entry {i} needs tokens [{lo}, {hi}) of a {T}-token buffer")
+    row = 1 if (overlap and i > 0) else 0
+    res = torch.empty((B, (hi - lo) // m, d), dtype=Ca.dtype, device=Ca.device)
+    for b in range(B):   # one call per batch row: the window of each row is contiguous
+        L.csa_compress(Ca[b:b + 1, lo:hi], Za[b:b + 1, lo:hi], m,
+                       Cb=None if Cb is None else Cb[b:b + 1, lo:hi],
+                       Zb=None if Zb is None else Zb[b:b + 1, lo:hi], Ba=Ba, Bb=Bb,
+                       out=res[b:b + 1])
+    return res[:, row]
+
+
 class GraphForward:
     """A layer forward replayed as one CUDA graph, host transfers included.
 

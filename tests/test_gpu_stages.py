@@ -422,3 +422,24 @@ def test_index_topk_workspace_left_zero(K, fmt, B, N):
         K.device_error()
         assert torch.equal(s, s0) and torch.equal(i, i0)
         assert int(ws.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("kind,m,T,ents", [("csa", 4, 4096, [0, 1, 2, 511, 1023]), ("hca", 128, 4096, [0, 1, 31])])
+def test_compress_entry_matches_whole_sequence(K, kind, m, T, ents):
+    # the entry a closing block adds during decode equals that entry of the
+    # whole-sequence compression (oracle)
+    from compressed_sparse_long_05_b300 import path as P
+    B, d = 2, 512
+    Ca = _rms((B, T, d), 140)
+    Za = _randn((B, T, d), torch.bfloat16, 141)
+    Cb = _rms((B, T, d), 142) if kind == "csa" else None
+    Zb = _randn((B, T, d), torch.bfloat16, 143) if kind == "csa" else None
+    for b in range(B):
+        if kind == "csa":
+            ref = O.compress_csa(f64(Ca[b]), f64(Cb[b]), f64(Za[b]), f64(Zb[b]), m)
+        else:
+            ref = O.compress_hca(f64(Ca[b]), f64(Za[b]), m)
+        for i in ents:
+            got = P.compress_entry(i, m, Ca, Za, Cb=Cb, Zb=Zb)
+            torch.cuda.synchronize()
+            assert_close(f64(got[b]), ref[i], TOL_BF16, TOL_BF16, f"{kind} entry {i} b={b}")
