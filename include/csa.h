@@ -39,7 +39,7 @@ extern "C" {
 typedef enum {
   CSA_OK = 0,
   CSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size or misaligned pointer */
-  CSA_ERR_UNSUPPORTED = 2,  /* valid arguments this build has no kernel for */
+  CSA_ERR_UNSUPPORTED = 2,  /* valid arguments for which the library has no kernel */
   CSA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   CSA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
   CSA_ERR_TIMEOUT = 5,      /* device error word: a bounded wait gave up */
