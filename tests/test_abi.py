@@ -70,3 +70,23 @@ def test_host_side_argument_errors(L):
                         127, 10000.0, None, 0, None) == 1
     # empty batch is a no-op
     assert L.csa_topk(fake, fake, 0, 1, 100, 5, 4, 0, None) == 0
+
+
+def test_workspace_sizes_follow_the_plan(L):
+    # host-side planning only (no device is touched)
+    L.csa_index_topk_workspace_size.restype = ctypes.c_size_t
+    L.csa_attend_workspace_size.restype = ctypes.c_size_t
+    # the histogram workspace of the fused decode call: one 2048-bin row per batch row
+    assert L.csa_index_topk_workspace_size(4, 1, 32768, 1) == 4 * 2048 * 4
+    assert L.csa_index_topk_workspace_size(8, 1, 262144, 3) == 8 * 2048 * 4
+    assert L.csa_index_topk_workspace_size(1, 2, 32768, 1) == 0          # not a decode row
+    assert L.csa_index_topk_workspace_size(1, 1, 32768, 0) == 0          # fp32 scores: two calls
+    # decode, 128K context, batch 4: 9 chunks of 128 rows per head group; unless the
+    # chunks merge inside a cluster, each keeps a [64 heads][512] fp32 partial
+    ws = L.csa_attend_workspace_size(4, 1, 32768, 1024, 128, 128, 512, 64, 4, 128, 131071, 1, 1, 0)
+    assert ws == 0 or ws >= 72 * 64 * 512 * 4
+    # causal prefill: every stored row is rotated once into the workspace (1 KB per row)
+    ws = L.csa_attend_workspace_size(1, 32768, 8192, 1024, 32768, 128, 512, 64, 4, 128, 0, 1, 1, 0)
+    assert ws >= (8192 + 32768) * 1024
+    # shapes the tensor-core path does not take need no workspace
+    assert L.csa_attend_workspace_size(1, 1, 100, 16, 16, 4, 128, 32, 4, 16, 399, 0, 0, 0) == 0
