@@ -148,8 +148,9 @@ def compress_hca(C, Z, m: int, Bias=None) -> np.ndarray:
 
 
 def visible_count(t: int, m: int) -> int:
-    """Number of compressed entries query t may see: entries s with (s+1)m <= t+1."""
-    return (t + 1) // m
+    """Number of compressed entries query t may see: entries s with (s+1)m <= t+1
+    (none for a query at a negative position)."""
+    return max(0, (t + 1) // m)
 
 
 def index_scores(qI, w, K, t_pos, m: int) -> np.ndarray:

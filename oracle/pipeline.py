@@ -46,19 +46,23 @@ def indexer_inputs(x: dict, b: int, rows):
 def run_rows(cfg: dict, x: dict, b: int, rows, selected=None, entries=None):
     """Oracle outputs for query rows ``rows`` of batch row b.
 
-    Returns a dict with 'scores' [len(rows), N] (CSA only), 'selected' (list of
-    index arrays, CSA only) and 'out' [len(rows), n_h, d].  ``selected`` may
-    supply the index sets the attention uses (e.g. a set already checked
-    against the oracle's own top-k rule); ``entries`` may supply precomputed
-    compressed entries.
+    Query row i sits at absolute position x["q_pos"][b][i]; row j of the
+    window buffer of batch row b holds raw token x["win_base"][b] + j.
+
+    Returns a dict with 't' (the rows' positions), 'scores' [len(rows), N]
+    (CSA only), 'selected' (list of index arrays, CSA only) and 'out'
+    [len(rows), n_h, d].  ``selected`` may supply the index sets the attention
+    uses (e.g. a set already checked against the oracle's own top-k rule);
+    ``entries`` may supply precomputed compressed entries.
     """
     rows = np.asarray(rows, dtype=np.int64)
     m, r, base, n_win = cfg["m"], cfg["r"], cfg["rope_base"], cfg["n_win"]
-    t_pos = cfg["q_pos0"] + rows
+    t_pos = np.asarray(x["q_pos"][b], dtype=np.int64)[rows]
+    win_base = int(np.asarray(x["win_base"])[b])
     ent = entries_of(cfg, x, b) if entries is None else entries
     win = window_of(x, b)
     q = x["q"][b]
-    res = {}
+    res = {"t": t_pos}
     outs = []
     if cfg["kind"].startswith("csa"):
         qI, K = indexer_inputs(x, b, rows)
@@ -71,11 +75,10 @@ def run_rows(cfg: dict, x: dict, b: int, rows, selected=None, entries=None):
         res["selected"] = selected
         for i, t in enumerate(t_pos):
             outs.append(O.csa_attend_token(np.asarray(q[rows[i]], dtype=np.float64), int(t), ent,
-                                           selected[i], win, cfg["win_base"], x["sink"], m, n_win,
-                                           r, base))
+                                           selected[i], win, win_base, x["sink"], m, n_win, r, base))
     else:
         for i, t in enumerate(t_pos):
             outs.append(O.hca_attend_token(np.asarray(q[rows[i]], dtype=np.float64), int(t), ent,
-                                           win, cfg["win_base"], x["sink"], m, n_win, r, base))
+                                           win, win_base, x["sink"], m, n_win, r, base))
     res["out"] = np.stack(outs) if outs else np.zeros((0,))
     return res

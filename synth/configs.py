@@ -63,28 +63,55 @@ def get(name: str) -> dict:
 
 
 def scaled(name: str, **overrides) -> dict:
-    """A copy of workload ``name`` with some sizes replaced (for parity cases)."""
+    """A copy of workload ``name`` with some sizes replaced (for parity cases);
+    ``lengths`` (decode) gives each sequence its own context length."""
     cfg = copy.deepcopy(WORKLOADS[name])
     cfg.update(overrides)
-    cfg["name"] = name + "".join(f"_{k}{v}" for k, v in sorted(overrides.items()))
+
+    def tag(v):
+        return "-".join(map(str, v)) if isinstance(v, (list, tuple)) else str(v)
+    cfg["name"] = name + "".join(f"_{k}{tag(v)}" for k, v in sorted(overrides.items()))
     return derive(cfg)
 
 
 def derive(cfg: dict) -> dict:
-    """Fill in the derived sizes: entry count N and query count/positions."""
+    """Fill in the derived sizes: entry count N, query count and the context
+    length of each sequence.
+
+    Prefill: every sequence has T tokens, query row i sits at token i and the
+    window buffer holds all T tokens.  Decode: sequence b holds lengths[b]
+    tokens (default L for every sequence; the new token is the last one, at
+    position lengths[b] - 1), the compressed cache is sized for the longest
+    sequence and the window buffer holds each sequence's last n_win tokens.
+    """
     kind = cfg["kind"]
     if kind.endswith("prefill"):
         cfg["N"] = cfg["T"] // cfg["m"]
         cfg["Tq"] = cfg["T"]
-        cfg["q_pos0"] = 0            # query i sits at absolute position i
         cfg["T_win"] = cfg["T"]      # window buffer holds every token
-        cfg["win_base"] = 0
+        cfg["lengths"] = [cfg["T"]] * cfg["B"]
     else:
-        L = cfg["L"]
-        cfg["N"] = L // cfg["m"]
+        lengths = list(cfg.get("lengths") or [cfg["L"]] * cfg["B"])
+        if len(lengths) != cfg["B"] or min(lengths) < 1:
+            raise ValueError("one context length >= 1 per sequence")
+        cfg["lengths"] = lengths
+        cfg["L"] = max(lengths)
+        cfg["N"] = cfg["L"] // cfg["m"]
         cfg["Tq"] = 1
-        cfg["q_pos0"] = L - 1        # the new token is the last of the context
         cfg["T_win"] = cfg["n_win"]  # window buffer holds the last n_win tokens
-        cfg["win_base"] = L - cfg["n_win"]
     cfg.setdefault("rope_base", ROPE_BASE)
     return cfg
+
+
+def query_positions(cfg: dict):
+    """Absolute token position of every query row: [B][Tq] nested lists."""
+    if cfg["kind"].endswith("prefill"):
+        return [list(range(cfg["T"])) for _ in range(cfg["B"])]
+    return [[L - 1] for L in cfg["lengths"]]
+
+
+def window_bases(cfg: dict):
+    """Token held by row 0 of each sequence's window buffer."""
+    if cfg["kind"].endswith("prefill"):
+        return [0] * cfg["B"]
+    return [max(0, L - cfg["n_win"]) for L in cfg["lengths"]]

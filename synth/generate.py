@@ -10,7 +10,9 @@ name and seed):
 * compression logits Z^a, Z^b, Z: N(0,1);
 * indexer queries and keys: N(0,1) * qk_scale (1/sqrt(c_I));
 * indexer head weights w: U(0,1) * w_scale;
-* per-head sink logits z'_h: N(0,1).
+* per-head sink logits z'_h: N(0,1);
+* query positions q_pos [B, Tq] and window-buffer bases win_base [B] (int32)
+  from the workload's context lengths (synth.configs.derive).
 
 The mixed-precision workload stores the first d-r dims of every entry as FP8
 e4m3 with one float32 scale per entry (amax/448) and the last r (RoPE) dims as
@@ -164,6 +166,9 @@ def make_inputs(cfg: dict, seed: int = 0, device="cpu") -> dict:
     def g(t):
         return _gen(device, name, t, seed)
 
+    from .configs import query_positions, window_bases
+    out["q_pos"] = torch.tensor(query_positions(cfg), dtype=torch.int32, device=device)
+    out["win_base"] = torch.tensor(window_bases(cfg), dtype=torch.int32, device=device)
     out["q"] = normal((B, Tq, n_h, d), dt, device, g("q"), rms_normalise=True)
     out["sink"] = normal((n_h,), torch.float32, device, g("sink"))
 
