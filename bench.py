@@ -105,12 +105,22 @@ def row_bytes(cfg):
 
 
 def work(cfg):
-    """{stage: (bytes, flops)} for one step of the workload."""
-    B, Tq, N, m, d = cfg["B"], cfg["Tq"], cfg["N"], cfg["m"], cfg["d"]
-    n_h, n_win, q0 = cfg["n_h"], cfg["n_win"], cfg["q_pos0"]
+    """{stage: (bytes, flops)} for one step of the workload (summed over its
+    sequences, each at its own query positions)."""
+    out = {}
+    for L_b, pos in zip(cfg["lengths"], synth.configs.query_positions(cfg)):
+        one = dict(cfg, B=1, lengths=[L_b])
+        for st, (b, f) in _work_one(one, np.asarray(pos, dtype=np.int64)).items():
+            b0, f0 = out.get(st, (0, 0.0))
+            out[st] = (b0 + b, f0 + f)
+    return out
+
+
+def _work_one(cfg, t):
+    B, Tq, N, m, d = 1, cfg["Tq"], cfg["N"], cfg["m"], cfg["d"]
+    n_h, n_win = cfg["n_h"], cfg["n_win"]
     el = 4 if cfg["dtype"] == "f32" else 2
     rb = row_bytes(cfg)
-    t = q0 + np.arange(Tq, dtype=np.int64)
     vis = np.minimum(N, (t + 1) // m)
     win = np.minimum(n_win, t + 1)
     out = {}
@@ -228,7 +238,7 @@ def make_step(K, cfg, x, buf):
     """Stage callables of one step on inputs x (device tensors) with buffers buf."""
     from compressed_sparse_long_05_b300 import path as P
     m, r, n_win = cfg["m"], cfg["r"], cfg["n_win"]
-    q0, wb, base = cfg["q_pos0"], cfg["win_base"], cfg["rope_base"]
+    q0, wb, base = x["q_pos"], x["win_base"], cfg["rope_base"]
     kind = cfg["kind"]
     stages = []
     if kind == "csa_prefill":
@@ -275,7 +285,7 @@ def alloc_buffers(K, cfg, x, dev):
     buf.out = torch.empty_like(x["q"])
     ent = buf.entries if kind.endswith("prefill") else P._entries_arg(x)
     nbytes = K.attend_workspace_size(x["q"], ent, P._win_arg(x), cfg.get("k", 0), cfg["m"],
-                                     cfg["n_win"], cfg["q_pos0"], cfg["r"], not kind.startswith("csa"))
+                                     cfg["n_win"], cfg["r"], not kind.startswith("csa"))
     buf.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
     return buf
 
@@ -298,7 +308,21 @@ def count_kernel_nodes(step, stream):
     return kern
 
 
-def gpu_arm(args, cfg, rank, world):
+def config_dict(cfg):
+    """The `config` object of a JSON line: the workload and its sizes."""
+    out = {k: cfg[k] for k in ("B", "Tq", "N", "d", "r", "n_h", "m", "n_win") if k in cfg}
+    for k in ("L", "T", "k", "H_I", "c_I"):
+        if k in cfg:
+            out[k] = cfg[k]
+    if len(set(cfg["lengths"])) > 1:
+        out["lengths"] = cfg["lengths"]
+    out.update({"workload": cfg["name"], "kind": cfg["kind"], "storage": cfg["dtype"]})
+    return out
+
+
+def gpu_arm(args, cfg, rank, world, with_e2e=True):
+    """Times `args.steps` steps of workload `cfg` on this rank's GPU; returns
+    (JSON line fields, the first input copy)."""
     import compressed_sparse_long_05_b300 as K
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -383,7 +407,11 @@ def gpu_arm(args, cfg, rank, world):
         torch.distributed.barrier()
     K.device_error()
 
-    # ---------------- per-stage durations (same launches, events between stages) ----------------
+    # ---------------- per-stage durations ----------------
+    # The same launches with an event recorded between stages, on the stream
+    # they run on.  An event between two kernels keeps the second from
+    # starting while the first drains, so the stage times add up to a little
+    # more than the step time above (which lets consecutive kernels overlap).
     names = [n for n, _ in steps[0]]
     stage_ms = {n: [] for n in names}
     reps = min(args.steps, 200) if use_graph else min(args.steps, 5)
@@ -407,7 +435,7 @@ def gpu_arm(args, cfg, rank, world):
     stage_avg = {n: float(np.mean(v)) for n, v in stage_ms.items()}
 
     # ---------------- end to end through the public API, host buffers ----------------
-    e2e = e2e_leg(K, cfg, xs[0], bufs[0], stream, args, dev)
+    e2e = e2e_leg(K, cfg, xs[0], bufs[0], stream, args, dev) if with_e2e else None
 
     ms_step = ms_total / args.steps
     tokens_per_step = cfg["B"] * cfg["Tq"] * world
@@ -441,23 +469,20 @@ def gpu_arm(args, cfg, rank, world):
             kernels[n]["TFLOP/s"] = round(tf, 1)
             kernels[n]["tensor_frac"] = round(tf / tf_sust, 4)
     step_frac_hbm = step_bytes / (ms_step / 1e3) / 1e9 / hbm_peak
-    cfg_out = {k: cfg[k] for k in ("B", "Tq", "N", "d", "r", "n_h", "m", "n_win") if k in cfg}
-    for k in ("L", "T", "k", "H_I", "c_I"):
-        if k in cfg:
-            cfg_out[k] = cfg[k]
-    cfg_out.update({"workload": cfg["name"], "kind": cfg["kind"], "storage": cfg["dtype"],
-                    "l2": f"inputs rotate over {copies} copies (> 2x L2 per cycle)",
-                    "graph": use_graph})
+    cfg_out = config_dict(cfg)
+    cfg_out.update({"l2": f"inputs rotate over {copies} copies (> 2x L2 per cycle)"
+                    if copies > 1 else "inputs larger than 2x L2", "graph": use_graph})
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if cfg["dtype"] != "f32" else "f32", "data": "synthetic",
         "config": cfg_out, "roofline": roof, "step_hbm_frac": round(step_frac_hbm, 4),
         "kernels": kernels, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
-    return line, xs[0]
+    x_first = xs[0]
+    del xs, bufs, steps, cycle, singles, inst_graphs
+    torch.cuda.synchronize()
+    return line, x_first
 
 
 def e2e_leg(K, cfg, x, buf, stream, args, dev):
@@ -517,18 +542,38 @@ def e2e_leg(K, cfg, x, buf, stream, args, dev):
 # ----------------------------------------------------------------------------
 
 
+def cpu_info():
+    """(logical cores usable by this process, CPU model name)."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except Exception:
+        cores = os.cpu_count() or 1
+    model = "unknown"
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return cores, model
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        return 1
+
+
 def oracle_sample(cfg, x_np, budget_s):
     """Runs the oracle on query rows of the workload until ~budget_s elapsed.
 
-    Returns (tokens/s, description, threads).  Prefill workloads count the
-    compression of one batch row in full plus whole query rows of the rest.
+    Returns (tokens/s, description).  Prefill workloads count the compression
+    of one batch row in full plus whole query rows of the rest.
     """
     from oracle import pipeline as OP
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-    except Exception:
-        threads = os.cpu_count() or 1
     kind = cfg["kind"]
     t_start = time.perf_counter()
     done_rows = 0
@@ -557,16 +602,60 @@ def oracle_sample(cfg, x_np, budget_s):
         t_step_per_row = t_comp + per_row * rows_total
         tps = rows_total / t_step_per_row
         desc = (f"compression of one {cfg['T']}-token sequence in full ({t_comp:.2f}s) + "
-                f"{done_rows} query rows of index/top-k/attend; tokens/s = T / (compress + T x per-row)")
+                f"{done_rows} query rows of index/top-k/attend; tokens/s = T / (compress + T x "
+                "per-row time), extrapolated from the sampled rows")
     else:
         tps = 1.0 / per_row
         desc = f"{done_rows} decode query rows (index over all N entries, top-k, attend)"
-    return tps, desc, threads
+    return tps, desc
+
+
+def cpu_baseline(cfg, x_np, budget_s):
+    """The oracle timed on this host: its BLAS thread pool as it stands, and
+    one thread, on bounded samples of the workload (~2/3 and ~1/3 of budget_s)."""
+    cores, model = cpu_info()
+    threads = blas_threads()
+    tps, desc = oracle_sample(cfg, x_np, budget_s * 2 / 3)
+    try:
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=1):
+            tps1, _ = oracle_sample(cfg, x_np, budget_s / 3)
+    except Exception:
+        tps1 = None
+    return {"value": round(tps, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": desc, "nproc": cores, "cpu_model": model,
+            "value_1_thread": None if tps1 is None else round(tps1, 4),
+            "threads_note": "float64 numpy oracle: its row loop is serial Python; only the BLAS "
+                            f"matrix products use the {threads}-thread pool"}
+
+
+class _RowView:
+    """Read-only view of a large tensor for the oracle: indexing down to a
+    2-D (or smaller) slice returns that slice alone as a float32/int numpy
+    array, so a sampled row never needs the whole tensor on the host."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, k):
+        if isinstance(k, (np.ndarray, list)):          # a set of rows: fetch just those
+            return _np(self.t[torch.as_tensor(np.asarray(k), device=self.t.device)])
+        v = self.t[k]
+        return _RowView(v) if v.dim() > 2 else _np(v)
+
+    def __len__(self):
+        return self.t.shape[0]
+
+
+def _np(v):
+    return v.float().cpu().numpy() if v.dtype in (torch.bfloat16, torch.float32) else v.cpu().numpy()
 
 
 def host_copy(x):
-    return {k: (v.float().cpu().numpy() if v.dtype in (torch.bfloat16, torch.float32)
-                else v.cpu().numpy()) for k, v in x.items()}
+    """Inputs as the oracle reads them: numpy copies, except that tensors above
+    256 MB stay where they are behind a per-row view."""
+    return {k: (_RowView(v) if v.numel() * v.element_size() > (256 << 20) else _np(v))
+            for k, v in x.items()}
 
 
 def reference_arm(args, cfg, rank, world):
@@ -583,24 +672,27 @@ def reference_arm(args, cfg, rank, world):
     for _ in range(warm):
         oracle_sample(cfg, xn, min(0.2, per_step_budget))
     vals = []
-    desc, threads = "", 1
+    desc = ""
     for s in range(run_steps):
-        tps, desc, threads = oracle_sample(cfg, xn, per_step_budget)
+        tps, desc = oracle_sample(cfg, xn, per_step_budget)
         vals.append(tps)
     value = float(np.mean(vals))
     tokens = cfg["B"] * cfg["Tq"]
+    cores, model = cpu_info()
+    cfg_out = config_dict(cfg)
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
             "n_gpus": world, "steps": run_steps, "steps_requested": args.steps, "warmup": warm,
             "ms_per_step": round(tokens / value * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg["name"], "kind": cfg["kind"]},
-            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": threads,
-                             "kind": "oracle", "sample": desc + f"; {run_steps} sample steps of ~{per_step_budget:.0f}s"},
+            "config": cfg_out,
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": blas_threads(),
+                             "kind": "oracle", "nproc": cores, "cpu_model": model,
+                             "sample": desc + f"; {run_steps} sample steps of ~{per_step_budget:.0f}s"},
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
-# ----------------------------------------------------------------------------
+PREFILL_WORKLOAD = "csa_prefill_32k"
 
 
 def main():
@@ -611,17 +703,27 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.configs.WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle CPU work")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="default workload only: skip the 32K-prefill half of the metric")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=INT",
                     help="override a size of the workload (smaller cases for profiling)")
     args = ap.parse_args()
     over = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.set}
     cfg = synth.scaled(args.workload, **over) if over else synth.get(args.workload)
     decode = cfg["kind"].endswith("decode")
+    steps_given, warm_given = args.steps, args.warmup
     if args.steps is None:
         args.steps = 20000 if decode else 10
     if args.warmup is None:
         args.warmup = 50 if decode else 3
     args.warmup = max(3, args.warmup)
+    # the metric is quoted at decode @128K and prefill @32K: the default run times both
+    with_prefill = args.workload == DEFAULT_WORKLOAD and not over and not args.no_prefill
+    pcfg = synth.get(PREFILL_WORKLOAD) if with_prefill else None
+    pargs = argparse.Namespace(**vars(args))
+    pargs.steps = steps_given if steps_given is not None else 10
+    pargs.steps = max(3, min(pargs.steps, 20))
+    pargs.warmup = max(3, min(warm_given if warm_given is not None else 3, 5))
 
     world = int(os.environ.get("WORLD_SIZE", 1))
     rank = int(os.environ.get("RANK", 0))
@@ -629,18 +731,33 @@ def main():
         backend = "nccl" if args.impl == "native" else "gloo"
         torch.distributed.init_process_group(backend)
 
+    common = {"metric": METRIC, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "data": "synthetic"}
     if args.impl == "reference":
         line = reference_arm(args, cfg, rank, world)
+        if rank == 0 and with_prefill:
+            pline = reference_arm(pargs, pcfg, rank, world)
+            line["prefill_32k"] = {k: pline[k] for k in ("value", "unit", "ms_per_step", "config",
+                                                         "cpu_baseline")}
         if rank == 0:
             print(json.dumps(line), flush=True)
     else:
-        line, x0 = gpu_arm(args, cfg, rank, world)
+        fields, x0 = gpu_arm(args, cfg, rank, world)
+        line = dict(common)
+        line.update(fields)
+        line["dtype"] = "bf16" if cfg["dtype"] != "f32" else "f32"
+        if rank == 0 and world == 1:
+            line["cpu_baseline"] = cpu_baseline(cfg, host_copy(x0), args.cpu_budget)
+        del x0
+        if with_prefill:
+            pf, px0 = gpu_arm(pargs, pcfg, rank, world)
+            pf = {k: pf[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "config",
+                                     "roofline", "kernels", "e2e", "gpu_launches", "clocks")}
+            if rank == 0 and world == 1:
+                pf["cpu_baseline"] = cpu_baseline(pcfg, host_copy(px0), args.cpu_budget)
+            del px0
+            line["prefill_32k"] = pf
         if rank == 0:
-            if world == 1:
-                xn = host_copy(x0)
-                tps, desc, threads = oracle_sample(cfg, xn, args.cpu_budget)
-                line["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": threads,
-                                        "kind": "oracle", "sample": desc}
             print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()

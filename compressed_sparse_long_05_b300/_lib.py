@@ -38,14 +38,14 @@ _lib = None
 _I, _P, _F, _Z = ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
     "csa_compress": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
-    "csa_index": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
-    "csa_topk": [_P, _P, _I, _I, _I, _I, _I, _I, _P],
-    "csa_index_topk": [_P, _P, _P, _P, _P, _P, _P] + [_I] * 9 + [_P, _Z, _P],
+    "csa_index": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
+    "csa_topk": [_P, _P, _P, _I, _I, _I, _I, _I, _P],
+    "csa_index_topk": [_P, _P, _P, _P, _P, _P, _P, _P] + [_I] * 8 + [_P, _Z, _P],
     "csa_index_topk_workspace_size": [_I] * 4,
-    "csa_attend": [_P, KV, _P, KV, _P, _P] + [_I] * 12 + [_F, _P, _Z, _P],
-    "hca_attend": [_P, KV, KV, _P, _P] + [_I] * 11 + [_F, _P, _Z, _P],
-    "csa_attend_noalloc": [_P, KV, _P, KV, _P, _P] + [_I] * 12 + [_F, _P],
-    "csa_attend_workspace_size": [_I] * 14,
+    "csa_attend": [_P, KV, _P, KV, _P, _P, _P, _P] + [_I] * 10 + [_F, _P, _Z, _P],
+    "hca_attend": [_P, KV, KV, _P, _P, _P, _P] + [_I] * 10 + [_F, _P, _Z, _P],
+    "csa_attend_noalloc": [_P, KV, _P, KV, _P, _P, _P, _P] + [_I] * 10 + [_F, _P],
+    "csa_attend_workspace_size": [_I] * 13,
     "csa_device_error": [_P],
     "csa_status_string": [_I],
     "csa_last_cuda_error": [],
@@ -101,6 +101,32 @@ def _kv(rows):
     return KV(_dt(rows), rows.data_ptr(), None, None)
 
 
+def positions(q_pos, B, Tq, device):
+    """Query positions as the library takes them: None (row i at position i),
+    an int p0 (row i of every batch row at p0 + i) made into a [B, Tq] int32
+    device tensor, or such a tensor as given."""
+    if q_pos is None or (isinstance(q_pos, int) and q_pos == 0):
+        return None
+    if isinstance(q_pos, int):
+        t = torch.arange(q_pos, q_pos + Tq, dtype=torch.int32, device=device)
+        return t.unsqueeze(0).expand(B, Tq).contiguous()
+    if q_pos.dtype != torch.int32 or tuple(q_pos.shape) != (B, Tq) or not q_pos.is_contiguous():
+        raise ValueError(f"q_pos must be a contiguous int32 [{B}, {Tq}] tensor")
+    return q_pos
+
+
+def window_bases(win_base, B, device):
+    """Window buffer bases: None (0), an int shared by every batch row, or an
+    int32 [B] device tensor."""
+    if win_base is None or (isinstance(win_base, int) and win_base == 0):
+        return None
+    if isinstance(win_base, int):
+        return torch.full((B,), win_base, dtype=torch.int32, device=device)
+    if win_base.dtype != torch.int32 or tuple(win_base.shape) != (B,) or not win_base.is_contiguous():
+        raise ValueError(f"win_base must be a contiguous int32 [{B}] tensor")
+    return win_base
+
+
 def _rows_shape(rows):
     if isinstance(rows, (tuple, list)):
         nope, _, rope = rows
@@ -121,30 +147,34 @@ def csa_compress(Ca, Za, m, Cb=None, Zb=None, Ba=None, Bb=None, out=None):
     return out
 
 
-def csa_index(qI, w, K, m, q_pos0, qI_sf=None, K_sf=None, scores=None):
-    """Indexer scores [B, Tq, N] float32 (-inf where not visible)."""
+def csa_index(qI, w, K, m, q_pos, qI_sf=None, K_sf=None, scores=None):
+    """Indexer scores [B, Tq, N] float32 (-inf where not visible).
+
+    ``q_pos``: query positions (see :func:`positions`)."""
     fp4 = qI.dtype == torch.uint8
     B, Tq, H = qI.shape[:3]
     c = qI.shape[3] * (2 if fp4 else 1)
     N = K.shape[1]
     dt = DT_E2M1_BLOCK16 if fp4 else _dt(qI)
+    qp = positions(q_pos, B, Tq, qI.device)
     if scores is None:
         scores = torch.empty((B, Tq, N), dtype=torch.float32, device=qI.device)
-    _check("csa_index", lib().csa_index(_p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(scores),
-                                        B, Tq, N, H, c, m, q_pos0, dt, _stream()))
+    _check("csa_index", lib().csa_index(_p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(qp),
+                                        _p(scores), B, Tq, N, H, c, m, dt, _stream()))
     return scores
 
 
-def csa_topk(scores, k, m, q_pos0, idx=None):
+def csa_topk(scores, k, m, q_pos, idx=None):
     """Selected entry indices [B, Tq, k] int32, ascending, -1 padded."""
     B, Tq, N = scores.shape
+    qp = positions(q_pos, B, Tq, scores.device)
     if idx is None:
         idx = torch.empty((B, Tq, k), dtype=torch.int32, device=scores.device)
-    _check("csa_topk", lib().csa_topk(_p(scores), _p(idx), B, Tq, N, k, m, q_pos0, _stream()))
+    _check("csa_topk", lib().csa_topk(_p(scores), _p(qp), _p(idx), B, Tq, N, k, m, _stream()))
     return idx
 
 
-def csa_index_topk(qI, w, K, k, m, q_pos0, qI_sf=None, K_sf=None, scores=None, idx=None, ws=None):
+def csa_index_topk(qI, w, K, k, m, q_pos, qI_sf=None, K_sf=None, scores=None, idx=None, ws=None):
     """Indexer scores and the top-k index sets of one call (same results as
     csa_index then csa_topk); returns (scores, idx, ws).
 
@@ -160,20 +190,21 @@ def csa_index_topk(qI, w, K, k, m, q_pos0, qI_sf=None, K_sf=None, scores=None, i
         scores = torch.empty((B, Tq, N), dtype=torch.float32, device=qI.device)
     if idx is None:
         idx = torch.empty((B, Tq, k), dtype=torch.int32, device=qI.device)
+    qp = positions(q_pos, B, Tq, qI.device)
     nbytes = lib().csa_index_topk_workspace_size(B, Tq, N, dt)
     ws = _workspace(ws, nbytes, qI.device, zero=True)   # histograms start zero; calls leave them zero
     _check("csa_index_topk", lib().csa_index_topk(
-        _p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(scores), _p(idx), B, Tq, N, H, c, m, q_pos0,
+        _p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(qp), _p(scores), _p(idx), B, Tq, N, H, c, m,
         k, dt, _p(ws) if nbytes else None, nbytes, _stream()))
     return scores, idx, ws
 
 
-def attend_workspace_size(q, entries, win, k, m, n_win, q_pos0, r, is_hca):
+def attend_workspace_size(q, entries, win, k, m, n_win, r, is_hca):
     B, Tq, n_h, d = q.shape
     _, N, _ = _rows_shape(entries)
     _, T_win, _ = _rows_shape(win)
     kv_dt = _kv(entries).dtype
-    return lib().csa_attend_workspace_size(B, Tq, N, k, T_win, n_h, d, r, m, n_win, q_pos0,
+    return lib().csa_attend_workspace_size(B, Tq, N, k, T_win, n_h, d, r, m, n_win,
                                            _dt(q), kv_dt, 1 if is_hca else 0)
 
 
@@ -185,24 +216,28 @@ def _workspace(ws, nbytes, device, zero=False):
     return ws
 
 
-def csa_attend(q, entries, idx, win, sink, m, n_win, win_base, q_pos0, r, rope_base=10000.0,
+def csa_attend(q, entries, idx, win, sink, m, n_win, win_base, q_pos, r, rope_base=10000.0,
                out=None, ws=None):
-    """Sparse shared-KV attention output [B, Tq, n_h, d] (dtype of q)."""
+    """Sparse shared-KV attention output [B, Tq, n_h, d] (dtype of q).
+
+    ``q_pos``: query positions (see :func:`positions`); ``win_base``: token of
+    window row 0 per batch row (see :func:`window_bases`)."""
     B, Tq, n_h, d = q.shape
     _, N, _ = _rows_shape(entries)
     _, T_win, _ = _rows_shape(win)
     k = idx.shape[2]
+    qp, wb = positions(q_pos, B, Tq, q.device), window_bases(win_base, B, q.device)
     if out is None:
         out = torch.empty_like(q)
-    nbytes = attend_workspace_size(q, entries, win, k, m, n_win, q_pos0, r, False)
+    nbytes = attend_workspace_size(q, entries, win, k, m, n_win, r, False)
     ws = _workspace(ws, nbytes, q.device)
     _check("csa_attend", lib().csa_attend(
-        _p(q), _kv(entries), _p(idx), _kv(win), _p(sink), _p(out), B, Tq, N, k, T_win, win_base,
-        n_h, d, r, m, n_win, q_pos0, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
+        _p(q), _kv(entries), _p(idx), _kv(win), _p(qp), _p(wb), _p(sink), _p(out), B, Tq, N, k,
+        T_win, n_h, d, r, m, n_win, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
     return out
 
 
-def csa_attend_noalloc(q, entries, idx, win, sink, m, n_win, win_base, q_pos0, r,
+def csa_attend_noalloc(q, entries, idx, win, sink, m, n_win, win_base, q_pos, r,
                        rope_base=10000.0, out=None):
     """csa_attend with its scratch in the library's fixed device array (no workspace).
 
@@ -213,27 +248,29 @@ def csa_attend_noalloc(q, entries, idx, win, sink, m, n_win, win_base, q_pos0, r
     _, N, _ = _rows_shape(entries)
     _, T_win, _ = _rows_shape(win)
     k = idx.shape[2]
+    qp, wb = positions(q_pos, B, Tq, q.device), window_bases(win_base, B, q.device)
     if out is None:
         out = torch.empty_like(q)
     _check("csa_attend_noalloc", lib().csa_attend_noalloc(
-        _p(q), _kv(entries), _p(idx), _kv(win), _p(sink), _p(out), B, Tq, N, k, T_win, win_base,
-        n_h, d, r, m, n_win, q_pos0, rope_base, _stream()))
+        _p(q), _kv(entries), _p(idx), _kv(win), _p(qp), _p(wb), _p(sink), _p(out), B, Tq, N, k,
+        T_win, n_h, d, r, m, n_win, rope_base, _stream()))
     return out
 
 
-def hca_attend(q, entries, win, sink, m, n_win, win_base, q_pos0, r, rope_base=10000.0,
+def hca_attend(q, entries, win, sink, m, n_win, win_base, q_pos, r, rope_base=10000.0,
                out=None, ws=None):
     """Dense (HCA) shared-KV attention output [B, Tq, n_h, d] (dtype of q)."""
     B, Tq, n_h, d = q.shape
     _, N, _ = _rows_shape(entries)
     _, T_win, _ = _rows_shape(win)
+    qp, wb = positions(q_pos, B, Tq, q.device), window_bases(win_base, B, q.device)
     if out is None:
         out = torch.empty_like(q)
-    nbytes = attend_workspace_size(q, entries, win, 0, m, n_win, q_pos0, r, True)
+    nbytes = attend_workspace_size(q, entries, win, 0, m, n_win, r, True)
     ws = _workspace(ws, nbytes, q.device)
     _check("hca_attend", lib().hca_attend(
-        _p(q), _kv(entries), _kv(win), _p(sink), _p(out), B, Tq, N, T_win, win_base, n_h, d, r,
-        m, n_win, q_pos0, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
+        _p(q), _kv(entries), _kv(win), _p(qp), _p(wb), _p(sink), _p(out), B, Tq, N, T_win, n_h, d,
+        r, m, n_win, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
     return out
 
 

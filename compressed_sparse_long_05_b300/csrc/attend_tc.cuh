@@ -76,11 +76,13 @@ struct AttendTcArgs {
   const float* win_scale;
   const __nv_bfloat16* win_rope;
   const int32_t* idx;            // [B, Tq, k] or null (dense)
+  const int32_t* q_pos;          // [B, Tq] query positions (null: t = i)
+  const int32_t* win_base;       // [B] token of window row 0 (null: 0)
   const float* sink;             // [n_h]
   __nv_bfloat16* out;            // [B, Tq, n_h, 512]
   float* part_o;                 // [items][64 heads][512 dims] (split mode)
   float* part_ml;                // [items][64][2]   (split mode)
-  int B, Tq, N, k, T_win, win_base, n_h, m, n_win, q_pos0;
+  int B, Tq, N, k, T_win, n_h, m, n_win;
   int HG;                        // head groups = n_h / 64
   int nch;                       // chunks per (query row, head group)
   int chunk_rows;                // rows per chunk (multiple of 128)
@@ -117,10 +119,13 @@ struct AttRow {
   long long t;
   int nsel;        // compressed rows (selected or visible)
   long long w0;    // first window token
+  long long wbase; // token of window buffer row 0 of batch row b
   int nrows;       // nsel + window size
   int r0, r1;      // this chunk's rows [r0, r1)
 };
 
+// The row set of work item `it`.  A negative position has no rows (its output
+// is zero); the gather warps flag it.
 CSA_DEVINL AttRow att_item(const AttendTcArgs& a, int it) {
   AttRow x;
   x.c = it % a.nch;
@@ -129,14 +134,20 @@ CSA_DEVINL AttRow att_item(const AttendTcArgs& a, int it) {
   rest /= a.HG;
   x.i = rest % a.Tq;
   x.b = rest / a.Tq;
-  x.t = (long long)a.q_pos0 + x.i;
-  long long vis = (x.t + 1) / a.m;
-  if (vis > a.N) vis = a.N;
-  if (vis < 0) vis = 0;
-  x.nsel = a.idx ? (int)min((long long)a.k, vis) : (int)vis;
-  x.w0 = x.t - a.n_win + 1;
-  if (x.w0 < 0) x.w0 = 0;
-  x.nrows = x.nsel + (int)(x.t - x.w0 + 1);
+  x.t = query_pos(a.q_pos, (long long)x.b * a.Tq + x.i, x.i);
+  x.wbase = window_base(a.win_base, x.b);
+  if (x.t < 0) {
+    x.nsel = 0;
+    x.w0 = 0;
+    x.nrows = 0;
+  } else {
+    long long vis = (x.t + 1) / a.m;
+    if (vis > a.N) vis = a.N;
+    x.nsel = a.idx ? (int)min((long long)a.k, vis) : (int)vis;
+    x.w0 = x.t - a.n_win + 1;
+    if (x.w0 < 0) x.w0 = 0;
+    x.nrows = x.nsel + (int)(x.t - x.w0 + 1);
+  }
   x.r0 = min(x.nrows, x.c * a.chunk_rows);
   x.r1 = min(x.nrows, x.r0 + a.chunk_rows);
   return x;
@@ -349,6 +360,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
     bool ok = true;
     for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
       const AttRow x = att_item(a, it);
+      if (x.t < 0 && gw == 0 && lane == 0 && x.c == 0 && x.hg == 0) csa_flag_error(ERRBIT_BAD_INDEX);
       if (x.r1 <= x.r0) continue;
       // ---- tiles ----
       for (int r0 = x.r0; r0 < x.r1 && ok; r0 += ATT_TILE, ++n) {
@@ -375,15 +387,19 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             }
           } else {
             const long long tok = x.w0 + (rr - x.nsel);
-            const size_t row = (size_t)x.b * a.T_win + (size_t)(tok - a.win_base);
-            if (a.kv_mixed) {
-              src = reinterpret_cast<const uint8_t*>(a.win) + row * (ATT_D - ATT_R);
-              rsrc = a.win_rope + row * ATT_R;
-              rscale = __ldg(a.win_scale + row);
+            if (tok >= x.wbase && tok < x.wbase + a.T_win) {
+              const size_t row = (size_t)x.b * a.T_win + (size_t)(tok - x.wbase);
+              if (a.kv_mixed) {
+                src = reinterpret_cast<const uint8_t*>(a.win) + row * (ATT_D - ATT_R);
+                rsrc = a.win_rope + row * ATT_R;
+                rscale = __ldg(a.win_scale + row);
+              } else {
+                src = reinterpret_cast<const uint8_t*>(a.win) + row * ATT_D * 2;
+              }
+              pos = tok;
             } else {
-              src = reinterpret_cast<const uint8_t*>(a.win) + row * ATT_D * 2;
+              csa_flag_error(ERRBIT_BAD_INDEX);   // outside this batch row's window buffer
             }
-            pos = tok;
           }
         }
         // rows with no source (past the chunk, index -1) take logit -inf in the softmax
@@ -828,7 +844,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
 struct CombineArgs {
   const float* part_o; const float* part_ml; const float* sink;
   __nv_bfloat16* out;
-  int Tq, n_h, HG, nch, q_pos0;
+  const int32_t* q_pos;           // [B, Tq] (null: t = i)
+  int Tq, n_h, HG, nch;
   int rel_rope;       // 1 = output already relative to t (no rotation)
   RopeFreqs rf;
 };
@@ -887,7 +904,7 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine_kernel(const Combi
   v8[7] = __shfl_down_sync(0xffffffffu, acc.w, 1);
   if (half == 0) {
     if (!a.rel_rope && db >= ATT_D - ATT_R) {
-      const long long t = (long long)a.q_pos0 + i;
+      const long long t = query_pos(a.q_pos, bi, i);
 #pragma unroll
       for (int p = 0; p < CMB_DIMS / 2; ++p) {
         float cs, sn;
@@ -911,7 +928,7 @@ struct RotateArgs {
   long long rows;                 // B * rows per batch row
   int rows_per_b;
   int m;                          // >0: compressed entries (pos = m(s+1)-1); 0: tokens
-  long long base;                 // token position of row 0 (tokens)
+  const int32_t* base;            // tokens: [B] token position of each batch row's row 0 (null: 0)
   RopeFreqs rf;
 };
 
@@ -925,7 +942,8 @@ __global__ void __launch_bounds__(256) rope_rotate_rows_kernel(const RotateArgs 
   uint4 v = __ldg(reinterpret_cast<const uint4*>(a.src + row * ATT_D + u * 8));
   if (u >= (ATT_D - ATT_R) / 8) {
     const long long s = row % a.rows_per_b;
-    const long long pos = a.m > 0 ? (long long)a.m * (s + 1) - 1 : a.base + s;
+    const long long pos = a.m > 0 ? (long long)a.m * (s + 1) - 1
+                                  : window_base(a.base, (int)(row / a.rows_per_b)) + s;
     v = rope_unit(v, pos, a.rf, (u - (ATT_D - ATT_R) / 8) * 4);
   }
   *reinterpret_cast<uint4*>(a.dst + row * ATT_D + u * 8) = v;

@@ -20,6 +20,16 @@ enum : unsigned int {
 
 CSA_DEVINL void csa_flag_error(unsigned int bit) { atomicOr(&g_csa_error_word, bit); }
 
+// Absolute token position of query row `row` = b * Tq + i: q_pos[row] when the
+// caller passed positions, else i (causal prefill from token 0).
+CSA_DEVINL long long query_pos(const int32_t* q_pos, long long row, int i) {
+  return q_pos ? (long long)__ldg(q_pos + row) : (long long)i;
+}
+// Window buffer base token of batch row b (0 without a base array).
+CSA_DEVINL long long window_base(const int32_t* win_base, int b) {
+  return win_base ? (long long)__ldg(win_base + b) : 0LL;
+}
+
 // Programmatic dependent launch.  Every kernel lets the next launch in the
 // stream start as early as possible (its prologue overlaps this grid's tail),
 // and waits for the previous grid to complete and flush before its first global

@@ -177,12 +177,12 @@ csa_status_t plan_index(csa::IndexTcArgs& a, int QT, int B, int Tq, int N) {
 
 template <int H>
 csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w, const void* K,
-                              const void* K_sf, float* scores, int B, int Tq, int N, int m,
-                              int q_pos0, uint32_t* hist, cudaStream_t stream) {
+                              const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
+                              int N, int m, uint32_t* hist, cudaStream_t stream) {
   csa::IndexFp4Args fa;
   memset(&fa, 0, sizeof(fa));
   csa::IndexTcArgs& a = fa.t;
-  a.w = w; a.scores = scores; a.B = B; a.Tq = Tq; a.N = N; a.m = m; a.q_pos0 = q_pos0;
+  a.w = w; a.scores = scores; a.q_pos = q_pos; a.B = B; a.Tq = Tq; a.N = N; a.m = m;
   csa_status_t st = plan_index(a, 128 / H, B, Tq, N);
   if (st != CSA_OK) return st;
   if ((long long)B * N >= 0x7fffffffLL || (long long)B * Tq * H >= 0x7fffffffLL)
@@ -214,10 +214,12 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
 }
 
 template <int H, int C>
-csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, float* scores, int B,
-                             int Tq, int N, int m, int q_pos0, uint32_t* hist, cudaStream_t stream) {
+csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, const int32_t* q_pos,
+                             float* scores, int B, int Tq, int N, int m, uint32_t* hist,
+                             cudaStream_t stream) {
   csa::IndexTcArgs a;
-  a.w = w; a.scores = scores; a.B = B; a.Tq = Tq; a.N = N; a.m = m; a.q_pos0 = q_pos0;
+  memset(&a, 0, sizeof(a));
+  a.w = w; a.scores = scores; a.q_pos = q_pos; a.B = B; a.Tq = Tq; a.N = N; a.m = m;
   csa_status_t st = plan_index(a, 256 / H, B, Tq, N);
   if (st != CSA_OK) return st;
   const int sms = sm_count();
@@ -296,17 +298,16 @@ int attend_max_clusters(int cl) {
   return cache[cl];
 }
 
-AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int m, int n_win, int q_pos0,
-                    int dense, int kv_mixed) {
+// The split is sized for the widest row set any query can have: min(k, N)
+// (CSA) or N (HCA) entries plus n_win window tokens.  Queries with fewer rows
+// leave their last chunks short or empty.
+AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int n_win, int dense,
+                    int kv_mixed) {
   AttPlan p;
   memset(&p, 0, sizeof(p));
   p.HG = n_h / csa::ATT_HG;
-  const long long t_last = (long long)q_pos0 + Tq - 1;
-  long long vis = (t_last + 1) / m;
-  if (vis > N) vis = N;
-  const long long nsel = dense ? vis : (vis < k ? vis : k);
-  const long long win = t_last + 1 < n_win ? t_last + 1 : n_win;
-  const long long rows_max = nsel + win;
+  const long long nsel = dense ? N : (N < k ? N : k);
+  const long long rows_max = nsel + n_win;
   const int tiles = (int)((rows_max + csa::ATT_TILE - 1) / csa::ATT_TILE);
   const long long units = (long long)B * Tq * p.HG;
   const int sms = sm_count();
@@ -392,8 +393,8 @@ csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t s
 // CTAs (rows up to 16 x 32768 entries); 1024 threads per CTA when few CTAs
 // run, else 512.  `hist` (optional): per-row histograms of the first
 // IDX_HBITS key bits of the visible scores, built by the index kernel.
-csa_status_t launch_topk2(const float* scores, int32_t* idx, int rows, int Tq, int N, int k, int m,
-                          int q_pos0, uint32_t* hist, cudaStream_t st) {
+csa_status_t launch_topk2(const float* scores, const int32_t* q_pos, int32_t* idx, int rows, int Tq,
+                          int N, int k, int m, uint32_t* hist, cudaStream_t st) {
   int CL = 1;
   if (N > 32768) {
     CL = 8;
@@ -412,7 +413,7 @@ csa_status_t launch_topk2(const float* scores, int32_t* idx, int rows, int Tq, i
   int cand_cap = (int)((budget - fixed) / 4);
   if (cand_cap > slice) cand_cap = slice;
   const size_t smem = csa::topk2_smem_bytes(slice, cand_cap, bits1, merge);
-  csa::Topk2Args a{scores, idx, Tq, N, k, m, q_pos0, slice, cand_cap, hist};
+  csa::Topk2Args a{scores, idx, q_pos, Tq, N, k, m, slice, cand_cap, hist};
   const bool wide = (long long)rows * CL <= 2LL * sm_count();
   if (hist) return wide ? launch_topk2_nt<1024, csa::IDX_HBITS>(a, CL, rows, smem, st)
                         : launch_topk2_nt<512, csa::IDX_HBITS>(a, CL, rows, smem, st);
@@ -495,16 +496,16 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
 
 // ---------------------------------------------------------------------------
 static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w, const void* K,
-                              const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
-                              int m, int q_pos0, int dtype, uint32_t* hist, void* stream) {
-  if (B < 0 || Tq < 0 || N < 0 || H <= 0 || c <= 0 || m <= 0 || q_pos0 < 0)
-    return CSA_ERR_INVALID_ARG;
+                              const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
+                              int N, int H, int c, int m, int dtype, uint32_t* hist, void* stream) {
+  if (B < 0 || Tq < 0 || N < 0 || H <= 0 || c <= 0 || m <= 0) return CSA_ERR_INVALID_ARG;
   if (B == 0 || Tq == 0 || N == 0) return CSA_OK;
   if (!qI || !w || !K || !scores) return CSA_ERR_INVALID_ARG;
+  if (q_pos && !aligned(q_pos, 4)) return CSA_ERR_INVALID_ARG;
   if (dtype == CSA_DT_F32) {
     if (c > 256) return CSA_ERR_UNSUPPORTED;
     csa::IndexF32Args a{reinterpret_cast<const float*>(qI), w, reinterpret_cast<const float*>(K),
-                        scores, Tq, N, H, c, m, q_pos0};
+                        scores, q_pos, Tq, N, H, c, m};
     dim3 grid((N + 7) / 8, B * Tq);
     cudaError_t e = launch_ex(csa::index_f32_kernel, grid, dim3(256), 0, S(stream), 1, a);
     if (e != cudaSuccess) return cuda_fail(e, "csa_index f32 launch");
@@ -514,13 +515,13 @@ static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w
     if (!aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4) || !aligned(scores, 4))
       return CSA_ERR_INVALID_ARG;
     if (H == 64 && c == 128)
-      return launch_index_tc<64, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, hist, S(stream));
+      return launch_index_tc<64, 128>(qI, w, K, q_pos, scores, B, Tq, N, m, hist, S(stream));
     if (H == 64 && c == 64)
-      return launch_index_tc<64, 64>(qI, w, K, scores, B, Tq, N, m, q_pos0, hist, S(stream));
+      return launch_index_tc<64, 64>(qI, w, K, q_pos, scores, B, Tq, N, m, hist, S(stream));
     if (H == 32 && c == 128)
-      return launch_index_tc<32, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, hist, S(stream));
+      return launch_index_tc<32, 128>(qI, w, K, q_pos, scores, B, Tq, N, m, hist, S(stream));
     if (H == 128 && c == 128)
-      return launch_index_tc<128, 128>(qI, w, K, scores, B, Tq, N, m, q_pos0, hist, S(stream));
+      return launch_index_tc<128, 128>(qI, w, K, q_pos, scores, B, Tq, N, m, hist, S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
   if (dtype == CSA_DT_E2M1_BLOCK16) {
@@ -530,20 +531,20 @@ static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w
       return CSA_ERR_INVALID_ARG;
     if (c != csa::FP4_C) return CSA_ERR_UNSUPPORTED;
     if (H == 64)
-      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, hist, S(stream));
+      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, m, hist, S(stream));
     if (H == 32)
-      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, hist, S(stream));
+      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, m, hist, S(stream));
     if (H == 128)
-      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, m, q_pos0, hist, S(stream));
+      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, m, hist, S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
   return CSA_ERR_UNSUPPORTED;
 }
 
 csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
-                       const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
-                       int m, int q_pos0, int dtype, void* stream) {
-  return index_impl(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, H, c, m, q_pos0, dtype, nullptr, stream);
+                       const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
+                       int N, int H, int c, int m, int dtype, void* stream) {
+  return index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, H, c, m, dtype, nullptr, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -558,14 +559,14 @@ size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype) {
 }
 
 csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, const void* K,
-                            const void* K_sf, float* scores, int32_t* idx, int B, int Tq, int N,
-                            int H, int c, int m, int q_pos0, int k, int dtype, void* ws,
+                            const void* K_sf, const int32_t* q_pos, float* scores, int32_t* idx,
+                            int B, int Tq, int N, int H, int c, int m, int k, int dtype, void* ws,
                             size_t ws_bytes, void* stream) {
   if (k < 1 || k > 4096) return CSA_ERR_INVALID_ARG;
   if (!index_topk_fused(B, Tq, N, dtype)) {
-    csa_status_t st = csa_index(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, H, c, m, q_pos0, dtype, stream);
+    csa_status_t st = csa_index(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, H, c, m, dtype, stream);
     if (st != CSA_OK) return st;
-    return csa_topk(scores, idx, B, Tq, N, k, m, q_pos0, stream);
+    return csa_topk(scores, q_pos, idx, B, Tq, N, k, m, stream);
   }
   if (!idx || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
   const size_t need = csa_index_topk_workspace_size(B, Tq, N, dtype);
@@ -573,25 +574,26 @@ csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, c
   // the histograms start zero (caller's first use) and the selector clears each
   // row's after reading it, so no clearing pass runs here
   uint32_t* hist = reinterpret_cast<uint32_t*>(ws);
-  csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, scores, B, Tq, N, H, c, m, q_pos0, dtype, hist, stream);
+  csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, H, c, m, dtype, hist,
+                               stream);
   if (st != CSA_OK) return st;
-  return launch_topk2(scores, idx, B * Tq, Tq, N, k, m, q_pos0, hist, S(stream));
+  return launch_topk2(scores, q_pos, idx, B * Tq, Tq, N, k, m, hist, S(stream));
 }
 
 // ---------------------------------------------------------------------------
-csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, int k, int m,
-                      int q_pos0, void* stream) {
-  if (B < 0 || Tq < 0 || N < 0 || k < 1 || k > 4096 || m <= 0 || q_pos0 < 0)
-    return CSA_ERR_INVALID_ARG;
+csa_status_t csa_topk(const float* scores, const int32_t* q_pos, int32_t* idx, int B, int Tq,
+                      int N, int k, int m, void* stream) {
+  if (B < 0 || Tq < 0 || N < 0 || k < 1 || k > 4096 || m <= 0) return CSA_ERR_INVALID_ARG;
   if (B == 0 || Tq == 0) return CSA_OK;
   if (!idx || (N > 0 && !scores)) return CSA_ERR_INVALID_ARG;
-  if (!aligned(scores, 4) || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
+  if (!aligned(scores, 4) || !aligned(idx, 4) || (q_pos && !aligned(q_pos, 4)))
+    return CSA_ERR_INVALID_ARG;
   const int rows = B * Tq;
   // few long decode rows up to 32768 entries: 8-bit radix passes over a 16-CTA
   // cluster; everything else up to 16 x 32768 entries: the candidate-filtering
   // selector (measured faster there: many short rows, and rows past 32768)
   if (!(N > 8192 && N <= 32768 && rows < 64) && N <= 16 * 32768)
-    return launch_topk2(scores, idx, rows, Tq, N, k, m, q_pos0, nullptr, S(stream));
+    return launch_topk2(scores, q_pos, idx, rows, Tq, N, k, m, nullptr, S(stream));
   // rows longer than 16 slices of 32768 keys: 8-bit radix passes over up to 16 SMs
   int CL = 1;
   if (N > 8192 && rows < 64) CL = rows <= 9 ? 16 : 8;
@@ -599,7 +601,7 @@ csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, i
   slice = (slice + 3) & ~3;
   const size_t smem = (size_t)slice * sizeof(uint32_t);
   if (smem > 200 * 1024) return CSA_ERR_UNSUPPORTED;
-  csa::TopkArgs a{scores, idx, Tq, N, k, m, q_pos0, slice};
+  csa::TopkArgs a{scores, idx, q_pos, Tq, N, k, m, slice};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows * CL);
   cfg.blockDim = dim3(csa::TOPK_THREADS);
@@ -638,101 +640,136 @@ csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, i
   return CSA_OK;
 }
 
+}  // extern "C"
+
 // ---------------------------------------------------------------------------
-static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* idx, csa_kv_t win,
-                                  const float* sink, void* out, int B, int Tq, int N, int k,
-                                  int T_win, int win_base, int n_h, int d, int r, int m, int n_win,
-                                  int q_pos0, float rope_base, void* ws, size_t ws_bytes,
-                                  void* stream, int dense) {
-  if (B < 0 || Tq < 0 || N < 0 || T_win < 0 || n_h <= 0 || d <= 0 || r < 0 || r > d || (r & 1) ||
-      r > 128 || m <= 0 || n_win <= 0 || q_pos0 < 0 || win_base < 0 || !(rope_base > 0.f))
+// csa_attend / hca_attend: arguments, host-side checks, plan and launches.
+namespace {
+
+struct AttendCall {
+  const void* q;
+  csa_kv_t ent, win;
+  const int32_t* idx;
+  const int32_t* q_pos;
+  const int32_t* win_base;
+  const float* sink;
+  void* out;
+  int B, Tq, N, k, T_win, n_h, d, r, m, n_win;
+  float rope_base;
+  int dense;
+};
+
+// Every host-side check of an attention call (sizes, null and misaligned
+// pointers, supported shapes).  Returns CSA_OK with *plan set for a launch, or
+// CSA_OK with *empty = true when there is nothing to do.
+csa_status_t attend_validate(const AttendCall& c, AttPlan* plan, bool* empty) {
+  *empty = false;
+  if (c.B < 0 || c.Tq < 0 || c.N < 0 || c.T_win < 0 || c.n_h <= 0 || c.d <= 0 || c.r < 0 ||
+      c.r > c.d || (c.r & 1) || c.r > 128 || c.m <= 0 || c.n_win <= 0 || !(c.rope_base > 0.f))
     return CSA_ERR_INVALID_ARG;
-  if (!dense && (k < 1 || k > 4096)) return CSA_ERR_INVALID_ARG;
-  if (N > 0 && !ent.data) return CSA_ERR_INVALID_ARG;
-  if (B == 0 || Tq == 0) return CSA_OK;
-  if (!q || !sink || !out || !win.data) return CSA_ERR_INVALID_ARG;
-  if (!dense && !idx) return CSA_ERR_INVALID_ARG;
-  // every window position of every query row must lie in the window buffer
-  const long long t_first = q_pos0, t_last = (long long)q_pos0 + Tq - 1;
-  const long long w_lo = t_first - n_win + 1 < 0 ? 0 : t_first - n_win + 1;
-  if (w_lo < win_base || t_last >= (long long)win_base + T_win) return CSA_ERR_INVALID_ARG;
-  (void)ws; (void)ws_bytes;
-  const RopeFreqs rf = make_rope(r, rope_base);
-  // q dtype is implied by the kv dtype for the tensor-core path; float32 here
-  if (ent.dtype == CSA_DT_F32 && win.dtype == CSA_DT_F32) {
-    if (d > 512 || (size_t)n_h * d > 16384) return CSA_ERR_UNSUPPORTED;
+  if (!c.dense && (c.k < 1 || c.k > 4096)) return CSA_ERR_INVALID_ARG;
+  if (c.N > 0 && !c.ent.data) return CSA_ERR_INVALID_ARG;
+  if (c.B == 0 || c.Tq == 0) {
+    *empty = true;
+    return CSA_OK;
+  }
+  if (!c.q || !c.sink || !c.out || (c.T_win > 0 && !c.win.data)) return CSA_ERR_INVALID_ARG;
+  if (!c.dense && !c.idx) return CSA_ERR_INVALID_ARG;
+  if ((c.q_pos && !aligned(c.q_pos, 4)) || (c.win_base && !aligned(c.win_base, 4)) ||
+      (c.idx && !aligned(c.idx, 4)))
+    return CSA_ERR_INVALID_ARG;
+  if (c.ent.dtype == CSA_DT_F32 && c.win.dtype == CSA_DT_F32) {
+    if (c.d > 512 || (size_t)c.n_h * c.d > 16384) return CSA_ERR_UNSUPPORTED;
+    memset(plan, 0, sizeof(*plan));
+    return CSA_OK;
+  }
+  if (!tc_attend_shape(c.n_h, c.d, c.r, c.ent.dtype) || c.ent.dtype != c.win.dtype)
+    return CSA_ERR_UNSUPPORTED;
+  const int mixed = c.ent.dtype == CSA_DT_E4M3_BF16ROPE;
+  if (!aligned(c.q, 16) || !aligned(c.out, 16) || (c.T_win > 0 && !aligned(c.win.data, 16)) ||
+      (c.N > 0 && !aligned(c.ent.data, 16)))
+    return CSA_ERR_INVALID_ARG;
+  if (mixed && ((c.T_win > 0 && (!c.win.scale || !c.win.rope || !aligned(c.win.rope, 16))) ||
+                (c.N > 0 && (!c.ent.scale || !c.ent.rope || !aligned(c.ent.rope, 16)))))
+    return CSA_ERR_INVALID_ARG;
+  if ((long long)c.B * c.N >= 0x7fffffffLL || (long long)c.B * c.T_win >= 0x7fffffffLL ||
+      (long long)c.B * c.Tq * c.n_h >= 0x7fffffffLL)
+    return CSA_ERR_UNSUPPORTED;
+  *plan = plan_attend(c.B, c.Tq, c.N, c.dense ? 0 : c.k, c.T_win, c.n_h, c.n_win, c.dense, mixed);
+  return CSA_OK;
+}
+
+// The launches of a validated call; ws holds at least plan.bytes (256-byte aligned).
+csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void* stream) {
+  const RopeFreqs rf = make_rope(c.r, c.rope_base);
+  cudaStream_t st = S(stream);
+  if (c.ent.dtype == CSA_DT_F32 && c.win.dtype == CSA_DT_F32) {
     csa::AttendF32Args a;
-    a.q = reinterpret_cast<const float*>(q);
-    a.ent = reinterpret_cast<const float*>(ent.data);
-    a.idx = dense ? nullptr : idx;
-    a.win = reinterpret_cast<const float*>(win.data);
-    a.sink = sink;
-    a.out = reinterpret_cast<float*>(out);
-    a.Tq = Tq; a.N = N; a.k = dense ? 0 : k; a.T_win = T_win; a.win_base = win_base;
-    a.n_h = n_h; a.d = d; a.r = r; a.m = m; a.n_win = n_win; a.q_pos0 = q_pos0;
-    a.dense = dense;
-    a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+    memset(&a, 0, sizeof(a));
+    a.q = reinterpret_cast<const float*>(c.q);
+    a.ent = reinterpret_cast<const float*>(c.ent.data);
+    a.idx = c.dense ? nullptr : c.idx;
+    a.win = reinterpret_cast<const float*>(c.win.data);
+    a.sink = c.sink;
+    a.out = reinterpret_cast<float*>(c.out);
+    a.q_pos = c.q_pos; a.win_base = c.win_base;
+    a.Tq = c.Tq; a.N = c.N; a.k = c.dense ? 0 : c.k; a.T_win = c.T_win;
+    a.n_h = c.n_h; a.d = c.d; a.r = c.r; a.m = c.m; a.n_win = c.n_win;
+    a.dense = c.dense;
+    a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
     a.rf = rf;
-    const size_t smem = ((size_t)2 * n_h * d + d + 5 * n_h) * sizeof(float);
+    const size_t smem = ((size_t)2 * c.n_h * c.d + c.d + 5 * c.n_h) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(csa::attend_f32_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "csa_attend f32 attr");
-    e = launch_ex(csa::attend_f32_kernel, dim3(B * Tq), dim3(csa::ATT_F32_THREADS), smem, S(stream), 1, a);
+    e = launch_ex(csa::attend_f32_kernel, dim3(c.B * c.Tq), dim3(csa::ATT_F32_THREADS), smem, st, 1, a);
     if (e != cudaSuccess) return cuda_fail(e, "csa_attend f32 launch");
     return CSA_OK;
   }
-  if (!tc_attend_shape(n_h, d, r, ent.dtype) || ent.dtype != win.dtype) return CSA_ERR_UNSUPPORTED;
-  const int mixed = ent.dtype == CSA_DT_E4M3_BF16ROPE;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(win.data, 16) || (N > 0 && !aligned(ent.data, 16)))
-    return CSA_ERR_INVALID_ARG;
-  if (mixed && (!win.scale || !win.rope || !aligned(win.rope, 16) ||
-                (N > 0 && (!ent.scale || !ent.rope || !aligned(ent.rope, 16)))))
-    return CSA_ERR_INVALID_ARG;
-  const AttPlan p = plan_attend(B, Tq, N, k, T_win, n_h, m, n_win, q_pos0, dense, mixed);
-  if (p.bytes > 0 && (!ws || ws_bytes < p.bytes || !aligned(ws, 256))) return CSA_ERR_WORKSPACE;
+  const int mixed = c.ent.dtype == CSA_DT_E4M3_BF16ROPE;
   uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
   csa::AttendTcArgs a;
   memset(&a, 0, sizeof(a));
-  a.q = reinterpret_cast<const __nv_bfloat16*>(q);
-  a.ent = ent.data; a.ent_scale = ent.scale;
-  a.ent_rope = reinterpret_cast<const __nv_bfloat16*>(ent.rope);
-  a.win = win.data; a.win_scale = win.scale;
-  a.win_rope = reinterpret_cast<const __nv_bfloat16*>(win.rope);
-  a.idx = dense ? nullptr : idx;
-  a.sink = sink;
-  a.out = reinterpret_cast<__nv_bfloat16*>(out);
-  a.B = B; a.Tq = Tq; a.N = N; a.k = dense ? 0 : k; a.T_win = T_win; a.win_base = win_base;
-  a.n_h = n_h; a.m = m; a.n_win = n_win; a.q_pos0 = q_pos0;
+  a.q = reinterpret_cast<const __nv_bfloat16*>(c.q);
+  a.ent = c.ent.data; a.ent_scale = c.ent.scale;
+  a.ent_rope = reinterpret_cast<const __nv_bfloat16*>(c.ent.rope);
+  a.win = c.win.data; a.win_scale = c.win.scale;
+  a.win_rope = reinterpret_cast<const __nv_bfloat16*>(c.win.rope);
+  a.idx = c.dense ? nullptr : c.idx;
+  a.q_pos = c.q_pos; a.win_base = c.win_base;
+  a.sink = c.sink;
+  a.out = reinterpret_cast<__nv_bfloat16*>(c.out);
+  a.B = c.B; a.Tq = c.Tq; a.N = c.N; a.k = c.dense ? 0 : c.k; a.T_win = c.T_win;
+  a.n_h = c.n_h; a.m = c.m; a.n_win = c.n_win;
   a.HG = p.HG; a.nch = p.nch; a.chunk_rows = p.chunk_rows; a.items = p.items;
   a.rotate_rows = p.rotate_rows; a.kv_mixed = mixed;
   a.cl_reduce = p.cl_reduce;
   a.rel_rope = p.rel_rope;
-  if ((long long)B * N >= 0x7fffffffLL || (long long)B * T_win >= 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
-  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.d));
   a.rf = rf;
-  cudaStream_t st = S(stream);
   if (!p.rotate_rows) {
     // rotate the RoPE dims of every stored row once
     csa::RotateArgs ra;
+    memset(&ra, 0, sizeof(ra));
     ra.rf = rf;
-    if (N > 0) {
-      ra.src = reinterpret_cast<const __nv_bfloat16*>(ent.data);
+    if (c.N > 0) {
+      ra.src = reinterpret_cast<const __nv_bfloat16*>(c.ent.data);
       ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_ent);
-      ra.rows = (long long)B * N; ra.rows_per_b = N; ra.m = m; ra.base = 0;
+      ra.rows = (long long)c.B * c.N; ra.rows_per_b = c.N; ra.m = c.m; ra.base = nullptr;
       cudaError_t e = launch_ex(csa::rope_rotate_rows_kernel, dim3((unsigned)((ra.rows * 64 + 255) / 256)),
                                 dim3(256), 0, st, 1, ra);
       if (e != cudaSuccess) return cuda_fail(e, "csa_attend rotate entries");
       a.ent = ra.dst;
     }
-    ra.src = reinterpret_cast<const __nv_bfloat16*>(win.data);
-    ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_win);
-    ra.rows = (long long)B * T_win; ra.rows_per_b = T_win; ra.m = 0; ra.base = win_base;
-    {
+    if (c.T_win > 0) {
+      ra.src = reinterpret_cast<const __nv_bfloat16*>(c.win.data);
+      ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_win);
+      ra.rows = (long long)c.B * c.T_win; ra.rows_per_b = c.T_win; ra.m = 0; ra.base = c.win_base;
       cudaError_t e = launch_ex(csa::rope_rotate_rows_kernel, dim3((unsigned)((ra.rows * 64 + 255) / 256)),
                                 dim3(256), 0, st, 1, ra);
       if (e != cudaSuccess) return cuda_fail(e, "csa_attend rotate window");
+      a.win = ra.dst;
     }
-    a.win = ra.dst;
   }
   if (p.nch > 1 && !p.cl_reduce) {
     a.part_o = reinterpret_cast<float*>(wsb + p.off_part_o);
@@ -740,8 +777,8 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
   }
   CUtensorMap tmq;
   memset(&tmq, 0, sizeof(tmq));
-  if (!tmap_bf16_3d(&tmq, q, csa::ATT_D, (uint64_t)B * Tq * n_h, 1, (uint64_t)csa::ATT_D * 2,
-                    (uint64_t)B * Tq * n_h * csa::ATT_D * 2, 64, csa::ATT_HG))
+  if (!tmap_bf16_3d(&tmq, c.q, csa::ATT_D, (uint64_t)c.B * c.Tq * c.n_h, 1, (uint64_t)csa::ATT_D * 2,
+                    (uint64_t)c.B * c.Tq * c.n_h * csa::ATT_D * 2, 64, csa::ATT_HG))
     return CSA_ERR_UNSUPPORTED;
   const int smem = csa::AttSmem::BYTES;
   cudaError_t e = cudaFuncSetAttribute(csa::attend_tc_kernel,
@@ -758,8 +795,10 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc launch");
   if (p.nch > 1 && !p.cl_reduce) {
     csa::CombineArgs ca;
-    ca.part_o = a.part_o; ca.part_ml = a.part_ml; ca.sink = sink; ca.out = a.out;
-    ca.Tq = Tq; ca.n_h = n_h; ca.HG = p.HG; ca.nch = p.nch; ca.q_pos0 = q_pos0; ca.rf = rf;
+    memset(&ca, 0, sizeof(ca));
+    ca.part_o = a.part_o; ca.part_ml = a.part_ml; ca.sink = c.sink; ca.out = a.out;
+    ca.q_pos = c.q_pos;
+    ca.Tq = c.Tq; ca.n_h = c.n_h; ca.HG = p.HG; ca.nch = p.nch; ca.rf = rf;
     ca.rel_rope = p.rel_rope;
     const size_t cmb_smem = (size_t)p.nch * csa::ATT_HG * 2 * sizeof(float);
     if (cmb_smem > 48 * 1024) {
@@ -768,36 +807,51 @@ static csa_status_t attend_common(const void* q, csa_kv_t ent, const int32_t* id
       if (e != cudaSuccess) return cuda_fail(e, "csa_attend combine attr");
     }
     e = launch_ex(csa::attend_combine_kernel,
-                  dim3((unsigned)((size_t)B * Tq * p.HG * (csa::ATT_D / csa::CMB_DIMS))),
+                  dim3((unsigned)((size_t)c.B * c.Tq * p.HG * (csa::ATT_D / csa::CMB_DIMS))),
                   dim3(csa::CMB_THREADS), cmb_smem, st, 1, ca);
     if (e != cudaSuccess) return cuda_fail(e, "csa_attend combine launch");
   }
   return CSA_OK;
 }
 
-csa_status_t csa_attend(const void* q, csa_kv_t entries, const int32_t* idx, csa_kv_t win,
-                        const float* sink, void* out, int B, int Tq, int N, int k, int T_win,
-                        int win_base, int n_h, int d, int r, int m, int n_win, int q_pos0,
-                        float rope_base, void* ws, size_t ws_bytes, void* stream) {
-  return attend_common(q, entries, idx, win, sink, out, B, Tq, N, k, T_win, win_base, n_h, d, r,
-                       m, n_win, q_pos0, rope_base, ws, ws_bytes, stream, 0);
+csa_status_t attend_with_workspace(const AttendCall& c, void* ws, size_t ws_bytes, void* stream) {
+  AttPlan p;
+  bool empty = false;
+  csa_status_t st = attend_validate(c, &p, &empty);
+  if (st != CSA_OK || empty) return st;
+  if (p.bytes > 0 && (!ws || ws_bytes < p.bytes || !aligned(ws, 256))) return CSA_ERR_WORKSPACE;
+  return attend_launch(c, p, ws, stream);
 }
 
-csa_status_t hca_attend(const void* q, csa_kv_t entries, csa_kv_t win, const float* sink,
-                        void* out, int B, int Tq, int N, int T_win, int win_base, int n_h, int d,
-                        int r, int m, int n_win, int q_pos0, float rope_base, void* ws,
-                        size_t ws_bytes, void* stream) {
-  return attend_common(q, entries, nullptr, win, sink, out, B, Tq, N, 0, T_win, win_base, n_h, d,
-                       r, m, n_win, q_pos0, rope_base, ws, ws_bytes, stream, 1);
+}  // namespace
+
+extern "C" {
+
+csa_status_t csa_attend(const void* q, csa_kv_t entries, const int32_t* idx, csa_kv_t win,
+                        const int32_t* q_pos, const int32_t* win_base, const float* sink,
+                        void* out, int B, int Tq, int N, int k, int T_win, int n_h, int d, int r,
+                        int m, int n_win, float rope_base, void* ws, size_t ws_bytes,
+                        void* stream) {
+  const AttendCall c{q, entries, win, idx, q_pos, win_base, sink, out, B, Tq, N, k, T_win,
+                     n_h, d, r, m, n_win, rope_base, 0};
+  return attend_with_workspace(c, ws, ws_bytes, stream);
+}
+
+csa_status_t hca_attend(const void* q, csa_kv_t entries, csa_kv_t win, const int32_t* q_pos,
+                        const int32_t* win_base, const float* sink, void* out, int B, int Tq,
+                        int N, int T_win, int n_h, int d, int r, int m, int n_win,
+                        float rope_base, void* ws, size_t ws_bytes, void* stream) {
+  const AttendCall c{q, entries, win, nullptr, q_pos, win_base, sink, out, B, Tq, N, 0, T_win,
+                     n_h, d, r, m, n_win, rope_base, 1};
+  return attend_with_workspace(c, ws, ws_bytes, stream);
 }
 
 size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h, int d, int r,
-                                 int m, int n_win, int q_pos0, int q_dtype, int kv_dtype,
-                                 int is_hca) {
+                                 int m, int n_win, int q_dtype, int kv_dtype, int is_hca) {
   (void)q_dtype;
-  if (B <= 0 || Tq <= 0 || n_h <= 0 || m <= 0 || N < 0) return 0;
+  if (B <= 0 || Tq <= 0 || n_h <= 0 || m <= 0 || N < 0 || T_win < 0 || n_win <= 0) return 0;
   if (!tc_attend_shape(n_h, d, r, kv_dtype)) return 0;
-  return plan_attend(B, Tq, N, is_hca ? 0 : k, T_win, n_h, m, n_win, q_pos0, is_hca ? 1 : 0,
+  return plan_attend(B, Tq, N, is_hca ? 0 : k, T_win, n_h, n_win, is_hca ? 1 : 0,
                      kv_dtype == CSA_DT_E4M3_BF16ROPE ? 1 : 0).bytes;
 }
 
@@ -811,50 +865,92 @@ static __device__ __align__(256) unsigned char g_attend_noalloc_scratch[CSA_NOAL
 
 namespace {
 
-constexpr int kNoallocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+typedef CUresult (*PFN_ctx_get_current)(CUcontext*);
+typedef CUresult (*PFN_ctx_get_id)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device.  The array's
-// name in host code is only a host-side handle, so the address is looked up
-// once per device (with that device current) and cached.
-csa_status_t noalloc_scratch(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "csa_attend_noalloc get device");
-  if (dev < 0 || dev >= kNoallocMaxDevices) return CSA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+// Unique id of the calling thread's current CUDA context (driver calls reached
+// through the runtime's entry-point query, so the library needs no -lcuda).
+// Ids are never reused within a process, unlike context handles, so a context
+// made after cudaDeviceReset never matches an address cached for the old one.
+bool current_context_id(unsigned long long* id) {
+  static PFN_ctx_get_current get_cur = nullptr;
+  static PFN_ctx_get_id get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_attend_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "csa_attend_noalloc scratch address");
-    g_noalloc_ptr[dev] = p;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_ctx_get_current>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_ctx_get_id>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+constexpr int kNoallocCacheSlots = 64;
+std::mutex g_noalloc_mu;
+unsigned long long g_noalloc_ctx[kNoallocCacheSlots] = {};
+void* g_noalloc_ptr[kNoallocCacheSlots] = {};
+int g_noalloc_next = 0;
+
+// Device address of the scratch array in the calling thread's current context.
+// The array's name in host code is only a host-side handle, and each context
+// that loads this library has its own copy at its own address, so the address
+// is looked up (cudaGetSymbolAddress) once per context and cached under the
+// context's unique id.
+csa_status_t noalloc_scratch(void** out) {
+  unsigned long long id = 0;
+  if (current_context_id(&id)) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    for (int i = 0; i < kNoallocCacheSlots; ++i)
+      if (g_noalloc_ptr[i] && g_noalloc_ctx[i] == id) {
+        *out = g_noalloc_ptr[i];
+        return CSA_OK;
+      }
   }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_attend_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_attend_noalloc scratch address");
+  // the lookup made the device's context current if none was: cache under its id
+  if (current_context_id(&id)) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    g_noalloc_ctx[g_noalloc_next] = id;
+    g_noalloc_ptr[g_noalloc_next] = p;
+    g_noalloc_next = (g_noalloc_next + 1) % kNoallocCacheSlots;
+  }
+  *out = p;
   return CSA_OK;
 }
 
 }  // namespace
 
 extern "C" csa_status_t csa_attend_noalloc(const void* q, csa_kv_t entries, const int32_t* idx,
-                                           csa_kv_t win, const float* sink, void* out, int B,
-                                           int Tq, int N, int k, int T_win, int win_base, int n_h,
-                                           int d, int r, int m, int n_win, int q_pos0,
-                                           float rope_base, void* stream) {
-  const size_t need = csa_attend_workspace_size(B, Tq, N, k, T_win, n_h, d, r, m, n_win, q_pos0,
-                                                CSA_DT_BF16, entries.dtype, 0);
-  if (need > CSA_NOALLOC_SCRATCH_BYTES) {
+                                           csa_kv_t win, const int32_t* q_pos,
+                                           const int32_t* win_base, const float* sink, void* out,
+                                           int B, int Tq, int N, int k, int T_win, int n_h, int d,
+                                           int r, int m, int n_win, float rope_base,
+                                           void* stream) {
+  const AttendCall c{q, entries, win, idx, q_pos, win_base, sink, out, B, Tq, N, k, T_win,
+                     n_h, d, r, m, n_win, rope_base, 0};
+  AttPlan p;
+  bool empty = false;
+  csa_status_t st = attend_validate(c, &p, &empty);   // argument errors come first
+  if (st != CSA_OK || empty) return st;
+  if (p.bytes > CSA_NOALLOC_SCRATCH_BYTES) {
     snprintf(g_cuda_msg, sizeof(g_cuda_msg),
-             "csa_attend_noalloc: these sizes need %zu scratch bytes, above the fixed %zu", need,
+             "csa_attend_noalloc: these sizes need %zu scratch bytes, above the fixed %zu", p.bytes,
              (size_t)CSA_NOALLOC_SCRATCH_BYTES);
     return CSA_ERR_WORKSPACE;
   }
   void* ws = nullptr;
-  if (need > 0) {
-    const csa_status_t s = noalloc_scratch(&ws);
-    if (s != CSA_OK) return s;
+  if (p.bytes > 0) {
+    st = noalloc_scratch(&ws);
+    if (st != CSA_OK) return st;
   }
-  return attend_common(q, entries, idx, win, sink, out, B, Tq, N, k, T_win, win_base, n_h, d, r,
-                       m, n_win, q_pos0, rope_base, ws, need > 0 ? (size_t)CSA_NOALLOC_SCRATCH_BYTES : 0,
-                       stream, 0);
+  return attend_launch(c, p, ws, stream);
 }

@@ -342,6 +342,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
     for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
       const IdxItem x = idx_item(a, it);
       float* ws = w_s + ((ew * 2) + (nitem & 1)) * 256;
+      if (ew == 0 && lane == 0 && x.j0 == 0) check_item_pos(a, x);
       for (int e = lane; e < x.nq * H; e += 32)
         ws[e] = __ldg(a.w + ((size_t)x.b * a.Tq + x.t0) * H + e);
       __syncwarp();
@@ -359,7 +360,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
           for (int qi = 0; qi < x.nq; ++qi) {
             const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
-            const int vis = vis32(a.q_pos0 + x.t0 + qi, a.m, a.N);
+            const int vis = item_vis(a, x, qi);
             if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
             if (a.hist) hist_add(wh, acc, s < vis);
           }

@@ -32,7 +32,8 @@ constexpr int IDX_TILE = 128;   // entries per tile (MMA M)
 struct IndexTcArgs {
   const float* w;        // [B, Tq, H]
   float* scores;         // [B, Tq, N]
-  int B, Tq, N, m, q_pos0;
+  const int32_t* q_pos;  // [B, Tq] query positions (null: t = i)
+  int B, Tq, N, m;
   int QT;                // queries per group (QT * H <= 256)
   int G;                 // query groups per batch row
   int tiles_max;         // ceil(N / 128)
@@ -93,8 +94,8 @@ struct IndexSmem {
 };
 
 CSA_DEVINL int vis_of(long long t, int m, int N) {
+  if (t < 0) return 0;
   long long v = (t + 1) / m;
-  if (v < 0) v = 0;
   return (int)(v < N ? v : N);
 }
 
@@ -125,15 +126,21 @@ CSA_DEVINL float fold_heads(uint32_t taddr, const float* wq) {
   return (p0 + p1) + (p2 + p3);
 }
 
-// visible entries of the query at position t (32-bit: positions < 2^31)
-CSA_DEVINL int vis32(int t, int m, int N) {
-  const int v = (t + 1) / m;
-  return v < N ? (v < 0 ? 0 : v) : N;
-}
-
 struct IdxItem {
   int b, g, t0, nq, j0, j1, jv;   // tiles [j0, j1) of the chunk; MMA for j < jv
 };
+
+// visible entries of query row t0 + qi of item x (a negative position sees nothing)
+CSA_DEVINL int item_vis(const IndexTcArgs& a, const IdxItem& x, int qi) {
+  const long long t = query_pos(a.q_pos, (long long)x.b * a.Tq + x.t0 + qi, x.t0 + qi);
+  return vis_of(t, a.m, a.N);
+}
+// Flags a negative query position of item x (called by one lane per item).
+CSA_DEVINL void check_item_pos(const IndexTcArgs& a, const IdxItem& x) {
+  for (int qi = 0; qi < x.nq; ++qi)
+    if (query_pos(a.q_pos, (long long)x.b * a.Tq + x.t0 + qi, x.t0 + qi) < 0)
+      csa_flag_error(ERRBIT_BAD_INDEX);
+}
 
 CSA_DEVINL IdxItem idx_item(const IndexTcArgs& a, int it) {
   IdxItem x;
@@ -143,8 +150,9 @@ CSA_DEVINL IdxItem idx_item(const IndexTcArgs& a, int it) {
   const int c = rem % a.chunks;
   x.t0 = x.g * a.QT;
   x.nq = min(a.QT, a.Tq - x.t0);
-  const int vis_last = vis_of((long long)a.q_pos0 + x.t0 + x.nq - 1, a.m, a.N);
-  const int tiles_vis = (vis_last + IDX_TILE - 1) / IDX_TILE;
+  int vis_max = 0;                               // the group's widest query decides the MMA tiles
+  for (int qi = 0; qi < x.nq; ++qi) vis_max = max(vis_max, item_vis(a, x, qi));
+  const int tiles_vis = (vis_max + IDX_TILE - 1) / IDX_TILE;
   x.j0 = c * a.chunk_tiles;
   x.j1 = min(a.tiles_max, x.j0 + a.chunk_tiles);
   x.jv = max(x.j0, min(x.j1, tiles_vis));
@@ -290,6 +298,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
       // this warp's own copy of the group's head weights (no cross-warp barrier,
       // so a warp that stops on a timed-out wait cannot strand the others)
       float* ws = w_s + ew * 256;
+      if (ew == 0 && lane == 0 && x.j0 == 0) check_item_pos(a, x);
       __syncwarp();                                // the previous item's reads are done
       for (int e = lane; e < x.nq * H; e += 32)
         ws[e] = __ldg(a.w + ((size_t)x.b * a.Tq + x.t0) * H + e);
@@ -307,7 +316,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
           for (int qi = 0; qi < x.nq; ++qi) {
             const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
-            const int vis = vis32(a.q_pos0 + x.t0 + qi, a.m, a.N);
+            const int vis = item_vis(a, x, qi);
             if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
             if (a.hist) hist_add(wh, acc, s < vis);
           }

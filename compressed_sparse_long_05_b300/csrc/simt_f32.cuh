@@ -15,7 +15,8 @@ namespace csa {
 // ----------------------------------------------------------------------------
 struct IndexF32Args {
   const float* q; const float* w; const float* K; float* scores;
-  int Tq, N, H, c, m, q_pos0;
+  const int32_t* q_pos;            // [B, Tq] (null: t = i)
+  int Tq, N, H, c, m;
 };
 
 __global__ void __launch_bounds__(256) index_f32_kernel(IndexF32Args a) {
@@ -26,9 +27,10 @@ __global__ void __launch_bounds__(256) index_f32_kernel(IndexF32Args a) {
   if (gw >= a.N) return;
   const int s = (int)gw;
   const int b = row / a.Tq, i = row % a.Tq;
-  const long long t = (long long)a.q_pos0 + i;
+  const long long t = query_pos(a.q_pos, row, i);
+  if (t < 0 && s == 0 && lane == 0) csa_flag_error(ERRBIT_BAD_INDEX);
   float* out = a.scores + (size_t)row * a.N + s;
-  if ((long long)(s + 1) * a.m > t + 1) {          // not visible
+  if (t < 0 || (long long)(s + 1) * a.m > t + 1) {   // not visible
     if (lane == 0) *out = -INFINITY;
     return;
   }
@@ -53,7 +55,9 @@ __global__ void __launch_bounds__(256) index_f32_kernel(IndexF32Args a) {
 struct AttendF32Args {
   const float* q; const float* ent; const int32_t* idx; const float* win; const float* sink;
   float* out;
-  int Tq, N, k, T_win, win_base, n_h, d, r, m, n_win, q_pos0;
+  const int32_t* q_pos;            // [B, Tq] (null: t = i)
+  const int32_t* win_base;         // [B] (null: 0)
+  int Tq, N, k, T_win, n_h, d, r, m, n_win;
   int dense;        // 1 = HCA: every visible entry, idx unused
   float inv_sqrt_d;
   RopeFreqs rf;
@@ -66,7 +70,8 @@ __global__ void __launch_bounds__(ATT_F32_THREADS) attend_f32_kernel(AttendF32Ar
   extern __shared__ float sm[];
   const int row = blockIdx.x;                    // b * Tq + i
   const int b = row / a.Tq, i = row % a.Tq;
-  const long long t = (long long)a.q_pos0 + i;
+  const long long t = query_pos(a.q_pos, row, i);
+  const long long wbase = window_base(a.win_base, b);
   const int nh = a.n_h, d = a.d, r = a.r;
   float* qs = sm;                                // [n_h][d] rotated queries
   float* acc = qs + (size_t)nh * d;              // [n_h][d]
@@ -101,11 +106,11 @@ __global__ void __launch_bounds__(ATT_F32_THREADS) attend_f32_kernel(AttendF32Ar
   // row list: [0, nsel) compressed entries, then the window tokens
   int nsel;
   const int32_t* irow = a.idx ? a.idx + (size_t)row * a.k : nullptr;
-  int vis = (int)min((long long)a.N, (t + 1) / a.m);
-  if (vis < 0) vis = 0;
-  nsel = a.dense ? vis : a.k;
+  int vis = t < 0 ? 0 : (int)min((long long)a.N, (t + 1) / a.m);
+  if (t < 0 && tid == 0) csa_flag_error(ERRBIT_BAD_INDEX);
+  nsel = t < 0 ? 0 : (a.dense ? vis : a.k);
   const long long w0 = max(0LL, t - a.n_win + 1);
-  const int nwin = (int)(t - w0 + 1);
+  const int nwin = t < 0 ? 0 : (int)(t - w0 + 1);
   for (int jr = 0; jr < nsel + nwin; ++jr) {
     const float* src;
     long long pos;
@@ -117,7 +122,11 @@ __global__ void __launch_bounds__(ATT_F32_THREADS) attend_f32_kernel(AttendF32Ar
       pos = (long long)a.m * (s + 1) - 1;
     } else {
       const long long tok = w0 + (jr - nsel);
-      src = a.win + ((size_t)b * a.T_win + (size_t)(tok - a.win_base)) * d;
+      if (tok < wbase || tok >= wbase + a.T_win) {    // outside this batch row's window buffer
+        if (tid == 0) csa_flag_error(ERRBIT_BAD_INDEX);
+        continue;
+      }
+      src = a.win + ((size_t)b * a.T_win + (size_t)(tok - wbase)) * d;
       pos = tok;
     }
     for (int x = tid; x < d; x += ATT_F32_THREADS) er[x] = src[x];

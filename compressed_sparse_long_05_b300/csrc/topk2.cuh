@@ -31,7 +31,8 @@ constexpr int TK2_MAXBINS = 1 << TK2_BITS1;
 struct Topk2Args {
   const float* scores;
   int32_t* idx;
-  int Tq, N, k, m, q_pos0;
+  const int32_t* q_pos;   // [rows] query positions (null: t = i)
+  int Tq, N, k, m;
   int slice;      // keys per CTA (multiple of 4)
   int cand_cap;   // candidate capacity per CTA
   uint32_t* hist;         // optional [rows][2^BITS1] first-digit histograms of the visible scores;
@@ -94,9 +95,9 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   const int rank = CL > 1 ? (int)cluster.block_rank() : 0;
   const int row = blockIdx.x / CL;
   const int i = row % a.Tq;
-  const long long t = (long long)a.q_pos0 + i;
-  int vis = (int)min((long long)a.N, (t + 1) / a.m);
-  if (vis < 0) vis = 0;
+  const long long t = query_pos(a.q_pos, row, i);
+  int vis = t < 0 ? 0 : (int)min((long long)a.N, (t + 1) / a.m);
+  if (t < 0 && rank == 0 && threadIdx.x == 0) csa_flag_error(ERRBIT_BAD_INDEX);
   const float* srow = a.scores + (size_t)row * a.N;
   int32_t* orow = a.idx + (size_t)row * a.k;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;

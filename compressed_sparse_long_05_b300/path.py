@@ -8,8 +8,9 @@ with m' = 128 and attends densely.  Decode steps start from a given
 compressed cache (a new entry is compressed only when a block closes).
 
 The functions take a dict of device tensors named as in ``synth.generate``
-and a size dict as in ``synth.configs``; they only allocate outputs and call
-the library.
+(including the per-row query positions ``q_pos`` [B, Tq] and the window-buffer
+bases ``win_base`` [B]) and a size dict as in ``synth.configs``; they only
+allocate outputs and call the library.
 """
 
 from __future__ import annotations
@@ -52,7 +53,7 @@ def forward(cfg: dict, x: dict, buf: Buffers | None = None):
     buf = buf or Buffers()
     kind = cfg["kind"]
     m, r, n_win = cfg["m"], cfg["r"], cfg["n_win"]
-    q_pos0, win_base, base = cfg["q_pos0"], cfg["win_base"], cfg["rope_base"]
+    q_pos, win_base, base = x["q_pos"], x["win_base"], cfg["rope_base"]
     if kind == "csa_prefill":
         buf.entries = L.csa_compress(x["Ca"], x["Za"], m, Cb=x["Cb"], Zb=x["Zb"], out=buf.entries)
         entries = buf.entries
@@ -65,18 +66,18 @@ def forward(cfg: dict, x: dict, buf: Buffers | None = None):
     if kind.startswith("csa"):
         qI, qI_sf, K, K_sf = _indexer_args(x)
         buf.scores, buf.idx, buf.ws_topk = L.csa_index_topk(
-            qI, x["w"], K, cfg["k"], m, q_pos0, qI_sf=qI_sf, K_sf=K_sf, scores=buf.scores,
+            qI, x["w"], K, cfg["k"], m, q_pos, qI_sf=qI_sf, K_sf=K_sf, scores=buf.scores,
             idx=buf.idx, ws=buf.ws_topk)
         if buf.ws is None:
-            n = L.attend_workspace_size(x["q"], entries, win, cfg["k"], m, n_win, q_pos0, r, False)
+            n = L.attend_workspace_size(x["q"], entries, win, cfg["k"], m, n_win, r, False)
             buf.ws = L._workspace(None, n, x["q"].device)
         buf.out = L.csa_attend(x["q"], entries, buf.idx, win, x["sink"], m, n_win, win_base,
-                               q_pos0, r, base, out=buf.out, ws=buf.ws)
+                               q_pos, r, base, out=buf.out, ws=buf.ws)
     else:
         if buf.ws is None:
-            n = L.attend_workspace_size(x["q"], entries, win, 0, m, n_win, q_pos0, r, True)
+            n = L.attend_workspace_size(x["q"], entries, win, 0, m, n_win, r, True)
             buf.ws = L._workspace(None, n, x["q"].device)
-        buf.out = L.hca_attend(x["q"], entries, win, x["sink"], m, n_win, win_base, q_pos0, r,
+        buf.out = L.hca_attend(x["q"], entries, win, x["sink"], m, n_win, win_base, q_pos, r,
                                base, out=buf.out, ws=buf.ws)
     return buf.out
 

@@ -21,10 +21,21 @@
  *     text via csa_last_cuda_error()).  Faults found on the device (a bounded
  *     wait that gave up, an out-of-range index) set a sticky device error word
  *     that csa_device_error() reads.
- *   - Query row i of a call sits at absolute token position q_pos0 + i, the
- *     same for every batch row.  Compressed entry s is visible to the query
- *     at position t iff (s+1)*m <= t+1, and its RoPE position is m*(s+1)-1.
- *     T mod m tail tokens are not compressed (§3.6.1: they wait in a buffer).
+ *   - Query positions: q_pos is a DEVICE array int32 [B, Tq]; q_pos[b,i] is
+ *     the absolute token position t of query row i of batch row b, so every
+ *     sequence of a batch may sit at its own context length (§2.3.1: the
+ *     visibility rule is per query t).  q_pos = NULL means t = i for every
+ *     batch row (causal prefill from token 0).  Compressed entry s is visible
+ *     to the query at t iff (s+1)*m <= t+1, and its RoPE position is
+ *     m*(s+1)-1; entries at s >= N are never read, whatever t.  T mod m tail
+ *     tokens are not compressed (§3.6.1: they wait in a buffer).  The host
+ *     cannot see device arrays: a position below 0 sets the device error
+ *     word's bad-index bit, and that row is treated as seeing nothing
+ *     (scores -inf, no index, output 0).
+ *   - Window rows: win_base is a DEVICE array int32 [B]; row j of batch row
+ *     b's window buffer holds raw token win_base[b] + j (NULL = 0 for every
+ *     batch row).  A window token outside a batch row's buffer sets the
+ *     bad-index bit and is left out of that query's row set.
  */
 #ifndef CSA_B300_H
 #define CSA_B300_H
@@ -96,19 +107,19 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
  *   H in {32,64,128}, c == 128; F32 any H, c <= 256.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
-                       const void* K_sf, float* scores, int B, int Tq, int N, int H, int c,
-                       int m, int q_pos0, int dtype, void* stream);
+                       const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
+                       int N, int H, int c, int m, int dtype, void* stream);
 
 /* ---------------------------------------------------------------------------
  * csa_topk — per query row, the k visible entries with the largest scores
  * (§2.3.1 "top-k selector"; C_t = TopK_k(I_t,:)).  Ties are broken toward the
  * lower entry index.  idx[b,i,:] holds the min(k, vis) selected entry indices
  * in ascending order, then -1 up to k.
- *   scores: [B, Tq, N] float32 (only s < vis(t) is read); idx: [B, Tq, k] int32.
- *   Requires 1 <= k <= 4096.
+ *   scores: [B, Tq, N] float32 (only s < vis(t) is read); q_pos: [B, Tq] as
+ *   above; idx: [B, Tq, k] int32.  Requires 1 <= k <= 4096.
  * ------------------------------------------------------------------------- */
-csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, int k, int m,
-                      int q_pos0, void* stream);
+csa_status_t csa_topk(const float* scores, const int32_t* q_pos, int32_t* idx, int B, int Tq,
+                      int N, int k, int m, void* stream);
 
 /* ---------------------------------------------------------------------------
  * csa_index_topk — csa_index followed by csa_topk in one call, with the same
@@ -126,8 +137,8 @@ csa_status_t csa_topk(const float* scores, int32_t* idx, int B, int Tq, int N, i
  *   loop zero-fills it once.  After a failed call, zero-fill it again.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, const void* K,
-                            const void* K_sf, float* scores, int32_t* idx, int B, int Tq, int N,
-                            int H, int c, int m, int q_pos0, int k, int dtype, void* ws,
+                            const void* K_sf, const int32_t* q_pos, float* scores, int32_t* idx,
+                            int B, int Tq, int N, int H, int c, int m, int k, int dtype, void* ws,
                             size_t ws_bytes, void* stream);
 size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype);
 
@@ -142,8 +153,9 @@ size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype);
  *   o = sum p * rotated row; out = o with its last r dims rotated by -t.
  *   q: [B, Tq, n_h, d] (F32 or BF16); out: same shape and dtype as q.
  *   entries: [B, N, d] rows (F32, BF16 or E4M3_BF16ROPE).
- *   win: [B, T_win, d] rows; row j holds raw token win_base + j and must cover
- *        every window position of every query row.
+ *   win: [B, T_win, d] rows; row j of batch row b holds raw token
+ *        win_base[b] + j (win_base: device int32 [B], NULL = 0).
+ *   q_pos: device int32 [B, Tq] query positions (NULL: t = i).
  *   idx: [B, Tq, k] int32 from csa_topk (-1 entries are skipped).
  *   sink: [n_h] float32.
  *   ws / ws_bytes: scratch of at least csa_attend_workspace_size(...) bytes,
@@ -152,22 +164,24 @@ size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype);
  *   n_h * d <= 16384.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_attend(const void* q, csa_kv_t entries, const int32_t* idx, csa_kv_t win,
-                        const float* sink, void* out, int B, int Tq, int N, int k, int T_win,
-                        int win_base, int n_h, int d, int r, int m, int n_win, int q_pos0,
-                        float rope_base, void* ws, size_t ws_bytes, void* stream);
+                        const int32_t* q_pos, const int32_t* win_base, const float* sink,
+                        void* out, int B, int Tq, int N, int k, int T_win, int n_h, int d, int r,
+                        int m, int n_win, float rope_base, void* ws, size_t ws_bytes,
+                        void* stream);
 
 /* hca_attend — csa_attend over every visible compressed entry (block size m = m'),
  * with no index list (§2.3.2: HCA keeps shared-KV MQA but has no top-k). */
-csa_status_t hca_attend(const void* q, csa_kv_t entries, csa_kv_t win, const float* sink,
-                        void* out, int B, int Tq, int N, int T_win, int win_base, int n_h, int d,
-                        int r, int m, int n_win, int q_pos0, float rope_base, void* ws,
-                        size_t ws_bytes, void* stream);
+csa_status_t hca_attend(const void* q, csa_kv_t entries, csa_kv_t win, const int32_t* q_pos,
+                        const int32_t* win_base, const float* sink, void* out, int B, int Tq,
+                        int N, int T_win, int n_h, int d, int r, int m, int n_win,
+                        float rope_base, void* ws, size_t ws_bytes, void* stream);
 
 /* Scratch bytes csa_attend / hca_attend need for these sizes (k = 0 for HCA).
- * q_dtype / kv_dtype as in the calls. */
+ * q_dtype / kv_dtype as in the calls.  The work split is planned for the
+ * largest row set any query can have (min(k, N) or N entries plus
+ * min(n_win, T_win) window rows), so it does not depend on the positions. */
 size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h, int d, int r,
-                                 int m, int n_win, int q_pos0, int q_dtype, int kv_dtype,
-                                 int is_hca);
+                                 int m, int n_win, int q_dtype, int kv_dtype, int is_hca);
 
 /* ---------------------------------------------------------------------------
  * csa_attend_noalloc — csa_attend without a caller-supplied workspace.  The
@@ -200,9 +214,9 @@ size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h
  * ------------------------------------------------------------------------- */
 #define CSA_NOALLOC_SCRATCH_BYTES (16u << 20)
 csa_status_t csa_attend_noalloc(const void* q, csa_kv_t entries, const int32_t* idx, csa_kv_t win,
-                                const float* sink, void* out, int B, int Tq, int N, int k,
-                                int T_win, int win_base, int n_h, int d, int r, int m, int n_win,
-                                int q_pos0, float rope_base, void* stream);
+                                const int32_t* q_pos, const int32_t* win_base, const float* sink,
+                                void* out, int B, int Tq, int N, int k, int T_win, int n_h, int d,
+                                int r, int m, int n_win, float rope_base, void* stream);
 
 /* Reads and clears the sticky device error word (synchronises `stream`).
  * Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE. */

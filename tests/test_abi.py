@@ -55,21 +55,32 @@ def test_host_side_argument_errors(L):
     # unsupported dtype / width
     assert L.csa_compress(fake, None, fake, None, None, None, fake, 1, 8, 64, 4, 3, None) == 2
     assert L.csa_compress(fake, None, fake, None, None, None, fake, 1, 8, 60, 4, 1, None) == 2
-    # top-k: k out of range, negative sizes
-    assert L.csa_topk(fake, fake, 1, 1, 100, 0, 4, 0, None) == 1
-    assert L.csa_topk(fake, fake, 1, 1, 100, 5000, 4, 0, None) == 1
-    assert L.csa_topk(fake, fake, -1, 1, 100, 5, 4, 0, None) == 1
+    # top-k: k out of range, negative sizes, misaligned positions
+    assert L.csa_topk(fake, None, fake, 1, 1, 100, 0, 4, None) == 1
+    assert L.csa_topk(fake, None, fake, 1, 1, 100, 5000, 4, None) == 1
+    assert L.csa_topk(fake, None, fake, -1, 1, 100, 5, 4, None) == 1
+    assert L.csa_topk(fake, mis, fake, 1, 1, 100, 5, 4, None) == 1
     # index: null scores
-    assert L.csa_index(fake, None, fake, fake, None, None, 1, 1, 8, 4, 32, 4, 0, 0, None) == 1
-    # attend: window buffer does not cover the query's window
+    assert L.csa_index(fake, None, fake, fake, None, None, None, 1, 1, 8, 4, 32, 4, 0, None) == 1
     kv = KV(1, 0x10000, None, None)
-    assert L.csa_attend(fake, kv, fake, kv, fake, fake, 1, 1, 8, 4, 16, 0, 128, 512, 64, 4, 128,
-                        1000, 10000.0, None, 0, None) == 1
     # attend: odd rope dims
-    assert L.csa_attend(fake, kv, fake, kv, fake, fake, 1, 1, 8, 4, 128, 0, 128, 512, 63, 4, 128,
-                        127, 10000.0, None, 0, None) == 1
+    assert L.csa_attend(fake, kv, fake, kv, None, None, fake, fake, 1, 1, 8, 4, 128, 128, 512, 63,
+                        4, 128, 10000.0, None, 0, None) == 1
+    # attend: misaligned window bases
+    assert L.csa_attend(fake, kv, fake, kv, None, mis, fake, fake, 1, 1, 8, 4, 128, 128, 512, 64,
+                        4, 128, 10000.0, None, 0, None) == 1
+    # attend: no index list
+    assert L.csa_attend(fake, kv, None, kv, None, None, fake, fake, 1, 1, 8, 4, 128, 128, 512, 64,
+                        4, 128, 10000.0, None, 0, None) == 1
+    # attend: no kernel for d = 500 with bf16 rows
+    assert L.csa_attend(fake, kv, fake, kv, None, None, fake, fake, 1, 1, 8, 4, 128, 128, 500, 64,
+                        4, 128, 10000.0, None, 0, None) == 2
+    # attend: a workspace the plan needs but the caller did not pass (prefill-shaped:
+    # every stored row is rotated once into the workspace)
+    assert L.csa_attend(fake, kv, fake, kv, None, None, fake, fake, 1, 4096, 1024, 64, 4096, 128,
+                        512, 64, 4, 128, 10000.0, None, 0, None) == 3
     # empty batch is a no-op
-    assert L.csa_topk(fake, fake, 0, 1, 100, 5, 4, 0, None) == 0
+    assert L.csa_topk(fake, None, fake, 0, 1, 100, 5, 4, None) == 0
 
 
 def test_workspace_sizes_follow_the_plan(L):
@@ -83,10 +94,10 @@ def test_workspace_sizes_follow_the_plan(L):
     assert L.csa_index_topk_workspace_size(1, 1, 32768, 0) == 0          # fp32 scores: two calls
     # decode, 128K context, batch 4: 9 chunks of 128 rows per head group; unless the
     # chunks merge inside a cluster, each keeps a [64 heads][512] fp32 partial
-    ws = L.csa_attend_workspace_size(4, 1, 32768, 1024, 128, 128, 512, 64, 4, 128, 131071, 1, 1, 0)
+    ws = L.csa_attend_workspace_size(4, 1, 32768, 1024, 128, 128, 512, 64, 4, 128, 1, 1, 0)
     assert ws == 0 or ws >= 72 * 64 * 512 * 4
     # causal prefill: every stored row is rotated once into the workspace (1 KB per row)
-    ws = L.csa_attend_workspace_size(1, 32768, 8192, 1024, 32768, 128, 512, 64, 4, 128, 0, 1, 1, 0)
+    ws = L.csa_attend_workspace_size(1, 32768, 8192, 1024, 32768, 128, 512, 64, 4, 128, 1, 1, 0)
     assert ws >= (8192 + 32768) * 1024
     # shapes the tensor-core path does not take need no workspace
-    assert L.csa_attend_workspace_size(1, 1, 100, 16, 16, 4, 128, 32, 4, 16, 399, 0, 0, 0) == 0
+    assert L.csa_attend_workspace_size(1, 1, 100, 16, 16, 4, 128, 32, 4, 16, 0, 0, 0) == 0

@@ -96,8 +96,9 @@ def _check_workload(K, name, batch_rows=None):
             ref = O.compress_hca(f64(x["C"][b]), f64(x["Z"][b]), m)
             assert_close(ent[probe], ref[probe], TOL_BF16, TOL_BF16, f"{name} compress")
         win = _window(x, b)
+        win_base = int(x["win_base"][b])
         for i in rows:
-            t = cfg["q_pos0"] + i
+            t = int(x["q_pos"][b, i])
             q = f64(x["q"][b, i])
             if cfg["kind"].startswith("csa"):
                 qI, Kc = _indexer(x, b, i)
@@ -110,9 +111,9 @@ def _check_workload(K, name, batch_rows=None):
                 n = min(cfg["k"], vis)
                 assert np.array_equal(got_i[:n], want), f"{name} top-k b={b} i={i}"
                 assert np.all(got_i[n:] == -1)
-                ref_o = O.csa_attend_token(q, t, ent, got_i, win, cfg["win_base"], sink, m, n_win, r, base)
+                ref_o = O.csa_attend_token(q, t, ent, got_i, win, win_base, sink, m, n_win, r, base)
             else:
-                ref_o = O.hca_attend_token(q, t, ent, win, cfg["win_base"], sink, m, n_win, r, base)
+                ref_o = O.hca_attend_token(q, t, ent, win, win_base, sink, m, n_win, r, base)
             assert_close(f64(out[b, i]), ref_o, tol, tol, f"{name} attend b={b} i={i} t={t}")
 
 

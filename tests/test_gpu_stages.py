@@ -79,7 +79,7 @@ def test_compress_bias(K):
 def test_index_f32(K):
     cfg = synth.get("tiny_csa_prefill_f32")
     x = synth.make_inputs(cfg, device=DEV)
-    s = K.csa_index(x["qI"], x["w"], x["K"], cfg["m"], cfg["q_pos0"])
+    s = K.csa_index(x["qI"], x["w"], x["K"], cfg["m"], x["q_pos"])
     torch.cuda.synchronize()
     ref = O.index_scores(f64(x["qI"][0]), f64(x["w"][0]), f64(x["K"][0]), np.arange(cfg["T"]), cfg["m"])
     for t in range(cfg["T"]):
