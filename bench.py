@@ -128,7 +128,10 @@ def _work_one(cfg, t):
     if kind.endswith("prefill"):
         T = cfg["T"]
         nt = 4 if kind == "csa_prefill" else 2
-        out["compress"] = (B * (nt * T * d * el + N * d * el), 0.0)
+        cb = nt * T * d * el + N * d * el
+        if cfg.get("index_keys") == "compressed":          # K^IComp from raw index rows
+            cb += 4 * T * cfg["c_I"] * el + N * cfg["c_I"] * el
+        out["compress"] = (B * cb, 0.0)
     if kind.startswith("csa"):
         H, c, k = cfg["H_I"], cfg["c_I"], cfg["k"]
         kb = (c // 2 + c // 16) if cfg["dtype"] == "mixed" else c * el
@@ -240,32 +243,32 @@ def make_step(K, cfg, x, buf):
     m, r, n_win = cfg["m"], cfg["r"], cfg["n_win"]
     q0, wb, base = x["q_pos"], x["win_base"], cfg["rope_base"]
     kind = cfg["kind"]
+    rot = bool(cfg.get("entry_rope"))
     stages = []
-    if kind == "csa_prefill":
-        stages.append(("compress", lambda: K.csa_compress(x["Ca"], x["Za"], m, Cb=x["Cb"], Zb=x["Zb"],
-                                                          out=buf.entries)))
-    if kind == "hca_prefill":
-        stages.append(("compress", lambda: K.csa_compress(x["C"], x["Z"], m, out=buf.entries)))
+    if kind.endswith("prefill"):
+        stages.append(("compress", lambda: P.compress_stage(cfg, x, buf)))
     ent = buf.entries if kind.endswith("prefill") else P._entries_arg(x)
     win = P._win_arg(x)
     if kind.startswith("csa") and cfg["Tq"] == 1:
         # decode: one call scores every entry and selects the top k (the index
         # kernel also builds the selector's first histogram)
-        qI, qI_sf, Kt, K_sf = P._indexer_args(x)
+        qI, qI_sf, Kt, K_sf = P._indexer_args(x, buf)
         stages.append(("index_topk", lambda: K.csa_index_topk(
             qI, x["w"], Kt, cfg["k"], m, q0, qI_sf=qI_sf, K_sf=K_sf, scores=buf.scores,
             idx=buf.idx, ws=buf.ws_topk)))
     elif kind.startswith("csa"):
-        qI, qI_sf, Kt, K_sf = P._indexer_args(x)
+        qI, qI_sf, Kt, K_sf = P._indexer_args(x, buf)
         stages.append(("index", lambda: K.csa_index(qI, x["w"], Kt, m, q0, qI_sf=qI_sf, K_sf=K_sf,
                                                     scores=buf.scores)))
         stages.append(("topk", lambda: K.csa_topk(buf.scores, cfg["k"], m, q0, idx=buf.idx)))
     if kind.startswith("csa"):
         stages.append(("attend", lambda: K.csa_attend(x["q"], ent, buf.idx, win, x["sink"], m, n_win,
-                                                      wb, q0, r, base, out=buf.out, ws=buf.ws)))
+                                                      wb, q0, r, base, out=buf.out, ws=buf.ws,
+                                                      entries_rotated=rot)))
     else:
         stages.append(("attend", lambda: K.hca_attend(x["q"], ent, win, x["sink"], m, n_win, wb, q0,
-                                                      r, base, out=buf.out, ws=buf.ws)))
+                                                      r, base, out=buf.out, ws=buf.ws,
+                                                      entries_rotated=rot)))
     return stages
 
 
@@ -276,6 +279,8 @@ def alloc_buffers(K, cfg, x, dev):
     kind = cfg["kind"]
     if kind.endswith("prefill"):
         buf.entries = torch.empty((B, N, d), dtype=x["q"].dtype, device=dev)
+        if "CIa" in x:
+            buf.K = torch.empty((B, N, cfg["c_I"]), dtype=x["CIa"].dtype, device=dev)
     if kind.startswith("csa"):
         buf.scores = torch.empty((B, Tq, N), dtype=torch.float32, device=dev)
         buf.idx = torch.empty((B, Tq, cfg["k"]), dtype=torch.int32, device=dev)
@@ -485,6 +490,66 @@ def gpu_arm(args, cfg, rank, world, with_e2e=True):
     return line, x_first
 
 
+def projection_leg(args, dev, tokens, g=16, d_g=1024, n_h=128, d=512, d_model=7168, reps=None):
+    """The grouped output projection at V4-Pro shape (DeepSeek-V4 report,
+    Chinese translation, §2.3.1 and §4.2.1: g = 16, d_g = 1024, d = 7168) for
+    `tokens` rows: the [tokens, n_h*d] attention output through 16 grouped
+    GEMMs to [tokens, g*d_g], then one GEMM to [tokens, d_model].  Synthetic
+    bf16 inputs and weights.  Returns timing, roofline and launch counts."""
+    import compressed_sparse_long_05_b300 as K
+    hbm_peak, tf_burst, tf_sust, peak_src = peaks()
+    gen = torch.Generator(device=dev).manual_seed(7)
+    Kg = (n_h // g) * d
+    A = torch.randn((tokens, n_h * d), generator=gen, device=dev).to(torch.bfloat16)
+    Wg = (torch.randn((g, d_g, Kg), generator=gen, device=dev) * Kg ** -0.5).to(torch.bfloat16)
+    Wo = (torch.randn((1, d_model, g * d_g), generator=gen, device=dev) * (g * d_g) ** -0.5).to(torch.bfloat16)
+    y = torch.empty((tokens, g * d_g), dtype=torch.bfloat16, device=dev)
+    z = torch.empty((tokens, d_model), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    reps = reps or max(3, min(args.steps, 20))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    t1, t2 = [], []
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            K.csa_grouped_proj(A, Wg, C=y)
+            K.csa_grouped_proj(y, Wo, C=z)
+        for _ in range(reps):
+            ev[0].record()
+            K.csa_grouped_proj(A, Wg, C=y)
+            ev[1].record()
+            K.csa_grouped_proj(y, Wo, C=z)
+            ev[2].record()
+            ev[2].synchronize()
+            t1.append(ev[0].elapsed_time(ev[1]))
+            t2.append(ev[1].elapsed_time(ev[2]))
+    K.device_error()
+    ms1, ms2 = float(np.median(t1)), float(np.median(t2))
+    f1 = 2.0 * tokens * g * Kg * d_g
+    f2 = 2.0 * tokens * (g * d_g) * d_model
+    b1 = 2 * (tokens * n_h * d + g * d_g * Kg + tokens * g * d_g)
+    b2 = 2 * (tokens * g * d_g + d_model * g * d_g + tokens * d_model)
+    out = {"tokens": tokens, "ms": round(ms1 + ms2, 5), "steps": reps,
+           "grouped": {"ms": round(ms1, 5), "TFLOP/s": round(f1 / ms1 / 1e9, 1),
+                       "GB/s": round(b1 / ms1 / 1e6, 1)},
+           "final": {"ms": round(ms2, 5), "TFLOP/s": round(f2 / ms2 / 1e9, 1),
+                     "GB/s": round(b2 / ms2 / 1e6, 1)},
+           "gpu_launches": 2 * reps}
+    if tokens >= 1024:
+        ach = (f1 + f2) / ((ms1 + ms2) * 1e9)
+        out["roofline"] = {"bound": "tensor", "achieved": round(ach, 1), "peak": tf_sust,
+                           "unit": "TFLOP/s", "frac": round(ach / tf_sust, 4),
+                           "peak_source": peak_src + " (bf16_tflops_sustained)"}
+    else:
+        ach = (b1 + b2) / ((ms1 + ms2) * 1e6)
+        out["roofline"] = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
+                           "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
+                           "peak_source": peak_src + " (hbm_gbs, copy)",
+                           "note": "few tokens: the weights (369 MB) dominate the bytes"}
+    del A, Wg, Wo, y, z
+    torch.cuda.synchronize()
+    return out
+
+
 def e2e_leg(K, cfg, x, buf, stream, args, dev):
     """Same metric through the public API with per-step H2D of the step's new inputs
     (queries, indexer queries and weights; prefill also the raw rows and window)
@@ -499,7 +564,7 @@ def e2e_leg(K, cfg, x, buf, stream, args, dev):
     names = ["q"] + (["qI", "w"] if "qI" in x else (["qI_fp4", "qI_sf", "w"] if "qI_fp4" in x else []))
     decode = cfg["kind"].endswith("decode")
     if not decode:
-        names += [n for n in ("Ca", "Cb", "Za", "Zb", "C", "Z") if n in x]
+        names += [n for n in ("Ca", "Cb", "Za", "Zb", "C", "Z", "CIa", "CIb", "ZIa", "ZIb") if n in x]
         names += ["win"] if "win" in x else []
     n_steps = max(3, min(args.steps, 200 if decode else 3))
     if decode:
@@ -560,11 +625,35 @@ def cpu_info():
 
 
 def blas_threads():
+    """(threads of numpy's BLAS pool, note).  Without threadpoolctl the pool
+    size is not known: the logical core count is reported, with the reason."""
     try:
         from threadpoolctl import threadpool_info
-        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        info = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if info:
+            return max(int(i.get("num_threads", 1)) for i in info), "numpy BLAS pool (threadpoolctl)"
+        note = "threadpoolctl saw no BLAS pool"
+    except Exception as e:   # pragma: no cover - depends on the host
+        note = f"threadpoolctl failed: {e!r}"[:160]
+    return cpu_info()[0], note + "; reporting the logical cores"
+
+
+def one_thread_rate(workload, budget_s):
+    """The oracle's tokens/s with every BLAS/OpenMP pool held to one thread:
+    a child process (the pool size is fixed when numpy loads) that generates
+    the workload's inputs on the CPU and times a bounded sample."""
+    import subprocess
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import sys, json; sys.path.insert(0, %r); import bench, synth; "
+            "cfg = synth.get(%r); x = bench.host_copy(synth.make_inputs(cfg, seed=0)); "
+            "print(json.dumps(bench.oracle_sample(cfg, x, %r)[0]))" % (ROOT, workload, budget_s))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=120 + 4 * budget_s)
+        return float(r.stdout.strip().splitlines()[-1])
     except Exception:
-        return 1
+        return None
 
 
 def oracle_sample(cfg, x_np, budget_s):
@@ -611,22 +700,18 @@ def oracle_sample(cfg, x_np, budget_s):
 
 
 def cpu_baseline(cfg, x_np, budget_s):
-    """The oracle timed on this host: its BLAS thread pool as it stands, and
-    one thread, on bounded samples of the workload (~2/3 and ~1/3 of budget_s)."""
+    """The oracle timed on this host: its BLAS thread pool as it stands on a
+    bounded sample of the workload (~2/3 of budget_s), and one thread in a
+    child process (~1/3)."""
     cores, model = cpu_info()
-    threads = blas_threads()
+    threads, note = blas_threads()
     tps, desc = oracle_sample(cfg, x_np, budget_s * 2 / 3)
-    try:
-        from threadpoolctl import threadpool_limits
-        with threadpool_limits(limits=1):
-            tps1, _ = oracle_sample(cfg, x_np, budget_s / 3)
-    except Exception:
-        tps1 = None
+    tps1 = one_thread_rate(cfg["name"], budget_s / 3) if cfg["name"] in synth.configs.WORKLOADS else None
     return {"value": round(tps, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": desc, "nproc": cores, "cpu_model": model,
             "value_1_thread": None if tps1 is None else round(tps1, 4),
-            "threads_note": "float64 numpy oracle: its row loop is serial Python; only the BLAS "
-                            f"matrix products use the {threads}-thread pool"}
+            "threads_note": f"{note}; float64 numpy oracle: its row loop is serial Python, only "
+                            "the BLAS matrix products use the pool"}
 
 
 class _RowView:
@@ -685,7 +770,7 @@ def reference_arm(args, cfg, rank, world):
             "ms_per_step": round(tokens / value * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": cfg_out,
-            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": blas_threads(),
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": blas_threads()[0],
                              "kind": "oracle", "nproc": cores, "cpu_model": model,
                              "sample": desc + f"; {run_steps} sample steps of ~{per_step_budget:.0f}s"},
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -757,6 +842,11 @@ def main():
                 pf["cpu_baseline"] = cpu_baseline(pcfg, host_copy(px0), args.cpu_budget)
             del px0
             line["prefill_32k"] = pf
+            dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+            line["output_projection"] = {
+                "what": "grouped output projection, V4-Pro shape (g=16, d_g=1024, d=7168), bf16",
+                "prefill_32k": projection_leg(args, dev, 32768),
+                "decode_b4": projection_leg(args, dev, 4)}
         if rank == 0:
             print(json.dumps(line), flush=True)
     if world > 1:

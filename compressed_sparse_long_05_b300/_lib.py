@@ -14,7 +14,9 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "lib", "libcsa_b300.so")
+# CSA_LIB_TRACE=1 loads the phase-trace build of the same sources (build --trace)
+TRACE = os.environ.get("CSA_LIB_TRACE") == "1"
+LIB_PATH = os.path.join(HERE, "lib", "libcsa_b300_trace.so" if TRACE else "libcsa_b300.so")
 
 DT_F32, DT_BF16, DT_E4M3_BF16ROPE, DT_E2M1_BLOCK16 = 0, 1, 2, 3
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or dtype",
@@ -29,8 +31,17 @@ class CsaError(RuntimeError):
 
 
 class KV(ctypes.Structure):
-    _fields_ = [("dtype", ctypes.c_int32), ("data", ctypes.c_void_p),
+    _fields_ = [("dtype", ctypes.c_int32), ("flags", ctypes.c_int32), ("data", ctypes.c_void_p),
                 ("scale", ctypes.c_void_p), ("rope", ctypes.c_void_p)]
+
+
+class CompressOpts(ctypes.Structure):
+    _fields_ = [("rms_norm", ctypes.c_int32), ("norm_eps", ctypes.c_float),
+                ("norm_weight", ctypes.c_void_p), ("rope_dims", ctypes.c_int32),
+                ("rope_base", ctypes.c_float)]
+
+
+KV_ROTATED = 1
 
 
 _lib = None
@@ -38,14 +49,18 @@ _lib = None
 _I, _P, _F, _Z = ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
     "csa_compress": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
+    "csa_compress_ex": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                        ctypes.POINTER(CompressOpts), _P],
     "csa_index": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
     "csa_topk": [_P, _P, _P, _I, _I, _I, _I, _I, _P],
     "csa_index_topk": [_P, _P, _P, _P, _P, _P, _P, _P] + [_I] * 8 + [_P, _Z, _P],
     "csa_index_topk_workspace_size": [_I] * 4,
     "csa_attend": [_P, KV, _P, KV, _P, _P, _P, _P] + [_I] * 10 + [_F, _P, _Z, _P],
-    "hca_attend": [_P, KV, KV, _P, _P, _P, _P] + [_I] * 10 + [_F, _P, _Z, _P],
+    "hca_attend": [_P, KV, KV, _P, _P, _P, _P] + [_I] * 9 + [_F, _P, _Z, _P],
     "csa_attend_noalloc": [_P, KV, _P, KV, _P, _P, _P, _P] + [_I] * 10 + [_F, _P],
     "csa_attend_workspace_size": [_I] * 13,
+    "csa_selftest_wait_timeout": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
+    "csa_grouped_proj": [_P, ctypes.c_int64, _P, _P, ctypes.c_int64, _I, _I, _I, _I, _P],
     "csa_device_error": [_P],
     "csa_status_string": [_I],
     "csa_last_cuda_error": [],
@@ -67,6 +82,9 @@ def lib():
             f = getattr(L, name)
             f.argtypes = args
             f.restype = _RESTYPES.get(name, ctypes.c_int)
+        if TRACE:
+            L.csa_trace_read.argtypes = [_P, _I]
+            L.csa_trace_read.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -93,12 +111,14 @@ def _dt(t):
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def _kv(rows):
-    """A row set: a float32/bf16 tensor [B, rows, d] or (e4m3 bytes, scale, bf16 rope)."""
+def _kv(rows, rotated=False):
+    """A row set: a float32/bf16 tensor [B, rows, d] or (e4m3 bytes, scale, bf16 rope);
+    ``rotated``: its RoPE dims are already rotated at each entry's position."""
+    fl = KV_ROTATED if rotated else 0
     if isinstance(rows, (tuple, list)):
         nope, scale, rope = rows
-        return KV(DT_E4M3_BF16ROPE, nope.data_ptr(), scale.data_ptr(), rope.data_ptr())
-    return KV(_dt(rows), rows.data_ptr(), None, None)
+        return KV(DT_E4M3_BF16ROPE, fl, nope.data_ptr(), scale.data_ptr(), rope.data_ptr())
+    return KV(_dt(rows), fl, rows.data_ptr(), None, None)
 
 
 def positions(q_pos, B, Tq, device):
@@ -137,13 +157,26 @@ def _rows_shape(rows):
 # ----------------------------------------------------------------------------
 
 
-def csa_compress(Ca, Za, m, Cb=None, Zb=None, Ba=None, Bb=None, out=None):
-    """Compressed entries [B, T//m, d] (Cb = Zb = None: HCA, no overlap)."""
+def csa_compress(Ca, Za, m, Cb=None, Zb=None, Ba=None, Bb=None, out=None, rms_norm=False,
+                 norm_eps=0.0, norm_weight=None, rope_dims=0, rope_base=10000.0):
+    """Compressed entries [B, T//m, d] (Cb = Zb = None: HCA, no overlap).
+
+    ``rms_norm`` / ``rope_dims``: the optional epilogue of csa_compress_ex
+    (RMSNorm of every entry, then RoPE of its last rope_dims dims at its
+    position m(i+1)-1)."""
     B, T, d = Ca.shape
     if out is None:
         out = torch.empty((B, T // m, d), dtype=Ca.dtype, device=Ca.device)
-    _check("csa_compress", lib().csa_compress(_p(Ca), _p(Cb), _p(Za), _p(Zb), _p(Ba), _p(Bb),
-                                              _p(out), B, T, d, m, _dt(Ca), _stream()))
+    if not rms_norm and not rope_dims:
+        _check("csa_compress", lib().csa_compress(_p(Ca), _p(Cb), _p(Za), _p(Zb), _p(Ba), _p(Bb),
+                                                  _p(out), B, T, d, m, _dt(Ca), _stream()))
+        return out
+    opts = CompressOpts(1 if rms_norm else 0, norm_eps,
+                        None if norm_weight is None else norm_weight.data_ptr(), rope_dims,
+                        rope_base)
+    _check("csa_compress_ex", lib().csa_compress_ex(
+        _p(Ca), _p(Cb), _p(Za), _p(Zb), _p(Ba), _p(Bb), _p(out), B, T, d, m, _dt(Ca),
+        ctypes.byref(opts), _stream()))
     return out
 
 
@@ -217,11 +250,12 @@ def _workspace(ws, nbytes, device, zero=False):
 
 
 def csa_attend(q, entries, idx, win, sink, m, n_win, win_base, q_pos, r, rope_base=10000.0,
-               out=None, ws=None):
+               out=None, ws=None, entries_rotated=False):
     """Sparse shared-KV attention output [B, Tq, n_h, d] (dtype of q).
 
     ``q_pos``: query positions (see :func:`positions`); ``win_base``: token of
-    window row 0 per batch row (see :func:`window_bases`)."""
+    window row 0 per batch row (see :func:`window_bases`); ``entries_rotated``:
+    the entries' RoPE dims are already rotated (csa_compress with rope_dims)."""
     B, Tq, n_h, d = q.shape
     _, N, _ = _rows_shape(entries)
     _, T_win, _ = _rows_shape(win)
@@ -232,7 +266,7 @@ def csa_attend(q, entries, idx, win, sink, m, n_win, win_base, q_pos, r, rope_ba
     nbytes = attend_workspace_size(q, entries, win, k, m, n_win, r, False)
     ws = _workspace(ws, nbytes, q.device)
     _check("csa_attend", lib().csa_attend(
-        _p(q), _kv(entries), _p(idx), _kv(win), _p(qp), _p(wb), _p(sink), _p(out), B, Tq, N, k,
+        _p(q), _kv(entries, entries_rotated), _p(idx), _kv(win), _p(qp), _p(wb), _p(sink), _p(out), B, Tq, N, k,
         T_win, n_h, d, r, m, n_win, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
     return out
 
@@ -258,7 +292,7 @@ def csa_attend_noalloc(q, entries, idx, win, sink, m, n_win, win_base, q_pos, r,
 
 
 def hca_attend(q, entries, win, sink, m, n_win, win_base, q_pos, r, rope_base=10000.0,
-               out=None, ws=None):
+               out=None, ws=None, entries_rotated=False):
     """Dense (HCA) shared-KV attention output [B, Tq, n_h, d] (dtype of q)."""
     B, Tq, n_h, d = q.shape
     _, N, _ = _rows_shape(entries)
@@ -269,9 +303,26 @@ def hca_attend(q, entries, win, sink, m, n_win, win_base, q_pos, r, rope_base=10
     nbytes = attend_workspace_size(q, entries, win, 0, m, n_win, r, True)
     ws = _workspace(ws, nbytes, q.device)
     _check("hca_attend", lib().hca_attend(
-        _p(q), _kv(entries), _kv(win), _p(qp), _p(wb), _p(sink), _p(out), B, Tq, N, T_win, n_h, d,
+        _p(q), _kv(entries, entries_rotated), _kv(win), _p(qp), _p(wb), _p(sink), _p(out), B, Tq, N, T_win, n_h, d,
         r, m, n_win, rope_base, _p(ws) if nbytes else None, nbytes, _stream()))
     return out
+
+
+def csa_grouped_proj(A, W, C=None, G=None, lda=None, ldc=None):
+    """One grouped projection GEMM: for j < G, C[:, jN:(j+1)N] = A[:, jK:(j+1)K] W[j]^T.
+
+    A: [M, >= G*K] bf16 (row stride ``lda``, default its row length); W:
+    [G, N, K] bf16; returns C [M, G*N] bf16 (or fills ``C``)."""
+    Gw, N, K = W.shape
+    G = Gw if G is None else G
+    M = A.shape[0]
+    lda = A.stride(0) if lda is None else lda
+    if C is None:
+        C = torch.empty((M, G * N), dtype=torch.bfloat16, device=A.device)
+    ldc = C.stride(0) if ldc is None else ldc
+    _check("csa_grouped_proj", lib().csa_grouped_proj(_p(A), lda, _p(W), _p(C), ldc, M, N, K, G,
+                                                      _stream()))
+    return C
 
 
 def device_error():

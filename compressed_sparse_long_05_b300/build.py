@@ -17,6 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libcsa_b300.so")
+LIB_TRACE = os.path.join(LIBDIR, "libcsa_b300_trace.so")   # phase-trace variant (-DCSA_TRACE)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,30 +32,32 @@ def sources():
     return sorted(os.path.join(SRC, f) for f in os.listdir(SRC) if f.endswith((".cu", ".cuh")))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     hdr = os.path.join(os.path.dirname(HERE), "include", "csa.h")
     return all(os.path.getmtime(s) <= t for s in sources() + [hdr, __file__])
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Compiles the library (or, with trace=True, its phase-trace variant)."""
+    lib = LIB_TRACE if trace else LIB
+    if not force and up_to_date(lib):
+        return lib
     os.makedirs(LIBDIR, exist_ok=True)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "--expt-relaxed-constexpr", "-Xptxas", "-v" if verbose else "-O3",
-           "-o", tmp, os.path.join(SRC, "csa_lib.cu")]
+           *(["-DCSA_TRACE"] if trace else []), "-o", tmp, os.path.join(SRC, "csa_lib.cu")]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
     if verbose:
         sys.stderr.write(res.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -91,6 +91,7 @@ struct AttendTcArgs {
   int rel_rope;                  // 1 = rows rotated by (position - t): q and out stay unrotated
   int kv_mixed;                  // 1 = e4m3 + scale + bf16 rope rows
   int cl_reduce;                 // 1 = the nch chunks of a head group are one cluster and merge over DSMEM
+  int ent_rotated;               // 1 = entries stored with their RoPE dims already rotated at m(s+1)-1
   float scale_log2;              // log2(e) / sqrt(d)
   RopeFreqs rf;
 };
@@ -246,6 +247,7 @@ CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint8
   float* wts = reinterpret_cast<float*>(smem + AttSmem::WTS);
   float* invd = reinterpret_cast<float*>(smem + AttSmem::INVD);
   cl.sync();                                          // every chunk's O and (max, sum) staged
+  if (threadIdx.x == 0) CSA_TRACE_MARK(17);
   if (threadIdx.x < ATT_HG) {
     const int h = threadIdx.x;
     float M = -INFINITY;
@@ -262,6 +264,7 @@ CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint8
     invd[h] = 1.f / den;
   }
   __syncthreads();
+  if (threadIdx.x == 0) CSA_TRACE_MARK(18);
   const float4* srcs[16];
 #pragma unroll
   for (int c = 0; c < 16; ++c)
@@ -292,7 +295,9 @@ CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint8
     pk.y = *reinterpret_cast<uint32_t*>(&hi2);
     *reinterpret_cast<uint2*>(a.out + (orow + h) * ATT_D + (q & 127) * 4) = pk;
   }
+  if (threadIdx.x == 0) CSA_TRACE_MARK(19);
   cl.sync();                                          // no CTA leaves while peers read its memory
+  if (threadIdx.x == 0) CSA_TRACE_MARK(20);
 }
 
 __global__ void __launch_bounds__(ATT_THREADS, 1)
@@ -325,6 +330,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttSmem::MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) { CSA_TRACE_WALL(0); CSA_TRACE_MARK(1); }
 
   if (threadIdx.x == 0) {
     for (int c = 0; c < 8; ++c) mbar_init(chunk_full + c, 4);
@@ -351,6 +357,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
+  if (threadIdx.x == 0) CSA_TRACE_MARK(2);
   const uint32_t TM_O = 0, TM_S = 256;     // O^T blocks at 0..255, S^T buffers at 256..383
 
   if (warp >= 4 && warp < 8) {
@@ -383,7 +390,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
               } else {
                 src = reinterpret_cast<const uint8_t*>(a.ent) + row * ATT_D * 2;
               }
-              pos = (long long)a.m * (s + 1) - 1;
+              pos = a.ent_rotated ? 0 : (long long)a.m * (s + 1) - 1;   // rotated already: turn by -t only
             }
           } else {
             const long long tok = x.w0 + (rr - x.nsel);
@@ -402,6 +409,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             }
           }
         }
+        if (n == (uint32_t)CSA_TRACE_TILE && gw == 0 && lane == 0) CSA_TRACE_MARK(5);
         // rows with no source (past the chunk, index -1) take logit -inf in the softmax
         {
           const uint32_t bits = __ballot_sync(0xffffffffu, src != nullptr);
@@ -441,6 +449,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             if (!ok) break;
             for (int c = 0; c < 8; ++c) cp_chunk(c);
             __syncwarp();
+            if (n == (uint32_t)CSA_TRACE_TILE && gw == 0 && lane == 0) CSA_TRACE_MARK(6);
             if (!a.rel_rope) {
               // absolute-RoPE mode: rotate this warp's 16 heads of the TMA-loaded
               // queries (chunk 7 = dims 448..511) at t, then release them to the MMA
@@ -470,6 +479,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             cp_async_commit();                        // wait for every copy this lane issued
             cp_async_wait<0>();
             __syncwarp();
+            if (n == (uint32_t)CSA_TRACE_TILE && gw == 0 && lane == 0) CSA_TRACE_MARK(7);
             uint8_t* c7 = sE + 7 * 16384;
 #pragma unroll 2
             for (int k2 = 0; k2 < 8; ++k2) {
@@ -483,6 +493,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(chunk_full + 7);
+            if (n == (uint32_t)CSA_TRACE_TILE && gw == 0 && lane == 0) CSA_TRACE_MARK(8);
           }
           continue;
         }
@@ -574,8 +585,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
           const int qrow = (x.b * a.Tq + x.i) * a.n_h + x.hg * ATT_HG;
 #pragma unroll
           for (int c = 0; c < 8; ++c) tma_load_3d(sQ + c * 8192, &tm_q, q_full, c * 64, qrow, 0);
+          if (nitem == 0) CSA_TRACE_MARK(3);
         }
         if (!mbar_wait(a.rel_rope ? q_full : q_ready, nitem & 1, abort_flag)) { ok = false; break; }
+        if (nitem == 0) CSA_TRACE_MARK(4);
         const uint32_t item = nitem++;
         int j = 0;
         for (int r0 = x.r0; r0 < x.r1; r0 += ATT_TILE, ++n, ++j) {
@@ -593,6 +606,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             }
           }
           if (!ok) break;
+          if (n == (uint32_t)CSA_TRACE_TILE) CSA_TRACE_MARK(9);
           umma_commit(s_full + sb);
           if (r0 + ATT_TILE >= x.r1) umma_commit(q_free);
           if (j == 0 && !mbar_wait(o_free, (item & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -609,6 +623,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             umma_commit(chunk_free + bk);
           }
           umma_commit(p_free);
+          if (n == (uint32_t)CSA_TRACE_TILE) CSA_TRACE_MARK(12);
         }
       }
       umma_commit(mma_done);
@@ -630,6 +645,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
       for (int r0 = x.r0; r0 < x.r1; r0 += ATT_TILE, ++n, ++j) {
         const uint32_t sb = n & 1, par = n & 1;
         if (!mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (n == (uint32_t)CSA_TRACE_TILE && q4 == 0 && lane == 0) CSA_TRACE_MARK(10);
         tc_fence_after();
         float xs[64];
         {
@@ -726,6 +742,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
+        if (n == (uint32_t)CSA_TRACE_TILE && q4 == 0 && lane == 0) CSA_TRACE_MARK(11);
         // ---- per-head row sums ----
         warp_reduce_scatter64<false>(pr, lane);
         sump[(par * 4 + q4) * 64 + 2 * lane] = pr[0];
@@ -739,6 +756,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
           l_run[e] += sump[(par * 4 + 0) * 64 + h] + sump[(par * 4 + 1) * 64 + h] +
                       sump[(par * 4 + 2) * 64 + h] + sump[(par * 4 + 3) * 64 + h];
         }
+        if (n == (uint32_t)CSA_TRACE_TILE && q4 == 0 && lane == 0) CSA_TRACE_MARK(13);
       }
       if (!ok) break;
       // ======================= item epilogue =======================
@@ -749,6 +767,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
         if (!mbar_wait(p_free, (n - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
       }
+      if (it == (int)blockIdx.x && q4 == 0 && lane == 0) CSA_TRACE_MARK(14);
       // per-head output scale into this warp's table
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -824,14 +843,17 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && j > 0) mbar_arrive(o_free);
+      if (it == (int)blockIdx.x && q4 == 0 && lane == 0) CSA_TRACE_MARK(15);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) CSA_TRACE_MARK(16);
   if (a.cl_reduce) attend_cluster_merge(a, smem, sE);
   if (warp == 8) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0) { CSA_TRACE_MARK(22); CSA_TRACE_WALL(21); }
 }
 
 // ----------------------------------------------------------------------------

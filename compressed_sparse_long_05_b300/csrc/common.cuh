@@ -20,6 +20,44 @@ enum : unsigned int {
 
 CSA_DEVINL void csa_flag_error(unsigned int bit) { atomicOr(&g_csa_error_word, bit); }
 
+CSA_DEVINL long long csa_globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return (long long)t;
+}
+
+// ----------------------------------------------------------------------------
+// Phase trace (built only into the traced library variant, -DCSA_TRACE): a
+// kernel marks the SM clock at its phase boundaries for CTAs below
+// CSA_TRACE_CTAS; the host reads the marks with csa_trace_read().  Marks
+// record, they change no work.
+// ----------------------------------------------------------------------------
+#ifdef CSA_TRACE
+namespace csa {
+constexpr int CSA_TRACE_CTAS = 160;
+constexpr int CSA_TRACE_SLOTS = 64;   // attention 0-23, index 24-39, top-k 40-55
+__device__ long long g_csa_trace[CSA_TRACE_CTAS][CSA_TRACE_SLOTS];
+__device__ int g_csa_trace_tile;   // which tile of a CTA the per-tile marks describe
+}  // namespace csa
+#define CSA_TRACE_TILE (csa::g_csa_trace_tile)
+#define CSA_TRACE_MARK(slot)                                                         \
+  do {                                                                               \
+    if (blockIdx.x < csa::CSA_TRACE_CTAS) {                                               \
+      long long c_;                                                                  \
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(c_));                           \
+      csa::g_csa_trace[blockIdx.x][(slot)] = c_;                                          \
+    }                                                                                \
+  } while (0)
+#define CSA_TRACE_WALL(slot)                                                         \
+  do {                                                                               \
+    if (blockIdx.x < csa::CSA_TRACE_CTAS) csa::g_csa_trace[blockIdx.x][(slot)] = csa_globaltimer(); \
+  } while (0)
+#else
+#define CSA_TRACE_MARK(slot) do {} while (0)
+#define CSA_TRACE_WALL(slot) do {} while (0)
+#define CSA_TRACE_TILE 0
+#endif
+
 // Absolute token position of query row `row` = b * Tq + i: q_pos[row] when the
 // caller passed positions, else i (causal prefill from token 0).
 CSA_DEVINL long long query_pos(const int32_t* q_pos, long long row, int i) {

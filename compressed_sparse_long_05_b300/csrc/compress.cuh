@@ -5,6 +5,9 @@
 // S = softmax over the entry's rows of (Z + bias).  CSA rows: a-rows of block
 // i and b-rows of block i-1 (none for i = 0); HCA rows: the block's m rows.
 //
+// Optional epilogue per entry: RMSNorm (§2.3.3) and RoPE of the last r dims
+// at the entry's position, so that the attention can take it pre-rotated.
+//
 // HBM streaming reduction: one CTA per compressed entry.  Thread (v, g) owns
 // one 16-byte channel vector v and visits rows g, g+G, ... with an online
 // softmax (running max, running sum, running weighted sum per channel); the G
@@ -45,6 +48,12 @@ struct CompressArgs {
   int overlap;      // 1 = CSA (b-rows of the previous block join), 0 = HCA
   int vecs;         // d / VEC
   int groups;       // row groups G (blockDim.x = vecs * groups)
+  // optional epilogue on each compressed entry (applied in this order):
+  int rms_norm;               // 1 = x / sqrt(mean(x^2) + eps) [* norm_weight]
+  const float* norm_weight;   // [d] or null
+  float norm_eps;
+  int rope_dims;              // r > 0: rotate the last r dims at the entry's position m(i+1)-1
+  RopeFreqs rf;
 };
 
 template <typename T>
@@ -94,30 +103,69 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
   }
 
   // merge the row groups: group 0 of each vector gathers the others
-  extern __shared__ float sm[];                  // [groups][vecs][3*VEC]
+  extern __shared__ float sm[];                  // [groups][vecs][3*VEC], then [vecs]
   float* mine = sm + ((size_t)g * a.vecs + v) * 3 * VEC;
 #pragma unroll
   for (int e = 0; e < VEC; ++e) {
     mine[e] = mx[e]; mine[VEC + e] = sum[e]; mine[2 * VEC + e] = acc[e];
   }
   __syncthreads();
-  if (g != 0) return;
-  for (int gg = 1; gg < a.groups; ++gg) {
-    const float* o = sm + ((size_t)gg * a.vecs + v) * 3 * VEC;
+  const bool owner = g == 0;                     // threads 0 .. vecs-1 hold the entry's channels
+  float res[VEC];
+  if (owner) {
+    for (int gg = 1; gg < a.groups; ++gg) {
+      const float* o = sm + ((size_t)gg * a.vecs + v) * 3 * VEC;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      float om = o[e];
-      if (om == -INFINITY) continue;             // group saw no rows
-      float nm = fmaxf(mx[e], om);
-      float s0 = __expf(mx[e] - nm), s1 = __expf(om - nm);
-      sum[e] = sum[e] * s0 + o[VEC + e] * s1;
-      acc[e] = acc[e] * s0 + o[2 * VEC + e] * s1;
-      mx[e] = nm;
+      for (int e = 0; e < VEC; ++e) {
+        float om = o[e];
+        if (om == -INFINITY) continue;           // group saw no rows
+        float nm = fmaxf(mx[e], om);
+        float s0 = __expf(mx[e] - nm), s1 = __expf(om - nm);
+        sum[e] = sum[e] * s0 + o[VEC + e] * s1;
+        acc[e] = acc[e] * s0 + o[2 * VEC + e] * s1;
+        mx[e] = nm;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) res[e] = acc[e] / sum[e];
+  }
+  if (a.rms_norm) {
+    // RMSNorm of the entry (DeepSeek-V4 report, Chinese translation, §2.3.3:
+    // the compressed entries are RMS-normalised before core attention).  Each
+    // owner's sum of squares goes to shared memory and every owner adds them
+    // in the same order, so the result does not depend on scheduling.
+    float* red = sm + (size_t)a.groups * a.vecs * 3 * VEC;   // [vecs]
+    if (owner) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) ss = fmaf(res[e], res[e], ss);
+      red[v] = ss;
+    }
+    __syncthreads();
+    if (owner) {
+      float tot = 0.f;
+      for (int w = 0; w < a.vecs; ++w) tot += red[w];
+      const float sc = rsqrtf(tot / (float)a.d + a.norm_eps);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e)
+        res[e] *= sc * (a.norm_weight ? __ldg(a.norm_weight + c0 + e) : 1.f);
     }
   }
-  float res[VEC];
+  if (!owner) return;
+  if (a.rope_dims > 0 && c0 >= a.d - a.rope_dims) {
+    // RoPE of the last r dims at the entry's position (the last token it
+    // summarises), so consumers can take the entry as already rotated
+    const long long pos = (long long)a.m * (i + 1) - 1;
+    const int j0 = (c0 - (a.d - a.rope_dims)) >> 1;
 #pragma unroll
-  for (int e = 0; e < VEC; ++e) res[e] = acc[e] / sum[e];
+    for (int p = 0; p < VEC / 2; ++p) {
+      float cs, sn;
+      rope_cos_sin(pos, a.rf.F[j0 + p], cs, sn);
+      const float x0 = res[2 * p], x1 = res[2 * p + 1];
+      res[2 * p] = x0 * cs - x1 * sn;
+      res[2 * p + 1] = x0 * sn + x1 * cs;
+    }
+  }
   T* out = reinterpret_cast<T*>(a.out) + ((size_t)b * a.N + i) * a.d + c0;
   V::store(out, res);
 }

@@ -16,6 +16,7 @@
 #include "index_tc.cuh"
 #include "index_fp4.cuh"
 #include "attend_tc.cuh"
+#include "gemm_tc.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -122,6 +123,21 @@ bool tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, uint
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor map with a full 3-D box, 128-byte swizzle, zero fill.
+bool tmap_bf16_3d_box(CUtensorMap* m, const void* base, const uint64_t dims_[3],
+                      const uint64_t strides_[2], const uint32_t box_[3]) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {dims_[0], dims_[1], dims_[2]};
+  cuuint64_t strides[2] = {strides_[0], strides_[1]};
+  cuuint32_t box[3] = {box_[0], box_[1], box_[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D byte tensor map (x fastest, 64-byte rows), 64-byte swizzle, zero fill.
 bool tmap_u8_3d_sw64(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, uint64_t z,
                      uint64_t y_stride, uint64_t z_stride, uint32_t box_y) {
@@ -216,10 +232,13 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
 template <int H, int C>
 csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, const int32_t* q_pos,
                              float* scores, int B, int Tq, int N, int m, uint32_t* hist,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, unsigned long long wait_ns = 0,
+                             int skip_load_plus1 = 0) {
   csa::IndexTcArgs a;
   memset(&a, 0, sizeof(a));
   a.w = w; a.scores = scores; a.q_pos = q_pos; a.B = B; a.Tq = Tq; a.N = N; a.m = m;
+  a.wait_ns = wait_ns;
+  a.skip_load_plus1 = skip_load_plus1;
   csa_status_t st = plan_index(a, 256 / H, B, Tq, N);
   if (st != CSA_OK) return st;
   const int sms = sm_count();
@@ -456,15 +475,24 @@ csa_status_t csa_device_error(void* stream) {
 }
 
 // ---------------------------------------------------------------------------
-csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const void* Zb,
-                          const float* Ba, const float* Bb, void* out, int B, int T, int d,
-                          int m, int dtype, void* stream) {
+csa_status_t csa_compress_ex(const void* Ca, const void* Cb, const void* Za, const void* Zb,
+                             const float* Ba, const float* Bb, void* out, int B, int T, int d,
+                             int m, int dtype, const csa_compress_opts_t* opts, void* stream) {
   const int overlap = (Cb != nullptr) ? 1 : 0;
   if ((Cb == nullptr) != (Zb == nullptr)) return CSA_ERR_INVALID_ARG;
   if (B < 0 || T < 0 || d <= 0 || m <= 0 || m > 4096) return CSA_ERR_INVALID_ARG;
   if (dtype != CSA_DT_F32 && dtype != CSA_DT_BF16) return CSA_ERR_UNSUPPORTED;
   const int vec = dtype == CSA_DT_BF16 ? 8 : 4;
   if (d % vec || d / vec > 256) return CSA_ERR_UNSUPPORTED;
+  csa_compress_opts_t o;
+  memset(&o, 0, sizeof(o));
+  if (opts) o = *opts;
+  if (o.rms_norm && (!(o.norm_eps >= 0.f) || (o.norm_weight && !aligned(o.norm_weight, 4))))
+    return CSA_ERR_INVALID_ARG;
+  if (o.rope_dims < 0 || (o.rope_dims & 1) || o.rope_dims > d || o.rope_dims > 128 ||
+      (o.rope_dims > 0 && !(o.rope_base > 0.f)))
+    return CSA_ERR_INVALID_ARG;
+  if (o.rope_dims % vec) return CSA_ERR_UNSUPPORTED;
   if (B == 0 || T / m == 0) return CSA_OK;   // nothing to compress (outputs may be empty)
   if (!Ca || !Za || !out) return CSA_ERR_INVALID_ARG;
   const void* ptrs[] = {Ca, Cb, Za, Zb, out};
@@ -472,11 +500,16 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
     if (p && !aligned(p, 16)) return CSA_ERR_INVALID_ARG;
   if ((Ba && !aligned(Ba, 4)) || (Bb && !aligned(Bb, 4))) return CSA_ERR_INVALID_ARG;
   const int N = T / m;
-  if (B == 0 || N == 0) return CSA_OK;
   csa::CompressArgs a;
+  memset(&a, 0, sizeof(a));
   a.Ca = Ca; a.Cb = Cb; a.Za = Za; a.Zb = Zb; a.Ba = Ba; a.Bb = Bb; a.out = out;
   a.B = B; a.T = T; a.d = d; a.m = m; a.N = N; a.overlap = overlap;
   a.vecs = d / vec;
+  a.rms_norm = o.rms_norm ? 1 : 0;
+  a.norm_weight = o.norm_weight;
+  a.norm_eps = o.norm_eps;
+  a.rope_dims = o.rope_dims;
+  if (o.rope_dims > 0) a.rf = make_rope(o.rope_dims, o.rope_base);
   int rows = overlap ? 2 * m : m;
   int groups = 256 / a.vecs;
   if (groups > rows) groups = rows;
@@ -484,7 +517,7 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
   a.groups = groups;
   dim3 grid(N, B);
   dim3 block(a.vecs * groups);
-  size_t smem = (size_t)groups * a.vecs * 3 * vec * sizeof(float);
+  size_t smem = ((size_t)groups * a.vecs * 3 * vec + a.vecs) * sizeof(float);
   {
     cudaError_t e = dtype == CSA_DT_BF16
                         ? launch_ex(csa::compress_kernel<__nv_bfloat16>, grid, block, smem, S(stream), 1, a)
@@ -492,6 +525,12 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
     if (e != cudaSuccess) return cuda_fail(e, "csa_compress launch");
   }
   return CSA_OK;
+}
+
+csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const void* Zb,
+                          const float* Ba, const float* Bb, void* out, int B, int T, int d,
+                          int m, int dtype, void* stream) {
+  return csa_compress_ex(Ca, Cb, Za, Zb, Ba, Bb, out, B, T, d, m, dtype, nullptr, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -545,6 +584,18 @@ csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const 
                        const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
                        int N, int H, int c, int m, int dtype, void* stream) {
   return index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, H, c, m, dtype, nullptr, stream);
+}
+
+csa_status_t csa_selftest_wait_timeout(const void* qI, const float* w, const void* K,
+                                       const int32_t* q_pos, float* scores, int B, int Tq, int N,
+                                       int m, int limit_us, void* stream) {
+  if (B <= 0 || Tq <= 0 || N <= 0 || m <= 0 || limit_us < 1 || limit_us > 2000000)
+    return CSA_ERR_INVALID_ARG;
+  if (!qI || !w || !K || !scores || !aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4) ||
+      !aligned(scores, 4) || (q_pos && !aligned(q_pos, 4)))
+    return CSA_ERR_INVALID_ARG;
+  return launch_index_tc<64, 128>(qI, w, K, q_pos, scores, B, Tq, N, m, nullptr, S(stream),
+                                  1000ull * (unsigned long long)limit_us, 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -669,6 +720,8 @@ csa_status_t attend_validate(const AttendCall& c, AttPlan* plan, bool* empty) {
     return CSA_ERR_INVALID_ARG;
   if (!c.dense && (c.k < 1 || c.k > 4096)) return CSA_ERR_INVALID_ARG;
   if (c.N > 0 && !c.ent.data) return CSA_ERR_INVALID_ARG;
+  if ((c.ent.flags & ~CSA_KV_ROTATED) || (c.win.flags & ~CSA_KV_ROTATED)) return CSA_ERR_INVALID_ARG;
+  if (c.win.flags) return CSA_ERR_UNSUPPORTED;   // window rows are stored unrotated
   if (c.B == 0 || c.Tq == 0) {
     *empty = true;
     return CSA_OK;
@@ -716,6 +769,7 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
     a.Tq = c.Tq; a.N = c.N; a.k = c.dense ? 0 : c.k; a.T_win = c.T_win;
     a.n_h = c.n_h; a.d = c.d; a.r = c.r; a.m = c.m; a.n_win = c.n_win;
     a.dense = c.dense;
+    a.ent_rotated = (c.ent.flags & CSA_KV_ROTATED) ? 1 : 0;
     a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
     a.rf = rf;
     const size_t smem = ((size_t)2 * c.n_h * c.d + c.d + 5 * c.n_h) * sizeof(float);
@@ -745,6 +799,7 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
   a.rotate_rows = p.rotate_rows; a.kv_mixed = mixed;
   a.cl_reduce = p.cl_reduce;
   a.rel_rope = p.rel_rope;
+  a.ent_rotated = (c.ent.flags & CSA_KV_ROTATED) ? 1 : 0;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.d));
   a.rf = rf;
   if (!p.rotate_rows) {
@@ -752,7 +807,7 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
     csa::RotateArgs ra;
     memset(&ra, 0, sizeof(ra));
     ra.rf = rf;
-    if (c.N > 0) {
+    if (c.N > 0 && !a.ent_rotated) {
       ra.src = reinterpret_cast<const __nv_bfloat16*>(c.ent.data);
       ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_ent);
       ra.rows = (long long)c.B * c.N; ra.rows_per_b = c.N; ra.m = c.m; ra.base = nullptr;
@@ -954,3 +1009,65 @@ extern "C" csa_status_t csa_attend_noalloc(const void* q, csa_kv_t entries, cons
   }
   return attend_launch(c, p, ws, stream);
 }
+
+// ---------------------------------------------------------------------------
+// csa_grouped_proj: the grouped output projection (and, with G = 1, the final
+// projection to the model width) as one tcgen05 GEMM per call.
+extern "C" csa_status_t csa_grouped_proj(const void* A, int64_t lda, const void* W, void* C,
+                                         int64_t ldc, int M, int N, int K, int G, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || G <= 0) return CSA_ERR_INVALID_ARG;
+  if (lda < (int64_t)G * K || ldc < (int64_t)G * N) return CSA_ERR_INVALID_ARG;
+  if (M == 0) return CSA_OK;
+  if (!A || !W || !C) return CSA_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16)) return CSA_ERR_INVALID_ARG;
+  // TMA strides are multiples of 16 bytes; the vector stores need 8-element rows
+  if (K % 8 || lda % 8 || ldc % 8 || N % 8) return CSA_ERR_UNSUPPORTED;
+  csa::GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.C = reinterpret_cast<__nv_bfloat16*>(C);
+  a.ldc = ldc;
+  a.M = M; a.N = N; a.K = K; a.G = G;
+  a.MT = (M + csa::GEMM_BM - 1) / csa::GEMM_BM;
+  a.NT = (N + csa::GEMM_BN - 1) / csa::GEMM_BN;
+  a.tiles = (long long)G * a.MT * a.NT;
+  CUtensorMap tmA, tmW;
+  const uint64_t dA[3] = {(uint64_t)K, (uint64_t)G, (uint64_t)M};
+  const uint64_t sA[2] = {(uint64_t)K * 2, (uint64_t)lda * 2};
+  const uint32_t bA[3] = {(uint32_t)csa::GEMM_BK, 1, (uint32_t)csa::GEMM_BM};
+  const uint64_t dW[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)G};
+  const uint64_t sW[2] = {(uint64_t)K * 2, (uint64_t)N * K * 2};
+  const uint32_t bW[3] = {(uint32_t)csa::GEMM_BK, (uint32_t)csa::GEMM_BN, 1};
+  if (!tmap_bf16_3d_box(&tmA, A, dA, sA, bA) || !tmap_bf16_3d_box(&tmW, W, dW, sW, bW))
+    return CSA_ERR_UNSUPPORTED;
+  const int smem = csa::GemmSmem::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(csa::gemm_grouped_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_grouped_proj attr");
+  const int sms = sm_count();
+  const int grid = a.tiles < sms ? (int)a.tiles : sms;
+  e = launch_ex(csa::gemm_grouped_kernel, dim3(grid), dim3(csa::GEMM_THREADS), smem, S(stream), 1,
+                tmA, tmW, a);
+  if (e != cudaSuccess) return cuda_fail(e, "csa_grouped_proj launch");
+  return CSA_OK;
+}
+
+#ifdef CSA_TRACE
+// Phase marks of the traced library variant: copies n <= CSA_TRACE_CTAS *
+// CSA_TRACE_SLOTS marks (row = CTA, column = slot) to host memory and clears them.
+extern "C" int csa_trace_read(long long* host, int n) {
+  const int cap = csa::CSA_TRACE_CTAS * csa::CSA_TRACE_SLOTS;
+  if (!host || n < 0) return -1;
+  if (n > cap) n = cap;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(host, csa::g_csa_trace, (size_t)n * sizeof(long long)) != cudaSuccess)
+    return -1;
+  static long long zeros[csa::CSA_TRACE_CTAS * csa::CSA_TRACE_SLOTS];
+  if (cudaMemcpyToSymbol(csa::g_csa_trace, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+  return n;
+}
+
+// Which tile of each CTA the attention kernel's per-tile marks describe (0 = first).
+extern "C" int csa_trace_set_tile(int tile) {
+  return cudaMemcpyToSymbol(csa::g_csa_trace_tile, &tile, sizeof(tile)) == cudaSuccess ? 0 : -1;
+}
+#endif

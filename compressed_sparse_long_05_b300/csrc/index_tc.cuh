@@ -44,6 +44,9 @@ struct IndexTcArgs {
   uint32_t tmem_cols;    // allocated TMEM columns (power of 2 >= nbuf * QT * H)
   int nbuf;              // accumulator buffers in tensor memory (2 or 4)
   uint32_t* hist;        // optional [B * Tq][IDX_HBINS] key-digit histograms (QT == 1), zeroed
+  // Failure-detection test hooks (zero in every normal launch):
+  unsigned long long wait_ns;   // limit of every wait in ns (0: WAIT_LIMIT_NS)
+  int skip_load_plus1;          // n > 0: CTA 0's producer leaves out its K-tile copy number n-1
 };
 
 // Key-digit histogram of the scores, built in the index epilogue for the
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(IDX_THREADS, 1)
 index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant__ CUtensorMap tm_q,
                 IndexTcArgs a) {
   const int NQH = a.QT * H;                      // MMA N
+  const uint64_t lim = a.wait_ns ? a.wait_ns : WAIT_LIMIT_NS;
   const IndexSmem<H, C> L(a.stages, NQH, a.hist != nullptr);
   const int S = L.S;
   extern __shared__ uint8_t smem_raw[];
@@ -185,6 +189,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t B_BYTES = (uint32_t)NQH * C * 2;
+  if (threadIdx.x == 0) { CSA_TRACE_WALL(24); CSA_TRACE_MARK(25); }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
@@ -210,6 +215,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
+  if (threadIdx.x == 0) CSA_TRACE_MARK(26);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -222,7 +228,11 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         const int ntl = x.jv - x.j0;
         auto load_a = [&](int j) -> bool {
           const uint32_t st = ia % S, ph = (ia / S) & 1;
-          if (!mbar_wait(empty + st, ph ^ 1, abort_flag)) return false;
+          if (!mbar_wait(empty + st, ph ^ 1, abort_flag, lim)) return false;
+          if (blockIdx.x == 0 && a.skip_load_plus1 == (int)ia + 1) {
+            ++ia;          // test hook: this stage never fills, its consumer's wait runs out
+            return true;
+          }
           mbar_arrive_expect_tx(full + st, L.A_BYTES);
 #pragma unroll
           for (int kc = 0; kc < L.KCH; ++kc)
@@ -235,18 +245,19 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         const int pre = min(ntl, S);
         for (int jj = 0; jj < pre && ok; ++jj) ok = load_a(x.j0 + jj);
         if (!ok) break;
-        if (nitem > 0 && !mbar_wait(b_free, (nitem - 1) & 1, abort_flag)) { ok = false; break; }
+        if (nitem > 0 && !mbar_wait(b_free, (nitem - 1) & 1, abort_flag, lim)) { ok = false; break; }
         mbar_arrive_expect_tx(b_full, B_BYTES);
         for (int kc = 0; kc < L.KCH; ++kc)
           tma_load_3d(sB + kc * (NQH * 128), &tm_q, b_full, kc * 64, x.t0 * H, x.b);
         b_issued = true;
+        if (nitem == 0) CSA_TRACE_MARK(27);
         ++nitem;
         for (int jj = pre; jj < ntl && ok; ++jj) ok = load_a(x.j0 + jj);
       }
       // drain copies still in flight before the CTA may exit
       for (uint32_t k = (ia > (uint32_t)S ? ia - S : 0); k < ia; ++k)
-        mbar_drain(full + (k % S), (k / S) & 1);
-      if (b_issued) mbar_drain(b_full, (nitem - 1) & 1);
+        mbar_drain(full + (k % S), (k / S) & 1, lim);
+      if (b_issued) mbar_drain(b_full, (nitem - 1) & 1, lim);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -257,12 +268,13 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
       for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
         const IdxItem x = idx_item(a, it);
         if (x.jv <= x.j0) continue;
-        if (!mbar_wait(b_full, nitem & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(b_full, nitem & 1, abort_flag, lim)) { ok = false; break; }
         for (int j = x.j0; j < x.jv; ++j) {
           const uint32_t st = ia % S, ph = (ia / S) & 1;
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
-          if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(full + st, ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag, lim)) { ok = false; break; }
+          if (!mbar_wait(full + st, ph, abort_flag, lim)) { ok = false; break; }
+          if (ia == 0) CSA_TRACE_MARK(28);
           tc_fence_after();
           const uint32_t aBase = smem_u32(sA + st * L.A_BYTES);
           const uint32_t bBase = smem_u32(sB);
@@ -279,11 +291,12 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           ++ia;
           ++iacc;
         }
+        CSA_TRACE_MARK(29);
         umma_commit(b_free);
         ++nitem;
       }
       umma_commit(mma_done);
-      mbar_drain(mma_done, 0);
+      mbar_drain(mma_done, 0, lim);
     }
   } else {
     // ---------------- epilogue (warps 2..9: two groups, alternate tiles) ----------------
@@ -311,7 +324,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
           ++iacc;
           if (!mine) continue;
-          if (!mbar_wait(acc_full + buf, aph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(acc_full + buf, aph, abort_flag, lim)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
           for (int qi = 0; qi < x.nq; ++qi) {
@@ -323,23 +336,27 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + buf);
+          if (ew == 0 && lane == 0) CSA_TRACE_MARK(iacc <= 2 ? 30 : 31);
         } else if ((j & 1) == grp) {
           for (int qi = 0; qi < x.nq; ++qi)
             if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
         }
       }
+      if (ew == 0 && lane == 0) CSA_TRACE_MARK(32);
       if (a.hist) {
         // both groups have added this item's scores: one group flushes (and clears)
         // the shared per-quarter histograms; the next item's adds wait for that.
         // Bounded waits: a warp that gave up still arrives, and the flag ends the rest.
         __syncwarp();
         if (lane == 0) mbar_arrive(epi_sync);
-        const bool s1 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
+        const bool s1 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag, lim));
         ++nsync;
+        if (ew == 0 && lane == 0) CSA_TRACE_MARK(33);
         if (ok && s1 && grp == 0) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
+        if (ew == 0 && lane == 0) CSA_TRACE_MARK(34);
         __syncwarp();
         if (lane == 0) mbar_arrive(epi_sync);
-        const bool s2 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
+        const bool s2 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag, lim));
         ++nsync;
         if (!s1 || !s2) ok = false;
       }
@@ -350,6 +367,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+  if (threadIdx.x == 0) { CSA_TRACE_MARK(36); CSA_TRACE_WALL(35); }
 }
 
 }  // namespace csa

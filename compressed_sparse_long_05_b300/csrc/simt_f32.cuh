@@ -59,6 +59,7 @@ struct AttendF32Args {
   const int32_t* win_base;         // [B] (null: 0)
   int Tq, N, k, T_win, n_h, d, r, m, n_win;
   int dense;        // 1 = HCA: every visible entry, idx unused
+  int ent_rotated;  // 1 = entries stored with their RoPE dims already rotated
   float inv_sqrt_d;
   RopeFreqs rf;
 };
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(ATT_F32_THREADS) attend_f32_kernel(AttendF32Ar
       if (s < 0) continue;                       // uniform across the block
       if (s >= a.N) { if (tid == 0) csa_flag_error(ERRBIT_BAD_INDEX); continue; }
       src = a.ent + ((size_t)b * a.N + s) * d;
-      pos = (long long)a.m * (s + 1) - 1;
+      pos = a.ent_rotated ? 0 : (long long)a.m * (s + 1) - 1;   // a turn by 0 leaves the row as stored
     } else {
       const long long tok = w0 + (jr - nsel);
       if (tok < wbase || tok >= wbase + a.T_win) {    // outside this batch row's window buffer

@@ -49,15 +49,17 @@ CSA_DEVINL uint64_t globaltimer_ns() {
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 // Bounded wait for phase `parity`.  Returns false (without waiting further) once
-// *abort is set by another role, or after WAIT_LIMIT_NS.
-CSA_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// *abort is set by another role, or after `limit_ns` (then it flags
+// ERRBIT_TIMEOUT and sets *abort itself).
+CSA_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         csa_flag_error(ERRBIT_TIMEOUT);
         *abort = 1;
         return false;
@@ -67,10 +69,10 @@ CSA_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
 }
 
 // Short bounded wait used on abort paths (drain copies in flight before exit).
-CSA_DEVINL void mbar_drain(uint64_t* bar, uint32_t parity) {
+CSA_DEVINL void mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns = WAIT_LIMIT_NS) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
+    if (globaltimer_ns() - t0 > limit_ns) return;
   }
 }
 

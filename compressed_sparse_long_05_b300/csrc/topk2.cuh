@@ -78,6 +78,7 @@ CSA_DEVINL int tk2_block_scan(int x, int* sh, int* total) {
 
 template <int NT, int CL, int BITS1>
 __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
+  if (threadIdx.x == 0) { CSA_TRACE_WALL(40); CSA_TRACE_MARK(41); }
   pdl_enter();
   constexpr int NW = NT / 32;
   constexpr int BINS1 = 1 << BITS1;
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
     for (int j = rank * (BINS1 / CL) + tid; j < (rank + 1) * (BINS1 / CL); j += NT) gh[j] = 0u;
   }
 
+  if (tid == 0) CSA_TRACE_MARK(42);
   // ---- 1. load the slice (every copy in flight at once), then keys + first-digit histogram ----
   {
     const bool vec = ((lo & 3) == 0) && ((reinterpret_cast<uintptr_t>(srow) & 15) == 0);
@@ -201,7 +203,11 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
     }
     int tot;
     const int above = tk2_block_scan<NT>(part, sh_scan, &tot);   // keys in bins above this thread's
-    if (above < a.k && above + part >= a.k) {
+    if (tot != vis) {
+      // the histogram does not count exactly the row's visible keys (a stale or
+      // partial caller-side histogram): no threshold is taken from it
+      if (tid == 0) sh_sel[0] = 0xfffffffeu;
+    } else if (above < a.k && above + part >= a.k) {
       int run = above;
 #pragma unroll
       for (int e = PER - 1; e >= 0; --e) {
@@ -216,10 +222,11 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
     }
     __syncthreads();
   }
-  if (sh_sel[0] == 0xffffffffu) {
-    // the histogram holds fewer than k keys: it does not describe these scores
-    // (only a broken caller-side histogram gets here).  Flag it and leave the
-    // row empty rather than select from a wrong threshold.
+  if (sh_sel[0] >= 0xfffffffeu) {
+    // the histogram does not describe these scores (its total is not the
+    // visible count, or it holds fewer than k keys; only a broken caller-side
+    // histogram gets here).  Flag it and leave the row empty rather than
+    // select from a wrong threshold.
     if (tid == 0 && rank == 0) csa_flag_error(ERRBIT_HIST);
     for (int j = rank * NT + tid; j < a.k; j += CL * NT) orow[j] = -1;
     if constexpr (CL > 1) cluster.sync();             // no rank leaves while peers may map its memory
@@ -227,6 +234,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   }
   const uint32_t b1 = sh_sel[0];
   uint32_t krem = sh_sel[1];
+  if (tid == 0) CSA_TRACE_MARK(43);
 
   // ---- 3. candidates: this slice's keys in bin b1 ----
   int ncand = 0;
@@ -262,6 +270,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   }
   const uint32_t* list = cand_ok ? cand : keys;
   const int list_n = cand_ok ? ncand : n;
+  if (tid == 0) CSA_TRACE_MARK(44);
 
   // ---- 4. three radix passes over the candidates (or the b1-filtered slice) ----
   uint32_t prefix = b1 << SHIFT1;
@@ -300,6 +309,10 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
       __syncthreads();
     }
     if (wid == 0) {
+      // every thread's reads of the previous pass's selection ended at the
+      // barrier above: mark "no digit found" before this pass selects
+      if (lane == 0) sh_sel[0] = 0xffffffffu;
+      __syncwarp();
       // lane l holds digits 4l..4l+3 (128 bins; unused high bins are zero)
       uint32_t c[4];
       uint32_t part = 0;
@@ -322,10 +335,19 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
       }
     }
     __syncthreads();
+    if (sh_sel[0] == 0xffffffffu) {
+      // fewer candidates than the histogram promised: same treatment as above
+      // (every rank merged the same counts, so the whole cluster leaves here)
+      if (tid == 0 && rank == 0) csa_flag_error(ERRBIT_HIST);
+      for (int j = rank * NT + tid; j < a.k; j += CL * NT) orow[j] = -1;
+      if constexpr (CL > 1) cluster.sync();
+      return;
+    }
     prefix |= sh_sel[0] << sh;
     pmask |= dmask << sh;
     krem = sh_sel[1];
   }
+  if (tid == 0) CSA_TRACE_MARK(45);
   const uint32_t T = prefix;          // exact k-th largest key
   const int q_eq = (int)krem;         // keys == T to take, lowest indices first
 
@@ -387,7 +409,9 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
     gt_before += __popc(gm);
     eq_before += __popc(em);
   }
+  if (tid == 0) CSA_TRACE_MARK(46);
   if constexpr (CL > 1) cluster.sync();   // peers may still read sh_tot / histograms
+  if (tid == 0) { CSA_TRACE_MARK(48); CSA_TRACE_WALL(47); }
 }
 
 }  // namespace csa

@@ -23,6 +23,7 @@ class Buffers:
 
     def __init__(self):
         self.entries = None
+        self.K = None
         self.scores = None
         self.idx = None
         self.out = None
@@ -42,10 +43,30 @@ def _win_arg(x):
     return (x["win_nope"], x["win_scale"], x["win_rope"])
 
 
-def _indexer_args(x):
+def _indexer_args(x, buf=None):
+    if "CIa" in x:                      # keys compressed from raw index rows
+        return x["qI"], None, buf.K, None
     if "qI" in x:
         return x["qI"], None, x["K"], None
     return x["qI_fp4"], x["qI_sf"], x["K_fp4"], x["K_sf"]
+
+
+def compress_stage(cfg: dict, x: dict, buf: Buffers):
+    """Prefill compression: the entries (CSA m overlapped, HCA m' plain), with
+    the workload's optional RMSNorm and RoPE pre-rotation, and, when the
+    workload gives raw index rows, the indexer keys K^IComp (same overlapped
+    compression at d = c_I; DeepSeek-V4 report, Chinese translation, §2.3.1)."""
+    m, r = cfg["m"], cfg["r"]
+    opts = dict(rms_norm=bool(cfg.get("entry_norm")), norm_eps=cfg.get("entry_norm_eps", 0.0),
+                rope_dims=r if cfg.get("entry_rope") else 0, rope_base=cfg["rope_base"])
+    if cfg["kind"] == "csa_prefill":
+        buf.entries = L.csa_compress(x["Ca"], x["Za"], m, Cb=x["Cb"], Zb=x["Zb"], out=buf.entries,
+                                     **opts)
+        if "CIa" in x:
+            buf.K = L.csa_compress(x["CIa"], x["ZIa"], m, Cb=x["CIb"], Zb=x["ZIb"], out=buf.K)
+    else:
+        buf.entries = L.csa_compress(x["C"], x["Z"], m, out=buf.entries, **opts)
+    return buf.entries
 
 
 def forward(cfg: dict, x: dict, buf: Buffers | None = None):
@@ -54,17 +75,14 @@ def forward(cfg: dict, x: dict, buf: Buffers | None = None):
     kind = cfg["kind"]
     m, r, n_win = cfg["m"], cfg["r"], cfg["n_win"]
     q_pos, win_base, base = x["q_pos"], x["win_base"], cfg["rope_base"]
-    if kind == "csa_prefill":
-        buf.entries = L.csa_compress(x["Ca"], x["Za"], m, Cb=x["Cb"], Zb=x["Zb"], out=buf.entries)
-        entries = buf.entries
-    elif kind == "hca_prefill":
-        buf.entries = L.csa_compress(x["C"], x["Z"], m, out=buf.entries)
-        entries = buf.entries
+    rot = bool(cfg.get("entry_rope"))
+    if kind.endswith("prefill"):
+        entries = compress_stage(cfg, x, buf)
     else:
         entries = _entries_arg(x)
     win = _win_arg(x)
     if kind.startswith("csa"):
-        qI, qI_sf, K, K_sf = _indexer_args(x)
+        qI, qI_sf, K, K_sf = _indexer_args(x, buf)
         buf.scores, buf.idx, buf.ws_topk = L.csa_index_topk(
             qI, x["w"], K, cfg["k"], m, q_pos, qI_sf=qI_sf, K_sf=K_sf, scores=buf.scores,
             idx=buf.idx, ws=buf.ws_topk)
@@ -72,14 +90,28 @@ def forward(cfg: dict, x: dict, buf: Buffers | None = None):
             n = L.attend_workspace_size(x["q"], entries, win, cfg["k"], m, n_win, r, False)
             buf.ws = L._workspace(None, n, x["q"].device)
         buf.out = L.csa_attend(x["q"], entries, buf.idx, win, x["sink"], m, n_win, win_base,
-                               q_pos, r, base, out=buf.out, ws=buf.ws)
+                               q_pos, r, base, out=buf.out, ws=buf.ws, entries_rotated=rot)
     else:
         if buf.ws is None:
             n = L.attend_workspace_size(x["q"], entries, win, 0, m, n_win, r, True)
             buf.ws = L._workspace(None, n, x["q"].device)
         buf.out = L.hca_attend(x["q"], entries, win, x["sink"], m, n_win, win_base, q_pos, r,
-                               base, out=buf.out, ws=buf.ws)
+                               base, out=buf.out, ws=buf.ws, entries_rotated=rot)
     return buf.out
+
+
+def output_projection(out, W_groups, W_out, y=None, z=None):
+    """The grouped output projection after the core attention (DeepSeek-V4
+    report, Chinese translation, §2.3.1 "分组输出投影"): the [B, Tq, n_h, d]
+    attention output, viewed as [B*Tq, n_h*d], is split into g groups of
+    (n_h/g)*d columns, group j is projected by W_groups[j] ([d_g, (n_h/g)*d])
+    to d_g dims, and the concatenated [B*Tq, g*d_g] result is projected by
+    W_out ([1, d_model, g*d_g]) to the model width.  Returns z [B*Tq, d_model];
+    y and z may be supplied for reuse."""
+    B, Tq, n_h, d = out.shape
+    A = out.reshape(B * Tq, n_h * d)
+    y = L.csa_grouped_proj(A, W_groups, C=y)
+    return L.csa_grouped_proj(y, W_out, C=z)
 
 
 def compress_entry(i: int, m: int, Ca, Za, Cb=None, Zb=None, Ba=None, Bb=None):

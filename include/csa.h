@@ -71,9 +71,15 @@ typedef enum {
 /* A set of key=value rows (compressed entries or raw window tokens).
  *   dtype F32 / BF16 : data = [B, rows, d]; scale, rope unused.
  *   dtype E4M3_BF16ROPE : data = e4m3 [B, rows, d-r], scale = float32 [B, rows],
- *                         rope = bf16 [B, rows, r]. */
+ *                         rope = bf16 [B, rows, r].
+ *   flags: 0, or CSA_KV_ROTATED for compressed entries whose last r dims are
+ *          already rotated at their own position m*(s+1)-1 (csa_compress_ex
+ *          with rope_dims = r writes them so); the attention then does not
+ *          rotate them again.  Window rows are always stored unrotated. */
+#define CSA_KV_ROTATED 1
 typedef struct {
   int32_t dtype;
+  int32_t flags;
   const void* data;
   const float* scale;
   const void* rope;
@@ -94,6 +100,32 @@ typedef struct {
 csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const void* Zb,
                           const float* Ba, const float* Bb, void* out, int B, int T, int d,
                           int m, int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_compress_ex — csa_compress with an optional epilogue on every
+ * compressed entry, applied in this order (the producer side of the path):
+ *   1. rms_norm: entry / sqrt(mean_c(entry^2) + norm_eps), times norm_weight
+ *      ([d] float32 device, NULL = 1) — §2.3.3: the compressed KV entries are
+ *      RMS-normalised before core attention;
+ *   2. rope_dims = r > 0: the last r dims rotated by RoPE (interleaved pairs,
+ *      theta_j = rope_base^(-2j/r)) at the entry's position m*(i+1)-1, so the
+ *      attention can take the entries pre-rotated (CSA_KV_ROTATED).
+ * opts is a HOST pointer (NULL = no epilogue, the same as csa_compress).
+ * The same call with d = c_I compresses the indexer keys (K^IComp of §2.3.1).
+ * rope_dims must be even, <= min(d, 128), and a multiple of 8 (BF16) or 4
+ * (F32).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t rms_norm;
+  float norm_eps;
+  const float* norm_weight;
+  int32_t rope_dims;
+  float rope_base;
+} csa_compress_opts_t;
+
+csa_status_t csa_compress_ex(const void* Ca, const void* Cb, const void* Za, const void* Zb,
+                             const float* Ba, const float* Bb, void* out, int B, int T, int d,
+                             int m, int dtype, const csa_compress_opts_t* opts, void* stream);
 
 /* ---------------------------------------------------------------------------
  * csa_index — lightning-indexer scores (§2.3.1 "Lightning Indexer"):
@@ -217,6 +249,45 @@ csa_status_t csa_attend_noalloc(const void* q, csa_kv_t entries, const int32_t* 
                                 const int32_t* q_pos, const int32_t* win_base, const float* sink,
                                 void* out, int B, int Tq, int N, int k, int T_win, int n_h, int d,
                                 int r, int m, int n_win, float rope_base, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_grouped_proj — the grouped output projection (§2.3.1 "分组输出投影":
+ * the n_h head outputs are split into g groups, each group is projected to a
+ * d_g-dimensional intermediate output, and those are projected to the model
+ * width d; §4.2.1: V4-Pro g = 16, d_g = 1024, d = 7168).  One call computes,
+ * for every group j < G,
+ *     C[:, j*N : (j+1)*N] = A[:, j*K : (j+1)*K] * W[j]^T
+ * in bf16 with float32 accumulation, rounded once to bf16:
+ *   A: [M, lda] bf16 (the attention output [tokens, n_h * d] has lda = n_h*d
+ *      and, split into G = g groups, K = (n_h / g) * d);
+ *   W: [G, N, K] bf16, each group's weight output-major (row n holds the K
+ *      weights of output n);
+ *   C: [M, ldc] bf16.
+ * The final projection is the same call with G = 1, K = g * d_g, N = d.
+ * Requires K, N, lda, ldc multiples of 8, lda >= G*K, ldc >= G*N, 16-byte
+ * aligned pointers.  Tensor-core tiles of 128 x 256 outputs; M, N and K need
+ * not be multiples of the tile.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_grouped_proj(const void* A, int64_t lda, const void* W, void* C, int64_t ldc,
+                              int M, int N, int K, int G, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_selftest_wait_timeout — a test of the library's failure detection; the
+ * pages define no such call.  It runs the BF16 index kernel exactly as
+ * csa_index (H = 64, c = 128, same arguments) but with a fault planted by
+ * the host: CTA 0's TMA producer leaves out its first K-tile copy, and every
+ * wait of the launch gives up after limit_us microseconds (1 .. 2000000; a
+ * normal launch waits up to 2 s).  The MMA issuer's wait on the missing tile
+ * runs out; it sets the timeout bit of the device error word and raises its
+ * CTA's abort flag; the other roles leave their loops, copies already issued
+ * are waited for, tensor memory is freed and the kernel returns, leaving the
+ * context usable.  The scores are then undefined.  csa_device_error()
+ * afterwards returns CSA_ERR_TIMEOUT (and clears the word).  The query rows
+ * must see at least one entry, or no copy is issued at all.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_selftest_wait_timeout(const void* qI, const float* w, const void* K,
+                                       const int32_t* q_pos, float* scores, int B, int Tq, int N,
+                                       int m, int limit_us, void* stream);
 
 /* Reads and clears the sticky device error word (synchronises `stream`).
  * Returns CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE. */

@@ -142,6 +142,15 @@ def compress_hca(C, Z, m: int, Bias=None) -> np.ndarray:
     return out
 
 
+def rms_norm(x, weight=None, eps: float = 0.0) -> np.ndarray:
+    """RMSNorm of each vector along the last axis: x / sqrt(mean(x^2) + eps),
+    times an optional per-channel weight ([uika] §2.3.3: the compressed KV
+    entries, and each query head, are RMS-normalised before core attention)."""
+    x = np.asarray(x, dtype=np.float64)
+    y = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return y if weight is None else y * np.asarray(weight, dtype=np.float64)
+
+
 # ----------------------------------------------------------------------------
 # 2. lightning indexer  ([uika] §2.3.1 "Lightning Indexer"; [notes] 关键设计 1)
 # ----------------------------------------------------------------------------
@@ -275,3 +284,22 @@ def hca_attend_token(q, t: int, entries, win, win_base: int, sink, m: int,
     rows = np.concatenate([ent[s], wrows], axis=0)
     pos = np.concatenate([entry_position(s, m), wpos])
     return attend_rows(q, t, rows, pos, sink, r, base)
+
+
+# ----------------------------------------------------------------------------
+# 5. grouped output projection  ([uika] §2.3.1 "分组输出投影"; §4.2.1 g, d_g)
+# ----------------------------------------------------------------------------
+
+
+def grouped_projection(A, W) -> np.ndarray:
+    """Group j of the columns of A times its own weight: the n_h head outputs
+    split into G groups, each projected to N = d_g dims.
+
+    A [M, >= G*K]; W [G, N, K] (row n of W[j] holds output n's weights).
+    Returns [M, G*N] with columns j*N .. (j+1)*N - 1 = A[:, j*K:(j+1)*K] @ W[j]^T.
+    The final projection to the model width is the same with G = 1.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    G, N, K = W.shape
+    return np.concatenate([A[:, j * K:(j + 1) * K] @ W[j].T for j in range(G)], axis=1)

@@ -15,12 +15,18 @@ from . import csa_oracle as O
 
 
 def entries_of(cfg: dict, x: dict, b: int) -> np.ndarray:
-    """Compressed entries of batch row b, float64 [N, d]."""
+    """Compressed entries of batch row b, float64 [N, d] (unrotated).
+
+    Prefill workloads compress the raw rows; with cfg["entry_norm"] each
+    compressed entry is then RMS-normalised with eps cfg["entry_norm_eps"]
+    ([uika] §2.3.3)."""
     kind = cfg["kind"]
-    if kind == "csa_prefill":
-        return O.compress_csa(x["Ca"][b], x["Cb"][b], x["Za"][b], x["Zb"][b], cfg["m"])
-    if kind == "hca_prefill":
-        return O.compress_hca(x["C"][b], x["Z"][b], cfg["m"])
+    if kind in ("csa_prefill", "hca_prefill"):
+        if kind == "csa_prefill":
+            ent = O.compress_csa(x["Ca"][b], x["Cb"][b], x["Za"][b], x["Zb"][b], cfg["m"])
+        else:
+            ent = O.compress_hca(x["C"][b], x["Z"][b], cfg["m"])
+        return O.rms_norm(ent, eps=cfg["entry_norm_eps"]) if cfg.get("entry_norm") else ent
     if "entries" in x:
         return np.asarray(x["entries"][b], dtype=np.float64)
     return O.decode_mixed_entries(x["ent_nope"][b], x["ent_scale"][b], x["ent_rope"][b])
@@ -32,9 +38,16 @@ def window_of(x: dict, b: int) -> np.ndarray:
     return O.decode_mixed_entries(x["win_nope"][b], x["win_scale"][b], x["win_rope"][b])
 
 
-def indexer_inputs(x: dict, b: int, rows):
-    """(qI [len(rows), H, c], K [N, c]) of batch row b, float64."""
-    if "qI" in x:
+def indexer_inputs(x: dict, b: int, rows, m: int = 4):
+    """(qI [len(rows), H, c], K [N, c]) of batch row b, float64.
+
+    With raw per-token indexer keys (CIa, CIb, ZIa, ZIb) the keys are their
+    overlapped compression, K^IComp of [uika] §2.3.1 ([notes] 关键设计 1:
+    the index keys go through the same weighted overlap compression)."""
+    if "CIa" in x:
+        qI = np.asarray(x["qI"][b][rows], dtype=np.float64)
+        K = O.compress_csa(x["CIa"][b], x["CIb"][b], x["ZIa"][b], x["ZIb"][b], m)
+    elif "qI" in x:
         qI = np.asarray(x["qI"][b][rows], dtype=np.float64)
         K = np.asarray(x["K"][b], dtype=np.float64)
     else:
@@ -65,7 +78,7 @@ def run_rows(cfg: dict, x: dict, b: int, rows, selected=None, entries=None):
     res = {"t": t_pos}
     outs = []
     if cfg["kind"].startswith("csa"):
-        qI, K = indexer_inputs(x, b, rows)
+        qI, K = indexer_inputs(x, b, rows, m)
         w = np.asarray(x["w"][b][rows], dtype=np.float64)
         scores = O.index_scores(qI, w, K, t_pos, m)
         res["scores"] = scores

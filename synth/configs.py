@@ -47,6 +47,16 @@ WORKLOADS = {
         kind="csa_decode", dtype="bf16", B=4, L=131072, m=4, d=512, r=64,
         n_h=64, H_I=64, c_I=128, k=512, n_win=128, w_scale=1.0 / 64,
         qk_scale=128 ** -0.5),
+    # the producer side of the CSA prefill (same report, §2.3.1: the indexer
+    # keys K^IComp are the overlapped compression of per-token index rows;
+    # §2.3.3: compressed entries are RMS-normalised before core attention):
+    # keys compressed from raw rows, entries RMS-normalised (eps 1e-6, no
+    # weight: the pages give neither) and stored pre-rotated at compression
+    "csa_prefill_32k_producer": dict(
+        kind="csa_prefill", dtype="bf16", B=1, T=32768, m=4, d=512, r=64,
+        n_h=128, H_I=64, c_I=128, k=1024, n_win=128, w_scale=1.0 / 64,
+        qk_scale=128 ** -0.5, index_keys="compressed", entry_norm=True,
+        entry_norm_eps=1e-6, entry_rope=True),
     "csa_prefill_flash_32k": dict(
         kind="csa_prefill", dtype="bf16", B=1, T=32768, m=4, d=512, r=64,
         n_h=64, H_I=64, c_I=128, k=512, n_win=128, w_scale=1.0 / 64,

@@ -8,7 +8,9 @@ name and seed):
   N(0,1) in float32, then each vector divided by its RMS, then stored in the
   workload dtype;
 * compression logits Z^a, Z^b, Z: N(0,1);
-* indexer queries and keys: N(0,1) * qk_scale (1/sqrt(c_I));
+* indexer queries and keys: N(0,1) * qk_scale (1/sqrt(c_I)); workloads whose
+  keys are compressed from raw rows get those rows (CIa, CIb ~ N(0,1) *
+  qk_scale) and their compression logits (ZIa, ZIb ~ N(0,1)) instead;
 * indexer head weights w: U(0,1) * w_scale;
 * per-head sink logits z'_h: N(0,1);
 * query positions q_pos [B, Tq] and window-buffer bases win_base [B] (int32)
@@ -183,13 +185,24 @@ def make_inputs(cfg: dict, seed: int = 0, device="cpu") -> dict:
         H, c = cfg["H_I"], cfg["c_I"]
         qI = normal((B, Tq, H, c), torch.float32 if mixed else dt, device, g("qI"),
                     scale=cfg["qk_scale"])
-        K = normal((B, N, c), torch.float32 if mixed else dt, device, g("K"),
-                   scale=cfg["qk_scale"])
+        if cfg.get("index_keys") == "compressed":
+            # raw per-token index rows; the keys are their overlapped compression
+            T = cfg["T"]
+            for nm in ("CIa", "CIb"):
+                out[nm] = normal((B, T, c), dt, device, g(nm), scale=cfg["qk_scale"])
+            for nm in ("ZIa", "ZIb"):
+                out[nm] = normal((B, T, c), dt, device, g(nm))
+            K = None
+        else:
+            K = normal((B, N, c), torch.float32 if mixed else dt, device, g("K"),
+                       scale=cfg["qk_scale"])
         if mixed:
             out["qI_fp4"], out["qI_sf"] = quantise_fp4_blocks(qI)
             out["K_fp4"], out["K_sf"] = quantise_fp4_blocks(K)
         else:
-            out["qI"], out["K"] = qI, K
+            out["qI"] = qI
+            if K is not None:
+                out["K"] = K
         out["w"] = uniform((B, Tq, H), torch.float32, device, g("w"), scale=cfg["w_scale"])
 
     if kind == "csa_prefill":

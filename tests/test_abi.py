@@ -62,7 +62,7 @@ def test_host_side_argument_errors(L):
     assert L.csa_topk(fake, mis, fake, 1, 1, 100, 5, 4, None) == 1
     # index: null scores
     assert L.csa_index(fake, None, fake, fake, None, None, None, 1, 1, 8, 4, 32, 4, 0, None) == 1
-    kv = KV(1, 0x10000, None, None)
+    kv = KV(dtype=1, flags=0, data=0x10000)
     # attend: odd rope dims
     assert L.csa_attend(fake, kv, fake, kv, None, None, fake, fake, 1, 1, 8, 4, 128, 128, 512, 63,
                         4, 128, 10000.0, None, 0, None) == 1

@@ -40,8 +40,13 @@ def _np(t):
 
 
 def _entries(cfg, x, buf, b):
+    """The compressed entries the GPU attention used, float64 and unrotated."""
     if cfg["kind"].endswith("prefill"):
-        return f64(buf.entries[b])
+        e = f64(buf.entries[b])
+        if cfg.get("entry_rope"):           # stored rotated at m(s+1)-1: turn them back
+            e = O.rope_rotate(e, -O.entry_position(np.arange(e.shape[0]), cfg["m"]), cfg["r"],
+                              cfg["rope_base"])
+        return e
     if "entries" in x:
         return f64(x["entries"][b])
     return O.decode_mixed_entries(_np(x["ent_nope"][b]), _np(x["ent_scale"][b]), f64(x["ent_rope"][b]))
@@ -53,8 +58,11 @@ def _window(x, b):
     return O.decode_mixed_entries(_np(x["win_nope"][b]), _np(x["win_scale"][b]), f64(x["win_rope"][b]))
 
 
-def _indexer(x, b, i):
-    """(q [H, c], K [N, c]) float64 for query row i of batch row b."""
+def _indexer(x, b, i, buf=None):
+    """(q [H, c], K [N, c]) float64 for query row i of batch row b (the keys
+    the GPU indexed: its own compression when the workload compresses them)."""
+    if "CIa" in x:
+        return f64(x["qI"][b, i]), f64(buf.K[b])
     if "qI" in x:
         return f64(x["qI"][b, i]), f64(x["K"][b])
     q = O.decode_fp4_blocks(_np(x["qI_fp4"][b, i]), _np(x["qI_sf"][b, i]))
@@ -88,9 +96,15 @@ def _check_workload(K, name, batch_rows=None):
         ent = _entries(cfg, x, buf, b)
         if cfg["kind"] == "csa_prefill":
             probe = [0, 1, 2, cfg["N"] // 2, cfg["N"] - 1]
-            ref = O.compress_csa(f64(x["Ca"][b, : m * (max(probe) + 1)]), f64(x["Cb"][b, : m * (max(probe) + 1)]),
-                                 f64(x["Za"][b, : m * (max(probe) + 1)]), f64(x["Zb"][b, : m * (max(probe) + 1)]), m)
+            ref = O.compress_csa(f64(x["Ca"][b]), f64(x["Cb"][b]), f64(x["Za"][b]), f64(x["Zb"][b]), m)
+            if cfg.get("entry_norm"):
+                ref = O.rms_norm(ref, eps=cfg["entry_norm_eps"])
             assert_close(ent[probe], ref[probe], TOL_BF16, TOL_BF16, f"{name} compress")
+            if "CIa" in x:
+                kref = O.compress_csa(f64(x["CIa"][b]), f64(x["CIb"][b]), f64(x["ZIa"][b]),
+                                      f64(x["ZIb"][b]), m)
+                assert_close(f64(buf.K[b])[probe], kref[probe], TOL_BF16, TOL_BF16,
+                             f"{name} indexer-key compress")
         if cfg["kind"] == "hca_prefill":
             probe = [0, 1, cfg["N"] // 2, cfg["N"] - 1]
             ref = O.compress_hca(f64(x["C"][b]), f64(x["Z"][b]), m)
@@ -101,7 +115,7 @@ def _check_workload(K, name, batch_rows=None):
             t = int(x["q_pos"][b, i])
             q = f64(x["q"][b, i])
             if cfg["kind"].startswith("csa"):
-                qI, Kc = _indexer(x, b, i)
+                qI, Kc = _indexer(x, b, i, buf)
                 ref_s = O.index_scores(qI[None], f64(x["w"][b, i])[None], Kc, np.array([t]), m)[0]
                 got_s = f64(buf.scores[b, i])
                 assert_scores_close(got_s, ref_s, f"{name} scores b={b} i={i}")
@@ -146,3 +160,9 @@ def test_csa_decode_flash_128k_full(K):
 
 def test_csa_prefill_flash_32k_full(K):
     _check_workload(K, "csa_prefill_flash_32k")
+
+
+def test_csa_prefill_32k_producer_full(K):
+    # indexer keys compressed from raw index rows, entries RMS-normalised and
+    # stored pre-rotated by the compression epilogue
+    _check_workload(K, "csa_prefill_32k_producer")

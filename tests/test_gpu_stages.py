@@ -443,3 +443,101 @@ def test_compress_entry_matches_whole_sequence(K, kind, m, T, ents):
             got = P.compress_entry(i, m, Ca, Za, Cb=Cb, Zb=Zb)
             torch.cuda.synchronize()
             assert_close(f64(got[b]), ref[i], TOL_BF16, TOL_BF16, f"{kind} entry {i} b={b}")
+
+
+# ----------------------------------------------------------------------------
+# producer side: RMSNorm and RoPE pre-rotation in the compression epilogue,
+# attention on pre-rotated entries, indexer keys compressed at d = c_I
+# ----------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("B,T,d,m,overlap,norm,weight,rope", [
+    (2, 1037, 512, 4, True, True, False, 64),     # CSA, V4 entry shape, ragged tail
+    (1, 999, 512, 128, False, True, True, 64),    # HCA, weighted RMSNorm
+    (1, 515, 128, 4, True, False, False, 0),      # indexer keys: d = c_I, plain
+    (1, 300, 64, 4, True, True, False, 0),        # small d: partial last warp
+    (1, 260, 128, 1, False, True, False, 32),     # m = 1
+])
+def test_compress_epilogue(K, dtype, B, T, d, m, overlap, norm, weight, rope):
+    Ca, Za = _randn((B, T, d), dtype, 150), _randn((B, T, d), dtype, 151)
+    Cb = _randn((B, T, d), dtype, 152) if overlap else None
+    Zb = _randn((B, T, d), dtype, 153) if overlap else None
+    w = (torch.rand((d,), generator=_gen(154), device=DEV) + 0.5) if weight else None
+    eps = 1e-6
+    out = K.csa_compress(Ca, Za, m, Cb=Cb, Zb=Zb, rms_norm=norm, norm_eps=eps, norm_weight=w,
+                         rope_dims=rope)
+    torch.cuda.synchronize()
+    K.device_error()
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    for b in range(B):
+        if overlap:
+            ref = O.compress_csa(f64(Ca[b]), f64(Cb[b]), f64(Za[b]), f64(Zb[b]), m)
+        else:
+            ref = O.compress_hca(f64(Ca[b]), f64(Za[b]), m)
+        if norm:
+            ref = O.rms_norm(ref, None if w is None else f64(w), eps)
+        if rope:
+            ref = O.rope_rotate(ref, O.entry_position(np.arange(ref.shape[0]), m), rope, 1e4)
+        assert_close(f64(out[b]), ref, tol, tol, f"compress epilogue b={b}")
+
+
+def test_compress_epilogue_rejects_bad_options(K):
+    Ca, Za = _randn((1, 64, 128), torch.bfloat16, 155), _randn((1, 64, 128), torch.bfloat16, 156)
+    from compressed_sparse_long_05_b300 import CsaError
+    with pytest.raises(CsaError):
+        K.csa_compress(Ca, Za, 4, rope_dims=12)      # not a multiple of the 8-element vector
+    with pytest.raises(CsaError):
+        K.csa_compress(Ca, Za, 4, rope_dims=7)       # odd
+
+
+@pytest.mark.parametrize("case", ["decode", "prefill", "hca_decode", "f32"])
+def test_attend_pre_rotated_entries(K, case):
+    # entries stored rotated at their positions (compression epilogue) give the
+    # oracle's attention over the unrotated entries: decode rotates each
+    # gathered row by -t only, prefill skips its rotation pre-pass for them
+    d, r, m = 512, 64, 4
+    n_h, n_win, dt = 128, 128, torch.bfloat16
+    if case == "decode":
+        B, Tq, T, k = 2, 1, 12000, 1024
+    elif case == "prefill":
+        B, Tq, T, k = 1, 600, 600, 64
+    elif case == "hca_decode":
+        B, Tq, T, k, m = 2, 1, 128 * 900, 0, 128
+    else:
+        B, Tq, T, k, d, r, n_h, n_win, dt = 1, 200, 200, 16, 128, 32, 4, 16, torch.float32
+    Ca, Za = _rms((B, T, d), 160).to(dt), _randn((B, T, d), dt, 161)
+    if m == 4:
+        Cb, Zb = _rms((B, T, d), 162).to(dt), _randn((B, T, d), dt, 163)
+    else:
+        Cb = Zb = None
+    ent_rot = K.csa_compress(Ca, Za, m, Cb=Cb, Zb=Zb, rope_dims=r)
+    ent = K.csa_compress(Ca, Za, m, Cb=Cb, Zb=Zb)
+    N = T // m
+    q_pos0 = T - Tq
+    T_win = n_win + Tq if Tq == 1 else T
+    win_base = T - T_win
+    q = _rms((B, Tq, n_h, d), 164).to(dt)
+    win = _rms((B, T_win, d), 165).to(dt)
+    sink = torch.randn((n_h,), generator=_gen(166), device=DEV)
+    if k:
+        scores = torch.rand((B, Tq, N), generator=_gen(167), device=DEV)
+        idx = K.csa_topk(scores, k, m, q_pos0)
+        out = K.csa_attend(q, ent_rot, idx, win, sink, m, n_win, win_base, q_pos0, r,
+                           entries_rotated=True)
+    else:
+        out = K.hca_attend(q, ent_rot, win, sink, m, n_win, win_base, q_pos0, r, entries_rotated=True)
+    torch.cuda.synchronize()
+    K.device_error()
+    tol = TOL_F32 if dt == torch.float32 else TOL_BF16
+    for b in range(B):
+        e64, w64 = f64(ent[b]), f64(win[b])
+        for i in sorted({0, Tq // 2, Tq - 1}):
+            t = q_pos0 + i
+            if k:
+                ref = O.csa_attend_token(f64(q[b, i]), t, e64, idx[b, i].cpu().numpy(), w64, win_base,
+                                         f64(sink), m, n_win, r, 1e4)
+            else:
+                ref = O.hca_attend_token(f64(q[b, i]), t, e64, w64, win_base, f64(sink), m, n_win, r,
+                                         1e4)
+            assert_close(f64(out[b, i]), ref, tol, tol, f"{case} b={b} i={i}")

@@ -363,3 +363,57 @@ def test_decode_e2m1_table_and_packing():
     assert got.shape == (1, 32)
     assert got[0, :4].tolist() == [0.5, 1.0, 6.0, -6.0]
     assert got[0, 16] == 1.0 and got[0, 17] == 0.0
+
+
+# ----------------------------------------------------------------------------
+# RMSNorm of the compressed entries ([uika] §2.3.3)
+# ----------------------------------------------------------------------------
+
+
+def test_rms_norm_unit_rms_same_direction():
+    x = rnd(7, 33) * np.exp(rnd(7, 1))           # rows of very different scales
+    y = O.rms_norm(x)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(y / np.linalg.norm(y, axis=-1, keepdims=True),
+                               x / np.linalg.norm(x, axis=-1, keepdims=True), rtol=1e-13)
+    np.testing.assert_allclose(O.rms_norm(3.7 * x), y, rtol=1e-13)     # scale invariant
+
+
+def test_rms_norm_weight_and_eps_closed_forms():
+    x = rnd(4, 16)
+    w = rnd(16)
+    np.testing.assert_allclose(O.rms_norm(x, w), O.rms_norm(x) * w, rtol=1e-14)
+    # a constant vector a: mean(x^2) = a^2, so y = a / sqrt(a^2 + eps)
+    a, eps = 0.3, 0.05
+    np.testing.assert_allclose(O.rms_norm(np.full((1, 8), a), eps=eps), a / math.sqrt(a * a + eps),
+                               rtol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# grouped output projection ([uika] §2.3.1; §4.2.1: g groups of d_g outputs)
+# ----------------------------------------------------------------------------
+
+
+def test_grouped_projection_is_a_block_diagonal_projection():
+    # the grouped projection is one projection whose weight is block diagonal
+    # (group j's inputs feed only group j's outputs): library block_diag + matmul
+    from scipy.linalg import block_diag
+    G, N, K, M = 4, 3, 5, 7
+    A, W = rnd(M, G * K), rnd(G, N, K)
+    full = block_diag(*[W[j].T for j in range(G)])          # [G*K, G*N]
+    np.testing.assert_allclose(O.grouped_projection(A, W), A @ full, rtol=1e-13, atol=1e-13)
+    # extra columns of A beyond G*K are not read
+    A2 = np.concatenate([A, rnd(M, 3)], axis=1)
+    np.testing.assert_array_equal(O.grouped_projection(A2, W), O.grouped_projection(A, W))
+
+
+def test_grouped_projection_one_hot_picks_a_weight_column():
+    # A = e_i (one row, one-hot at column j*K + c) selects W[j][:, c] into group j's outputs
+    G, N, K = 3, 4, 6
+    W = rnd(G, N, K)
+    for j, c in ((0, 0), (1, 5), (2, 3)):
+        a = np.zeros((1, G * K))
+        a[0, j * K + c] = 1.0
+        want = np.zeros(G * N)
+        want[j * N:(j + 1) * N] = W[j][:, c]
+        np.testing.assert_array_equal(O.grouped_projection(a, W)[0], want)
