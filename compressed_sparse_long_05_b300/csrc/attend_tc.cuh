@@ -105,10 +105,13 @@ struct AttSmem {
   static constexpr int MROW = SUMP + 2 * 4 * 64 * 4;       // [4 warps][64] f32 running max
   static constexpr int FAC = MROW + 4 * 64 * 4;            // [4][64] f32 rescale factors
   static constexpr int ML = FAC + 4 * 64 * 4;              // [64][2] f32 this chunk's (max, sum) (cluster merge)
-  static constexpr int WTS = ML + 64 * 2 * 4;              // [16 chunks][64] f32 merge weights (cluster merge)
-  static constexpr int INVD = WTS + 16 * 64 * 4;           // [64] f32 1 / denominator (cluster merge)
-  static constexpr int RMASK = INVD + 64 * 4;             // [2 tiles][4 warps] u32 row-valid bits
-  static constexpr int BAR = RMASK + 64;
+  static constexpr int MLALL = ML + 64 * 2 * 4;            // [16 chunks][64][2] f32 every chunk's (max, sum)
+  static constexpr int OWNW = MLALL + 16 * 64 * 2 * 4;     // [64] f32 this chunk's merge weight
+  static constexpr int INVD = OWNW + 64 * 4;               // [64] f32 1 / denominator (cluster merge)
+  static constexpr int SINK = INVD + 64 * 4;               // [64] f32 sink logits of the head group, in log2 units
+  static constexpr int RMASK = SINK + 64 * 4;              // [2 tiles][4 warps] u32 row-valid bits
+  static constexpr int ROPEF = RMASK + 64;                 // [64] u64 RoPE phase steps (copy of the args)
+  static constexpr int BAR = ROPEF + 64 * 8;
   static constexpr int NBAR = 32;
   static constexpr int MISC = BAR + NBAR * 8;
   static constexpr int BYTES = MISC + 64 + 1024;           // + alignment slack
@@ -167,6 +170,18 @@ CSA_DEVINL void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 CSA_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 32 lanes x 8 consecutive 32-bit columns (load and store)
+CSA_DEVINL void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+CSA_DEVINL void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 
 CSA_DEVINL void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -182,18 +197,60 @@ CSA_DEVINL void cp_async_mbar_arrive(uint64_t* bar) {
 template <int N>
 CSA_DEVINL void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// rotate the 4 (x0, x1) pairs of one 16-byte bf16 unit; pair p uses frequency j0 + p
-CSA_DEVINL uint4 rope_unit(uint4 v, long long pos, const RopeFreqs& rf, int j0) {
+// rotate the 4 (x0, x1) pairs of one 16-byte bf16 unit; pair p uses frequency j0 + p.
+// F is the CTA's shared-memory copy of the phase steps: lanes read different
+// frequencies, which a kernel-parameter array would serve one address at a time.
+CSA_DEVINL uint4 rope_unit(uint4 v, long long pos, const unsigned long long* F, int j0) {
   uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[p]);
     float2 f = __bfloat1622float2(h);
     float c, s;
-    rope_cos_sin(pos, rf.F[j0 + p], c, s);
+    rope_cos_sin(pos, F[j0 + p], c, s);
     w[p] = pack_bf16x2(f.x * c - f.y * s, f.x * s + f.y * c);
   }
   return v;
+}
+
+// 2^x on the special-function unit (one instruction; flushes results below
+// 2^-126 to zero, which a softmax weight can take)
+CSA_DEVINL float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// reduce-scatter butterfly over the warp of 64 values per lane, read through
+// get(e) (so the caller's values need not be copied): on exit lane l holds in
+// r[0], r[1] the op-reduced columns 2l and 2l+1 over all 32 lanes.
+template <bool IS_MAX, typename Get>
+CSA_DEVINL void warp_reduce_scatter64_from(Get get, float* r, int lane) {
+  {
+    const bool upper = (lane & 16) != 0;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float lo = get(e), hi = get(e + 32);
+      const float send = upper ? lo : hi;
+      const float keep = upper ? hi : lo;
+      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+      r[e] = IS_MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int lvl = 1; lvl < 5; ++lvl) {
+    const int off = 16 >> lvl;        // partner distance
+    const int hs = 32 >> lvl;         // half of the values still held
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int e = 0; e < hs; ++e) {
+      const float lo = r[e], hi = r[e + hs];
+      const float send = upper ? lo : hi;
+      const float keep = upper ? hi : lo;
+      const float got = __shfl_xor_sync(0xffffffffu, send, off);
+      r[e] = IS_MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
 }
 
 // reduce-scatter butterfly over the warp: on entry x[0..63] per lane; on exit
@@ -232,78 +289,163 @@ CSA_DEVINL uint4 e4m3x8_to_bf16(uint2 raw, float scale) {
 }
 
 // Cluster merge of a head group's chunks (one item per CTA; cluster rank = chunk).
-// Every CTA has staged its unnormalised O [64 heads][512 dims] f32 at sE and its
-// per-head (max, sum) at AttSmem::ML.  CTA c computes outputs [c*8192/nch,
-// (c+1)*8192/nch) of the 8192 float4 columns: out = sum_c 2^(m_c - M) O_c /
-// (sum_c 2^(m_c - M) l_c + 2^(z' log2 e - M)), reading every chunk's shared
-// memory over DSMEM (relative-RoPE mode: the output needs no rotation).
-CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint8_t* sE) {
+// Output dims are split among the CTAs in groups of 8: CTA o owns dim groups
+// [ceil(64 o / nch), ceil(64 (o+1) / nch)).
+//  1. every CTA sends its per-head (max, sum) into every peer's MLALL slot
+//     (st.async, completing on the peer's ml_bar); a CTA sends only after its
+//     own PV is done, so once a CTA holds everyone's values, every CTA's E / Q
+//     region is free to receive partials;
+//  2. meanwhile eight warps read this chunk's O^T from TMEM (one dim, 64 heads
+//     per thread) and stage it as bf16 in local shared memory grouped by
+//     owner ([owner][head][pitch]); a chunk that saw no row stages zeros;
+//  3. once every (max, sum) is in, one DSMEM bulk copy per owner moves that
+//     owner's block into its receive buffer ([chunk][head][pitch]),
+//     completing on the owner's merge_bar;
+//  4. while the copies fly, each CTA computes for every chunk c and head h the
+//     weight 2^(m_c - M_h) / (sum_c' l_c' 2^(m_c' - M_h) + 2^(z'_h - M_h)),
+//     M_h the largest of the chunks' maxima and the sink logit;
+//  5. each owner waits for its nch blocks and, per head and group of 8 dims,
+//     accumulates weight * partial in fp32 from 16-byte vectors and stores 8
+//     bf16 outputs at once (relative-RoPE mode: no output rotation).
+// Every CTA waits for each byte destined to it before it leaves, so no cluster
+// barrier is needed after the copies.  The partials are rounded to bf16 once
+// (relative 2^-9) before the fp32 sum.
+CSA_DEVINL int merge_dim_lo(int o, int nch) { return 8 * ((o * (ATT_D / 8) + nch - 1) / nch); }
+// dims per head row of a staged / received block: the largest owner's, in 8s
+CSA_DEVINL int merge_pitch(int nch) { return 8 * ((ATT_D / 8 + nch - 1) / nch); }
+constexpr int MERGE_RECV = 80 * 1024;   // receive buffer offset in the E / Q region
+
+CSA_DEVINL uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+CSA_DEVINL void st_async_f2(uint32_t addr, float a0, float a1, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(addr), "f"(a0), "f"(a1), "r"(mbar)
+               : "memory");
+}
+
+CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint32_t tmem,
+                                     uint64_t* merge_bar, uint64_t* ml_bar) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   const int nch = a.nch;
   const int crank = (int)cl.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const AttRow x = att_item(a, blockIdx.x);
-  float* ml = reinterpret_cast<float*>(smem + AttSmem::ML);
-  float* wts = reinterpret_cast<float*>(smem + AttSmem::WTS);
-  float* invd = reinterpret_cast<float*>(smem + AttSmem::INVD);
-  cl.sync();                                          // every chunk's O and (max, sum) staged
-  if (threadIdx.x == 0) CSA_TRACE_MARK(17);
-  if (threadIdx.x < ATT_HG) {
-    const int h = threadIdx.x;
-    float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, cl.map_shared_rank(ml, c)[2 * h]);
-    const float zs = __ldg(a.sink + x.hg * ATT_HG + h) * 1.4426950408889634f;
-    M = fmaxf(M, zs);
-    float den = exp2f(zs - M);
-    for (int c = 0; c < nch; ++c) {
-      const float* p = cl.map_shared_rank(ml, c);
-      const float w = exp2f(p[2 * h] - M);           // 0 for a chunk with no valid row (max -inf)
-      wts[c * ATT_HG + h] = w;
-      den += w * p[2 * h + 1];
-    }
-    invd[h] = 1.f / den;
+  const float* ml = reinterpret_cast<const float*>(smem + AttSmem::ML);
+  float* mlall = reinterpret_cast<float*>(smem + AttSmem::MLALL);     // [chunk][64][2]: (m, l), then weights
+  const int pitch = merge_pitch(nch);
+  const uint32_t blk = (uint32_t)(ATT_HG * pitch * 2);                 // bytes of one block
+  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + AttSmem::E);   // [owner][64][pitch]
+  __nv_bfloat16* recv = reinterpret_cast<__nv_bfloat16*>(smem + AttSmem::E + MERGE_RECV);  // [chunk][64][pitch]
+  const int lo = merge_dim_lo(crank, nch), dn = merge_dim_lo(crank + 1, nch) - lo;
+  volatile int no_abort = 0;   // the merge's waits end on data, never on a role's abort
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every peer has started
+  for (int i = threadIdx.x; i < nch * ATT_HG; i += blockDim.x) {
+    const int c = i / ATT_HG, h = i % ATT_HG;
+    st_async_f2(mapa_shared(smem_u32(mlall + (crank * ATT_HG + h) * 2), (uint32_t)c), ml[2 * h],
+                ml[2 * h + 1], mapa_shared(smem_u32(ml_bar), (uint32_t)c));
   }
+  if (warp < 8) {
+    // stage this chunk's O (needs nothing from the peers): warp w reads TMEM
+    // lane quarter w % 4 (dims bk*128 + (w%4)*32 + lane) for the dim blocks
+    // bk = 2 (w / 4) and 2 (w / 4) + 1
+    const int q4 = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const bool has_o = reinterpret_cast<const int*>(smem + AttSmem::MISC)[2] != 0;
+#pragma unroll 1
+    for (int bb = 0; bb < 2; ++bb) {
+      const int bk = 2 * (warp >> 2) + bb;
+      const int dim = bk * 128 + q4 * 32 + lane;
+      const int o = (dim >> 3) * nch / (ATT_D / 8);
+      __nv_bfloat16* dst = stage + (size_t)o * ATT_HG * pitch + (dim - merge_dim_lo(o, nch));
+      uint32_t r[64];
+      if (has_o) {
+        tmem_ld32(tmem + lane_base + bk * ATT_HG, r);
+        tmem_ld32(tmem + lane_base + bk * ATT_HG + 32, r + 32);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int h = 0; h < 64; ++h) r[h] = 0u;      // no row: TMEM holds no O
+      }
+#pragma unroll
+      for (int h = 0; h < ATT_HG; ++h) dst[(size_t)h * pitch] = __float2bfloat16_rn(__uint_as_float(r[h]));
+    }
+  }
+  fence_proxy_async();                                // staged bytes -> visible to the bulk copies
+  if (threadIdx.x == 0) CSA_TRACE_MARK(17);
+  // every chunk's (max, sum) is here, so every peer's PV is done and its
+  // receive buffer is free
+  mbar_wait(ml_bar, 0, &no_abort);
   __syncthreads();
   if (threadIdx.x == 0) CSA_TRACE_MARK(18);
-  const float4* srcs[16];
-#pragma unroll
-  for (int c = 0; c < 16; ++c)
-    srcs[c] = c < nch ? reinterpret_cast<const float4*>(cl.map_shared_rank(sE, c)) : nullptr;
-  const size_t orow = ((size_t)x.b * a.Tq + x.i) * a.n_h + (size_t)x.hg * ATT_HG;
-  const int q0 = crank * (ATT_HG * ATT_D / 4) / nch, q1 = (crank + 1) * (ATT_HG * ATT_D / 4) / nch;
-  for (int q = q0 + (int)threadIdx.x; q < q1; q += (int)blockDim.x) {
-    const int h = q >> 7;                             // 128 float4 columns per head
-    float4 v[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-      if (c < nch) v[c] = srcs[c][q];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-      if (c < nch) {
-        const float w = wts[c * ATT_HG + h];
-        acc.x = fmaf(w, v[c].x, acc.x);
-        acc.y = fmaf(w, v[c].y, acc.y);
-        acc.z = fmaf(w, v[c].z, acc.z);
-        acc.w = fmaf(w, v[c].w, acc.w);
-      }
-    const float s = invd[h];
-    __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * s, acc.y * s);
-    __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * s, acc.w * s);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-    *reinterpret_cast<uint2*>(a.out + (orow + h) * ATT_D + (q & 127) * 4) = pk;
+  if (threadIdx.x < (unsigned)nch) {
+    // block of owner o -> owner's recv[crank]
+    const int o = threadIdx.x;
+    const uint32_t src = smem_u32(stage) + (uint32_t)o * blk;
+    const uint32_t dst = mapa_shared(smem_u32(recv) + (uint32_t)crank * blk, (uint32_t)o);
+    const uint32_t bar = mapa_shared(smem_u32(merge_bar), (uint32_t)o);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "r"(src), "r"(blk), "r"(bar)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   }
+  // while the copies fly: the weight of every (chunk, head),
+  // 2^(m_c - M_h) / (sum_c' l_c' 2^(m_c' - M_h) + 2^(z'_h - M_h)), written over m_c
+  if (threadIdx.x >= 32 && threadIdx.x < 32 + ATT_HG) {
+    const int h = threadIdx.x - 32;
+    const float zs = reinterpret_cast<const float*>(smem + AttSmem::SINK)[h];
+    float M = zs;
+    for (int k = 0; k < nch; ++k)
+      if (mlall[(k * ATT_HG + h) * 2 + 1] > 0.f) M = fmaxf(M, mlall[(k * ATT_HG + h) * 2]);
+    float den = exp2f(zs - M);
+    for (int k = 0; k < nch; ++k) {
+      const float lk = mlall[(k * ATT_HG + h) * 2 + 1];
+      const float ek = lk > 0.f ? exp2f(mlall[(k * ATT_HG + h) * 2] - M) : 0.f;
+      mlall[(k * ATT_HG + h) * 2] = ek;
+      den += lk * ek;
+    }
+    const float inv = 1.f / den;
+    for (int k = 0; k < nch; ++k) mlall[(k * ATT_HG + h) * 2] *= inv;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) CSA_TRACE_MARK(19);
-  cl.sync();                                          // no CTA leaves while peers read its memory
+  // this CTA's blocks from every chunk (they must land before it may leave)
+  const bool got = mbar_wait(merge_bar, 0, &no_abort);
   if (threadIdx.x == 0) CSA_TRACE_MARK(20);
+  if (got) {
+    const size_t orow = ((size_t)x.b * a.Tq + x.i) * a.n_h + (size_t)x.hg * ATT_HG;
+    const int ng = dn >> 3;                           // groups of 8 dims this CTA owns
+    for (int i = threadIdx.x; i < ATT_HG * ng; i += blockDim.x) {
+      const int h = i / ng, g = i - h * ng;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      const uint4* src = reinterpret_cast<const uint4*>(recv + (size_t)h * pitch + 8 * g);
+      for (int c = 0; c < nch; ++c) {
+        const float w = mlall[(c * ATT_HG + h) * 2];
+        float f[8];
+        bf16x8_to_f(src[(size_t)c * ATT_HG * pitch / 8], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+      }
+      *reinterpret_cast<uint4*>(a.out + (orow + h) * ATT_D + lo + 8 * g) = f_to_bf16x8(acc);
+    }
+  }
+  if (threadIdx.x == 0) CSA_TRACE_MARK(26);
+  if (threadIdx.x < (unsigned)nch)                    // own copies have read their source
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  if (threadIdx.x == 0) CSA_TRACE_MARK(27);
 }
 
 __global__ void __launch_bounds__(ATT_THREADS, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = aligned_smem<1024>(smem_raw);
   uint8_t* sE = smem + AttSmem::E;
   uint8_t* sQ = smem + AttSmem::Q;
   uint8_t* sP = smem + AttSmem::P;
@@ -326,8 +468,19 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
   uint64_t* grp_b = bar + 22;        // softmax warps: sum partials (count 4)
   uint64_t* mma_done = bar + 23;
   uint64_t* q_ready = bar + 24;      // absolute-RoPE mode: q rotated at t -> MMA (count 4)
+  uint64_t* merge_bar = bar + 25;    // cluster merge: this CTA's slices from every chunk landed
+  uint64_t* ml_bar = bar + 26;       // cluster merge: every chunk's (max, sum) landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttSmem::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttSmem::MISC + 4);
+  unsigned long long* ropeF = reinterpret_cast<unsigned long long*>(smem + AttSmem::ROPEF);
+  if (threadIdx.x < 64) ropeF[threadIdx.x] = a.rf.F[threadIdx.x];
+  if (a.cl_reduce && threadIdx.x < ATT_HG) {
+    // the merge's sink logits, fetched now rather than on its critical path
+    // (parameters only: no grid dependency involved)
+    const int hg = (int)((blockIdx.x / a.nch) % a.HG);
+    reinterpret_cast<float*>(smem + AttSmem::SINK)[threadIdx.x] =
+        __ldg(a.sink + hg * ATT_HG + threadIdx.x) * 1.4426950408889634f;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) { CSA_TRACE_WALL(0); CSA_TRACE_MARK(1); }
@@ -345,7 +498,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
     mbar_init(grp_a, 4);
     mbar_init(grp_b, 4);
     mbar_init(mma_done, 1);
+    mbar_init(merge_bar, 1);
+    mbar_init(ml_bar, 1);
+    if (a.cl_reduce) {
+      // the merge receives nch (max, sum) sets and nch blocks of partials
+      const int pitch = merge_pitch(a.nch);
+      mbar_arrive_expect_tx(ml_bar, (uint32_t)(a.nch * ATT_HG * 8));
+      mbar_arrive_expect_tx(merge_bar, (uint32_t)(a.nch * ATT_HG * pitch * 2));
+    }
     *abort_flag = 0;
+    reinterpret_cast<volatile int*>(smem + AttSmem::MISC)[2] = 0;   // this CTA's O holds rows
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -356,6 +518,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // cluster merge: announce that this CTA runs (peers wait for it before their
+  // first store into this CTA's shared memory)
+  if (a.cl_reduce) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
   if (threadIdx.x == 0) CSA_TRACE_MARK(2);
   const uint32_t TM_O = 0, TM_S = 256;     // O^T blocks at 0..255, S^T buffers at 256..383
@@ -459,7 +624,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
               for (int k2 = 0; k2 < 4; ++k2) {
                 const int h = gw * 16 + k2 * 4 + (lane >> 3), u = lane & 7;
                 uint4* ptr = reinterpret_cast<uint4*>(sQ + 7 * 8192 + h * 128 + ((u ^ (h & 7)) << 4));
-                *ptr = rope_unit(*ptr, x.t, a.rf, u * 4);
+                *ptr = rope_unit(*ptr, x.t, ropeF, u * 4);
               }
               fence_proxy_async();
               __syncwarp();
@@ -488,7 +653,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
               const long long p = __shfl_sync(0xffffffffu, pos, rl) - (a.rel_rope ? x.t : 0);
               const int tr = gw * 32 + rl;
               uint4* ptr = reinterpret_cast<uint4*>(c7 + tr * 128 + ((u ^ (tr & 7)) << 4));
-              *ptr = rope_unit(*ptr, p, a.rf, u * 4);
+              *ptr = rope_unit(*ptr, p, ropeF, u * 4);
             }
             fence_proxy_async();
             __syncwarp();
@@ -558,7 +723,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             const long long p = __shfl_sync(0xffffffffu, pos, rl) - (a.rel_rope ? x.t : 0);
             const int tr = gw * 32 + rl;
             uint4* ptr = reinterpret_cast<uint4*>(c7 + tr * 128 + ((u ^ (tr & 7)) << 4));
-            *ptr = rope_unit(*ptr, p, a.rf, u * 4);
+            *ptr = rope_unit(*ptr, p, ropeF, u * 4);
           }
         }
         fence_proxy_async();
@@ -662,19 +827,19 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free + sb);
+        if (n == (uint32_t)CSA_TRACE_TILE && q4 == 0 && lane == 0) CSA_TRACE_MARK(23);
         const bool valid = (rmask[(n & 1) * 4 + q4] >> lane) & 1u;
 #pragma unroll
         for (int e = 0; e < 64; ++e) xs[e] = valid ? xs[e] * a.scale_log2 : -INFINITY;
         // ---- per-head tile max over the 128 rows ----
-        float red[64];
-#pragma unroll
-        for (int e = 0; e < 64; ++e) red[e] = xs[e];
-        warp_reduce_scatter64<true>(red, lane);
+        float red[32];
+        warp_reduce_scatter64_from<true>([&](int e) { return xs[e]; }, red, lane);
         maxp[(par * 4 + q4) * 64 + 2 * lane] = red[0];
         maxp[(par * 4 + q4) * 64 + 2 * lane + 1] = red[1];
         __syncwarp();
         if (lane == 0) mbar_arrive(grp_a);
         if (!mbar_wait(grp_a, par, abort_flag)) { ok = false; break; }
+        if (n == (uint32_t)CSA_TRACE_TILE && q4 == 0 && lane == 0) CSA_TRACE_MARK(24);
         bool resc = false;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -698,17 +863,18 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
         resc = __any_sync(0xffffffffu, resc);
         __syncwarp();
         // ---- P = exp2(x - m), bf16; row pieces of P^T ----
+        // (a head whose rows so far are all masked has m = -inf: its P is 0, not NaN)
+        // (the row sums are taken later from the same bf16-rounded P, unpacked)
         uint32_t pk[32];
-        float* pr = red;                              // reused: rounded P for the row sums
+        const float2* mm = reinterpret_cast<const float2*>(my_m);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = exp2f(xs[2 * e] - my_m[2 * e]);
-          const float p1 = exp2f(xs[2 * e + 1] - my_m[2 * e + 1]);
+          const float2 m2 = mm[e];
+          const float p0 = ex2_approx(xs[2 * e] - (m2.x == -INFINITY ? 0.f : m2.x));
+          const float p1 = ex2_approx(xs[2 * e + 1] - (m2.y == -INFINITY ? 0.f : m2.y));
           pk[e] = pack_bf16x2(p0, p1);
-          const float2 back = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk[e]));
-          pr[2 * e] = back.x;
-          pr[2 * e + 1] = back.y;
         }
+        if (n == (uint32_t)CSA_TRACE_TILE && q4 == 0 && lane == 0) CSA_TRACE_MARK(25);
         // PV of the previous tile must be done before P^T and O^T are touched
         if (!mbar_wait(p_free, (n & 1) ^ 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -722,19 +888,18 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
         }
         if (resc && j > 0) {
           // O^T columns (heads) times their factors; this warp owns dims rows
-          // q4*32 + lane of each 128-dim block
+          // q4*32 + lane of each 128-dim block.  Eight columns at a time: the
+          // packed P words stay live across this rare path.
 #pragma unroll 1
-          for (int bk = 0; bk < 4; ++bk) {
+          for (int cc = 0; cc < 4 * ATT_HG; cc += 8) {
+            uint32_t r[8];
+            const uint32_t ta = tmem + lane_base + TM_O + cc;
+            tmem_ld8(ta, r);
+            tmem_ld_wait();
 #pragma unroll
-            for (int hh = 0; hh < 64; hh += 32) {
-              uint32_t r[32];
-              const uint32_t ta = tmem + lane_base + TM_O + bk * ATT_HG + hh;
-              tmem_ld32(ta, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * my_f[hh + e]);
-              tmem_st32(ta, r);
-            }
+            for (int e = 0; e < 8; ++e)
+              r[e] = __float_as_uint(__uint_as_float(r[e]) * my_f[(cc & (ATT_HG - 1)) + e]);
+            tmem_st8(ta, r);
           }
           tmem_st_wait();
         }
@@ -743,10 +908,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
         if (n == (uint32_t)CSA_TRACE_TILE && q4 == 0 && lane == 0) CSA_TRACE_MARK(11);
-        // ---- per-head row sums ----
-        warp_reduce_scatter64<false>(pr, lane);
-        sump[(par * 4 + q4) * 64 + 2 * lane] = pr[0];
-        sump[(par * 4 + q4) * 64 + 2 * lane + 1] = pr[1];
+        // ---- per-head row sums (of the bf16-rounded P the MMA used) ----
+        float sr[32];
+        warp_reduce_scatter64_from<false>([&](int e) {
+          const uint32_t w = pk[e >> 1];
+          return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+        }, sr, lane);
+        sump[(par * 4 + q4) * 64 + 2 * lane] = sr[0];
+        sump[(par * 4 + q4) * 64 + 2 * lane + 1] = sr[1];
         __syncwarp();
         if (lane == 0) mbar_arrive(grp_b);
         if (!mbar_wait(grp_b, par, abort_flag)) { ok = false; break; }
@@ -768,6 +937,20 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
         tc_fence_after();
       }
       if (it == (int)blockIdx.x && q4 == 0 && lane == 0) CSA_TRACE_MARK(14);
+      if (a.cl_reduce) {
+        // cluster merge (one item per CTA): only this chunk's (max, sum) is
+        // recorded here; the merge after the role loops moves O out of TMEM
+        float* ml = reinterpret_cast<float*>(smem + AttSmem::ML);
+        if (q4 == 0) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            ml[(2 * lane + e) * 2] = m_run[e];
+            ml[(2 * lane + e) * 2 + 1] = j > 0 ? l_run[e] : 0.f;
+          }
+          if (lane == 0) reinterpret_cast<int*>(smem + AttSmem::MISC)[2] = j > 0 ? 1 : 0;
+        }
+        continue;
+      }
       // per-head output scale into this warp's table
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -792,7 +975,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
         float c = 1.f, s = 0.f;
         const bool rope_dim = dim >= ATT_D - ATT_R;
         const bool rot_out = single && rope_dim && !a.rel_rope;
-        if (rot_out) rope_cos_sin(-x.t, a.rf.F[(dim - (ATT_D - ATT_R)) >> 1], c, s);
+        if (rot_out) rope_cos_sin(-x.t, ropeF[(dim - (ATT_D - ATT_R)) >> 1], c, s);
         uint32_t r2[64];
         if (j > 0) {
           tmem_ld32(tmem + lane_base + TM_O + bk * ATT_HG, r2);
@@ -851,7 +1034,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
   __syncthreads();
   tc_fence_after();
   if (threadIdx.x == 0) CSA_TRACE_MARK(16);
-  if (a.cl_reduce) attend_cluster_merge(a, smem, sE);
+  if (a.cl_reduce) attend_cluster_merge(a, smem, tmem, merge_bar, ml_bar);
   if (warp == 8) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0) { CSA_TRACE_MARK(22); CSA_TRACE_WALL(21); }
 }
@@ -955,6 +1138,9 @@ struct RotateArgs {
 };
 
 __global__ void __launch_bounds__(256) rope_rotate_rows_kernel(const RotateArgs a) {
+  __shared__ unsigned long long F[64];          // lanes read different frequencies
+  if (threadIdx.x < 64) F[threadIdx.x] = a.rf.F[threadIdx.x];
+  __syncthreads();
   pdl_enter();
   // one thread per 16-byte unit; 64 units per 512-dim row
   const long long u_all = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -966,7 +1152,7 @@ __global__ void __launch_bounds__(256) rope_rotate_rows_kernel(const RotateArgs 
     const long long s = row % a.rows_per_b;
     const long long pos = a.m > 0 ? (long long)a.m * (s + 1) - 1
                                   : window_base(a.base, (int)(row / a.rows_per_b)) + s;
-    v = rope_unit(v, pos, a.rf, (u - (ATT_D - ATT_R) / 8) * 4);
+    v = rope_unit(v, pos, F, (u - (ATT_D - ATT_R) / 8) * 4);
   }
   *reinterpret_cast<uint4*>(a.dst + row * ATT_D + u * 8) = v;
 }

@@ -35,7 +35,7 @@ CSA_DEVINL long long csa_globaltimer() {
 #ifdef CSA_TRACE
 namespace csa {
 constexpr int CSA_TRACE_CTAS = 160;
-constexpr int CSA_TRACE_SLOTS = 64;   // attention 0-23, index 24-39, top-k 40-55
+constexpr int CSA_TRACE_SLOTS = 64;   // attention 0-31, index 32-47, top-k 48-63
 __device__ long long g_csa_trace[CSA_TRACE_CTAS][CSA_TRACE_SLOTS];
 __device__ int g_csa_trace_tile;   // which tile of a CTA the per-tile marks describe
 }  // namespace csa
@@ -117,10 +117,13 @@ CSA_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
 // The host stores, per frequency j, F_j = round(theta_j / (2*pi) * 2^64) as a
 // uint64.  For an integer position p the rotation phase in revolutions is
 // p * F_j / 2^64 modulo 1, which unsigned 64-bit multiplication gives exactly
-// (wrap-around is the modulo).  The top bits, read as a signed fraction in
-// [-1/2, 1/2), give an angle in [-pi, pi) that the fast hardware sine/cosine
-// evaluate to about 1e-6 absolute, so the angle stays accurate at any position
-// up to 2^40 (plain fp32 p * theta would be off by up to 0.06 rad at 2^20).
+// (wrap-around is the modulo).  Only its top 32 bits are needed: for
+// F = F_hi 2^32 + F_lo they are |p| F_hi + hi32(|p| F_lo) modulo 2^32, three
+// 32-bit operations.  Read as a signed fraction in [-1/2, 1/2) they give an
+// angle in [-pi, pi) that the fast hardware sine/cosine evaluate to about 1e-6
+// absolute, so the angle stays accurate at any position |p| < 2^31 (plain fp32
+// p * theta would be off by up to 0.06 rad at 2^20).  A negative position
+// turns the other way: the same cosine, the sine negated.
 // ----------------------------------------------------------------------------
 struct RopeFreqs {
   unsigned long long F[64];  // one per rotated pair; r/2 <= 64
@@ -128,9 +131,11 @@ struct RopeFreqs {
 };
 
 CSA_DEVINL void rope_cos_sin(long long pos, unsigned long long F, float& c, float& s) {
-  const unsigned long long ph = (unsigned long long)pos * F;
-  const float rev = (float)((long long)ph >> 40) * 5.9604644775390625e-8f;  // * 2^-24
+  const unsigned int ap = (unsigned int)(pos < 0 ? -pos : pos);
+  const unsigned int w = ap * (unsigned int)(F >> 32) + __umulhi(ap, (unsigned int)F);
+  const float rev = (float)(int)w * 2.3283064365386963e-10f;   // * 2^-32
   __sincosf(6.283185307179586f * rev, &s, &c);
+  if (pos < 0) s = -s;
 }
 
 // ----------------------------------------------------------------------------

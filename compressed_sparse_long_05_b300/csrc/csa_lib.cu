@@ -73,17 +73,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 }
 
 
-// Programmatic stream serialisation would let a kernel start while the previous
-// kernel in the stream finishes (every kernel here waits on the grid dependency
-// before its first global memory access, so either setting is correct).  Off:
-// measured in CUDA-graph replay of the decode and prefill steps, the early-
-// launched grids made each step slower (decode 128K: 69 vs 59 us per step).
+// Programmatic stream serialisation lets a kernel's CTAs launch while the
+// previous kernel in the stream still runs: every kernel here sets up its
+// barriers and tensor memory, then waits on the grid dependency before its
+// first global memory access, so the setting never changes results.  Off:
+// applied to every launch it made the decode step slower (128K: 69 vs 59 us,
+// early grids took the SMs the running one's clusters needed), and applied
+// only inside one layer forward (index -> top-k -> attention) the launch gaps
+// vanished but the early grids waited as long (63.4 vs 67.0 us per step).
 constexpr bool kProgrammaticLaunch = false;
 
-// Launch with an optional cluster size (and programmatic serialisation when on).
+// As launch_ex, with programmatic serialisation against the previous kernel when `pdl`.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                      int cluster, Args... args) {
+cudaError_t launch_ex_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          int cluster, bool pdl, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -91,7 +94,7 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  if (kProgrammaticLaunch) {
+  if (pdl) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
@@ -107,6 +110,14 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
+
+// Launch with an optional cluster size (and programmatic serialisation when on).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      int cluster, Args... args) {
+  return launch_ex_pdl(kern, grid, block, smem, st, cluster, kProgrammaticLaunch, args...);
+}
+
 
 // 3-D bf16 tensor map (x fastest), 128-byte swizzle, zero fill out of bounds.
 bool tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t x, uint64_t y, uint64_t z,
@@ -370,7 +381,8 @@ bool tc_attend_shape(int n_h, int d, int r, int kv_dtype) {
 }
 
 template <int NT, int CL, int BITS1>
-csa_status_t launch_topk2_cfg(const csa::Topk2Args& a, int rows, size_t smem, cudaStream_t st) {
+csa_status_t launch_topk2_cfg(const csa::Topk2Args& a, int rows, size_t smem, cudaStream_t st,
+                              bool pdl) {
   auto kern = csa::topk2_kernel<NT, CL, BITS1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "csa_topk attr");
@@ -391,20 +403,21 @@ csa_status_t launch_topk2_cfg(const csa::Topk2Args& a, int rows, size_t smem, cu
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = kProgrammaticLaunch ? 2 : 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return cuda_fail(e, "csa_topk launch");
   return CSA_OK;
 }
 
 template <int NT, int BITS1>
-csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t smem, cudaStream_t st) {
+csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t smem, cudaStream_t st,
+                             bool pdl) {
   switch (CL) {
-    case 1: return launch_topk2_cfg<NT, 1, BITS1>(a, rows, smem, st);
-    case 2: return launch_topk2_cfg<NT, 2, BITS1>(a, rows, smem, st);
-    case 4: return launch_topk2_cfg<NT, 4, BITS1>(a, rows, smem, st);
-    case 8: return launch_topk2_cfg<NT, 8, BITS1>(a, rows, smem, st);
-    default: return launch_topk2_cfg<NT, 16, BITS1>(a, rows, smem, st);
+    case 1: return launch_topk2_cfg<NT, 1, BITS1>(a, rows, smem, st, pdl);
+    case 2: return launch_topk2_cfg<NT, 2, BITS1>(a, rows, smem, st, pdl);
+    case 4: return launch_topk2_cfg<NT, 4, BITS1>(a, rows, smem, st, pdl);
+    case 8: return launch_topk2_cfg<NT, 8, BITS1>(a, rows, smem, st, pdl);
+    default: return launch_topk2_cfg<NT, 16, BITS1>(a, rows, smem, st, pdl);
   }
 }
 
@@ -434,10 +447,11 @@ csa_status_t launch_topk2(const float* scores, const int32_t* q_pos, int32_t* id
   const size_t smem = csa::topk2_smem_bytes(slice, cand_cap, bits1, merge);
   csa::Topk2Args a{scores, idx, q_pos, Tq, N, k, m, slice, cand_cap, hist};
   const bool wide = (long long)rows * CL <= 2LL * sm_count();
-  if (hist) return wide ? launch_topk2_nt<1024, csa::IDX_HBITS>(a, CL, rows, smem, st)
-                        : launch_topk2_nt<512, csa::IDX_HBITS>(a, CL, rows, smem, st);
-  return wide ? launch_topk2_nt<1024, csa::TK2_BITS1>(a, CL, rows, smem, st)
-              : launch_topk2_nt<512, csa::TK2_BITS1>(a, CL, rows, smem, st);
+  const bool pdl = kProgrammaticLaunch;
+  if (hist) return wide ? launch_topk2_nt<1024, csa::IDX_HBITS>(a, CL, rows, smem, st, pdl)
+                        : launch_topk2_nt<512, csa::IDX_HBITS>(a, CL, rows, smem, st, pdl);
+  return wide ? launch_topk2_nt<1024, csa::TK2_BITS1>(a, CL, rows, smem, st, pdl)
+              : launch_topk2_nt<512, csa::TK2_BITS1>(a, CL, rows, smem, st, pdl);
 }
 
 }  // namespace
@@ -845,8 +859,8 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
     e = cudaFuncSetAttribute(csa::attend_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_fail(e, "csa_attend cluster attr");
   }
-  e = launch_ex(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st,
-                p.cl_reduce ? p.nch : 1, tmq, a);
+  e = launch_ex_pdl(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st,
+                    p.cl_reduce ? p.nch : 1, kProgrammaticLaunch, tmq, a);
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc launch");
   if (p.nch > 1 && !p.cl_reduce) {
     csa::CombineArgs ca;

@@ -74,7 +74,7 @@ gemm_grouped_kernel(const __grid_constant__ CUtensorMap tm_A, const __grid_const
                     const GemmArgs a) {
   using L = GemmSmem;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = aligned_smem<1024>(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* full = bars;                           // [STAGES] A + W tile landed
   uint64_t* empty = bars + GEMM_STAGES;            // [STAGES] MMAs that read the stage done

@@ -134,7 +134,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
   using L = IndexFp4Smem;
   const IndexTcArgs& a = fa.t;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = aligned_smem<1024>(smem_raw);
   uint8_t* sA = smem + L::OFF_A;
   uint8_t* sB = smem + L::OFF_B;
   uint8_t* atomA = smem + L::OFF_ATOM_A;

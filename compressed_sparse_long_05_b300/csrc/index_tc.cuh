@@ -171,7 +171,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   const IndexSmem<H, C> L(a.stages, NQH, a.hist != nullptr);
   const int S = L.S;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = aligned_smem<1024>(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + L.OFF_B;
   float* w_s = reinterpret_cast<float*>(smem + L.OFF_W);
@@ -189,7 +189,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t B_BYTES = (uint32_t)NQH * C * 2;
-  if (threadIdx.x == 0) { CSA_TRACE_WALL(24); CSA_TRACE_MARK(25); }
+  if (threadIdx.x == 0) { CSA_TRACE_WALL(32); CSA_TRACE_MARK(33); }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
@@ -215,7 +215,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
-  if (threadIdx.x == 0) CSA_TRACE_MARK(26);
+  if (threadIdx.x == 0) CSA_TRACE_MARK(34);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -250,7 +250,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         for (int kc = 0; kc < L.KCH; ++kc)
           tma_load_3d(sB + kc * (NQH * 128), &tm_q, b_full, kc * 64, x.t0 * H, x.b);
         b_issued = true;
-        if (nitem == 0) CSA_TRACE_MARK(27);
+        if (nitem == 0) CSA_TRACE_MARK(35);
         ++nitem;
         for (int jj = pre; jj < ntl && ok; ++jj) ok = load_a(x.j0 + jj);
       }
@@ -274,7 +274,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
           if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag, lim)) { ok = false; break; }
           if (!mbar_wait(full + st, ph, abort_flag, lim)) { ok = false; break; }
-          if (ia == 0) CSA_TRACE_MARK(28);
+          if (ia == 0) CSA_TRACE_MARK(36);
           tc_fence_after();
           const uint32_t aBase = smem_u32(sA + st * L.A_BYTES);
           const uint32_t bBase = smem_u32(sB);
@@ -291,7 +291,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           ++ia;
           ++iacc;
         }
-        CSA_TRACE_MARK(29);
+        CSA_TRACE_MARK(37);
         umma_commit(b_free);
         ++nitem;
       }
@@ -336,13 +336,13 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + buf);
-          if (ew == 0 && lane == 0) CSA_TRACE_MARK(iacc <= 2 ? 30 : 31);
+          if (ew == 0 && lane == 0) CSA_TRACE_MARK(iacc <= 2 ? 38 : 39);
         } else if ((j & 1) == grp) {
           for (int qi = 0; qi < x.nq; ++qi)
             if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
         }
       }
-      if (ew == 0 && lane == 0) CSA_TRACE_MARK(32);
+      if (ew == 0 && lane == 0) CSA_TRACE_MARK(40);
       if (a.hist) {
         // both groups have added this item's scores: one group flushes (and clears)
         // the shared per-quarter histograms; the next item's adds wait for that.
@@ -351,9 +351,9 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         if (lane == 0) mbar_arrive(epi_sync);
         const bool s1 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag, lim));
         ++nsync;
-        if (ew == 0 && lane == 0) CSA_TRACE_MARK(33);
+        if (ew == 0 && lane == 0) CSA_TRACE_MARK(41);
         if (ok && s1 && grp == 0) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
-        if (ew == 0 && lane == 0) CSA_TRACE_MARK(34);
+        if (ew == 0 && lane == 0) CSA_TRACE_MARK(42);
         __syncwarp();
         if (lane == 0) mbar_arrive(epi_sync);
         const bool s2 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag, lim));
@@ -367,7 +367,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
-  if (threadIdx.x == 0) { CSA_TRACE_MARK(36); CSA_TRACE_WALL(35); }
+  if (threadIdx.x == 0) { CSA_TRACE_MARK(44); CSA_TRACE_WALL(43); }
 }
 
 }  // namespace csa

@@ -11,6 +11,17 @@ CSA_DEVINL uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory base rounded up to `align` bytes.  Offsetting the
+// __shared__ array itself (rather than rebuilding a pointer from an integer)
+// keeps the compiler aware that every access through the result is a
+// shared-memory access, so those compile to shared loads and stores instead
+// of generic ones.
+template <unsigned align>
+CSA_DEVINL uint8_t* aligned_smem(uint8_t* smem_raw) {
+  const uint32_t mis = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & (align - 1);
+  return smem_raw + ((align - mis) & (align - 1));
+}
+
 // ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------

@@ -78,7 +78,7 @@ CSA_DEVINL int tk2_block_scan(int x, int* sh, int* total) {
 
 template <int NT, int CL, int BITS1>
 __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
-  if (threadIdx.x == 0) { CSA_TRACE_WALL(40); CSA_TRACE_MARK(41); }
+  if (threadIdx.x == 0) { CSA_TRACE_WALL(48); CSA_TRACE_MARK(49); }
   pdl_enter();
   constexpr int NW = NT / 32;
   constexpr int BINS1 = 1 << BITS1;
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
     for (int j = rank * (BINS1 / CL) + tid; j < (rank + 1) * (BINS1 / CL); j += NT) gh[j] = 0u;
   }
 
-  if (tid == 0) CSA_TRACE_MARK(42);
+  if (tid == 0) CSA_TRACE_MARK(50);
   // ---- 1. load the slice (every copy in flight at once), then keys + first-digit histogram ----
   {
     const bool vec = ((lo & 3) == 0) && ((reinterpret_cast<uintptr_t>(srow) & 15) == 0);
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   }
   const uint32_t b1 = sh_sel[0];
   uint32_t krem = sh_sel[1];
-  if (tid == 0) CSA_TRACE_MARK(43);
+  if (tid == 0) CSA_TRACE_MARK(51);
 
   // ---- 3. candidates: this slice's keys in bin b1 ----
   int ncand = 0;
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   }
   const uint32_t* list = cand_ok ? cand : keys;
   const int list_n = cand_ok ? ncand : n;
-  if (tid == 0) CSA_TRACE_MARK(44);
+  if (tid == 0) CSA_TRACE_MARK(52);
 
   // ---- 4. three radix passes over the candidates (or the b1-filtered slice) ----
   uint32_t prefix = b1 << SHIFT1;
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
     pmask |= dmask << sh;
     krem = sh_sel[1];
   }
-  if (tid == 0) CSA_TRACE_MARK(45);
+  if (tid == 0) CSA_TRACE_MARK(53);
   const uint32_t T = prefix;          // exact k-th largest key
   const int q_eq = (int)krem;         // keys == T to take, lowest indices first
 
@@ -409,9 +409,9 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
     gt_before += __popc(gm);
     eq_before += __popc(em);
   }
-  if (tid == 0) CSA_TRACE_MARK(46);
+  if (tid == 0) CSA_TRACE_MARK(54);
   if constexpr (CL > 1) cluster.sync();   // peers may still read sh_tot / histograms
-  if (tid == 0) { CSA_TRACE_MARK(48); CSA_TRACE_WALL(47); }
+  if (tid == 0) { CSA_TRACE_MARK(56); CSA_TRACE_WALL(55); }
 }
 
 }  // namespace csa

@@ -21,23 +21,23 @@ import numpy as np
 
 # kernel -> (wall-clock entry slot, clock entry slot, clock exit slot, wall exit slot, phases)
 KERNELS = {
-    "index (index_tc_kernel)": (24, 25, 36, 35, {
-        26: "barriers + TMEM allocated",
-        27: "producer: first item's query group issued",
-        28: "MMA: first K tile landed",
-        29: "MMA: every MMA of the first item issued",
-        30: "epilogue warp 2: first tiles folded",
-        31: "epilogue warp 2: last tile folded",
-        32: "epilogue warp 2: item's tiles done",
-        33: "histogram flush start",
-        34: "histogram flush end",
+    "index (index_tc_kernel)": (32, 33, 44, 43, {
+        34: "barriers + TMEM allocated",
+        35: "producer: first item's query group issued",
+        36: "MMA: first K tile landed",
+        37: "MMA: every MMA of the first item issued",
+        38: "epilogue warp 2: first tiles folded",
+        39: "epilogue warp 2: last tile folded",
+        40: "epilogue warp 2: item's tiles done",
+        41: "histogram flush start",
+        42: "histogram flush end",
     }),
-    "top-k (topk2_kernel)": (40, 41, 48, 47, {
-        42: "histogram read, cluster barrier passed",
-        43: "threshold bin found",
-        44: "candidates gathered",
-        45: "radix passes done (k-th key known)",
-        46: "indices written",
+    "top-k (topk2_kernel)": (48, 49, 56, 55, {
+        50: "histogram read, cluster barrier passed",
+        51: "threshold bin found",
+        52: "candidates gathered",
+        53: "radix passes done (k-th key known)",
+        54: "indices written",
     }),
     "attention (attend_tc_kernel)": (0, 1, 22, 21, {
         2: "barriers + TMEM allocated",
@@ -49,16 +49,21 @@ KERNELS = {
         8: "traced tile: RoPE done, last chunk released",
         9: "traced tile: QK issued (all chunks in)",
         10: "traced tile: S in softmax warps",
+        23: "traced tile: S read from TMEM",
+        24: "traced tile: tile max exchanged (4 warps)",
+        25: "traced tile: P computed in registers",
         11: "traced tile: P written",
         12: "traced tile: PV issued",
         13: "traced tile: row sums done",
         14: "epilogue: last PV done",
-        15: "epilogue: O staged / stored",
+        15: "epilogue: O stored (single chunk or split mode)",
         16: "all roles done (before merge)",
-        17: "merge: cluster barrier passed",
-        18: "merge: weights computed",
-        19: "merge: outputs stored",
-        20: "merge: final cluster barrier",
+        17: "merge: own partial staged as bf16",
+        18: "merge: every chunk's (max, sum) received",
+        19: "merge: copies issued, weights computed",
+        20: "merge: this CTA's blocks received",
+        26: "merge: outputs stored",
+        27: "merge: own copies read",
     }),
 }
 
