@@ -421,6 +421,12 @@ csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t s
   }
 }
 
+// Cluster size for a few decode rows of 8K..32K keys whose first histogram the
+// index kernel built.
+#ifndef CSA_TOPK_DECODE_CL
+#define CSA_TOPK_DECODE_CL 8
+#endif
+
 // One CTA per row up to 32768 entries, longer rows over a cluster of 8 or 16
 // CTAs (rows up to 16 x 32768 entries); 1024 threads per CTA when few CTAs
 // run, else 512.  `hist` (optional): per-row histograms of the first
@@ -432,7 +438,7 @@ csa_status_t launch_topk2(const float* scores, const int32_t* q_pos, int32_t* id
     CL = 8;
     while (CL < 16 && (long long)CL * 32768 < N) CL <<= 1;
   } else if (hist && N > 8192 && (long long)rows * 8 <= 2LL * sm_count()) {
-    CL = 8;   // few decode rows: spread the sweeps over 8 CTAs (measured faster than 1 or 16)
+    CL = CSA_TOPK_DECODE_CL;   // few decode rows: spread the sweeps over a cluster
   }
   int slice = (N + CL - 1) / CL;
   slice = (slice + 3) & ~3;
