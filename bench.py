@@ -441,6 +441,8 @@ def gpu_arm(args, cfg, rank, world, with_e2e=True):
 
     # ---------------- end to end through the public API, host buffers ----------------
     e2e = e2e_leg(K, cfg, xs[0], bufs[0], stream, args, dev) if with_e2e else None
+    bf16 = (bf16_scores_leg(K, cfg, xs[0], dev)
+            if cfg["kind"] == "csa_decode" and cfg["dtype"] != "f32" else None)
 
     ms_step = ms_total / args.steps
     tokens_per_step = cfg["B"] * cfg["Tq"] * world
@@ -484,6 +486,8 @@ def gpu_arm(args, cfg, rank, world, with_e2e=True):
         "kernels": kernels, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if bf16:
+        line["bf16_scores"] = bf16
     x_first = xs[0]
     del xs, bufs, steps, cycle, singles, inst_graphs
     torch.cuda.synchronize()
@@ -548,6 +552,56 @@ def projection_leg(args, dev, tokens, g=16, d_g=1024, n_h=128, d=512, d_model=71
     del A, Wg, Wo, y, z
     torch.cuda.synchronize()
     return out
+
+
+def bf16_scores_leg(K, cfg, x, dev, reps=200):
+    """Index + top-k of a decode workload with the scores stored as bf16 (the
+    pages' FP32 -> BF16 index-score quantisation) against float32 scores: the
+    time of each (CUDA-graph replays, events on the launching stream) and the
+    recall of the float32 selection."""
+    from compressed_sparse_long_05_b300 import path as P
+    qI, qI_sf, Kt, K_sf = P._indexer_args(x)
+    B, N = cfg["B"], cfg["N"]
+    stream = torch.cuda.Stream(device=dev)
+    res = {}
+    sel = {}
+    for name, dt in (("f32", torch.float32), ("bf16", torch.bfloat16)):
+        scores = torch.empty((B, 1, N), dtype=dt, device=dev)
+        idx = torch.empty((B, 1, cfg["k"]), dtype=torch.int32, device=dev)
+        ws = None
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                _, _, ws = K.csa_index_topk(qI, x["w"], Kt, cfg["k"], cfg["m"], x["q_pos"], qI_sf=qI_sf,
+                                            K_sf=K_sf, scores=scores, idx=idx, ws=ws, score_dtype=dt)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            K.csa_index_topk(qI, x["w"], Kt, cfg["k"], cfg["m"], x["q_pos"], qI_sf=qI_sf, K_sf=K_sf,
+                             scores=scores, idx=idx, ws=ws, score_dtype=dt)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(10):
+                g.replay()
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+        e1.synchronize()
+        res[name + "_index_topk_ms"] = round(e0.elapsed_time(e1) / reps, 5)
+        sel[name] = idx.cpu().numpy()
+        del g
+    K.device_error()
+    rec = []
+    for b in range(B):
+        a32 = set(sel["f32"][b, 0].tolist()) - {-1}
+        a16 = set(sel["bf16"][b, 0].tolist()) - {-1}
+        rec.append(len(a32 & a16) / max(1, len(a32)))
+    res["recall_of_f32_selection"] = round(float(np.mean(rec)), 5)
+    res["speedup"] = round(res["f32_index_topk_ms"] / res["bf16_index_topk_ms"], 3)
+    res["note"] = ("one decode batch of the workload replayed on the same inputs (its 34 MB of keys stay "
+                   "in L2), so these are warm-cache times; the pages report a 2x faster selector at 99.7% "
+                   "recall on the trained model's scores")
+    return res
 
 
 def e2e_leg(K, cfg, x, buf, stream, args, dev):

@@ -51,9 +51,9 @@ _SIGS = {
     "csa_compress": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
     "csa_compress_ex": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                         ctypes.POINTER(CompressOpts), _P],
-    "csa_index": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
-    "csa_topk": [_P, _P, _P, _I, _I, _I, _I, _I, _P],
-    "csa_index_topk": [_P, _P, _P, _P, _P, _P, _P, _P] + [_I] * 8 + [_P, _Z, _P],
+    "csa_index": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
+    "csa_topk": [_P, _I, _P, _P, _I, _I, _I, _I, _I, _P],
+    "csa_index_topk": [_P, _P, _P, _P, _P, _P, _P, _I, _P] + [_I] * 8 + [_P, _Z, _P],
     "csa_index_topk_workspace_size": [_I] * 4,
     "csa_attend": [_P, KV, _P, KV, _P, _P, _P, _P] + [_I] * 10 + [_F, _P, _Z, _P],
     "hca_attend": [_P, KV, KV, _P, _P, _P, _P] + [_I] * 9 + [_F, _P, _Z, _P],
@@ -180,10 +180,11 @@ def csa_compress(Ca, Za, m, Cb=None, Zb=None, Ba=None, Bb=None, out=None, rms_no
     return out
 
 
-def csa_index(qI, w, K, m, q_pos, qI_sf=None, K_sf=None, scores=None):
-    """Indexer scores [B, Tq, N] float32 (-inf where not visible).
+def csa_index(qI, w, K, m, q_pos, qI_sf=None, K_sf=None, scores=None, score_dtype=torch.float32):
+    """Indexer scores [B, Tq, N] (-inf where not visible), float32 or bf16.
 
-    ``q_pos``: query positions (see :func:`positions`)."""
+    ``q_pos``: query positions (see :func:`positions`).  ``score_dtype``
+    torch.bfloat16 stores every score rounded to bf16."""
     fp4 = qI.dtype == torch.uint8
     B, Tq, H = qI.shape[:3]
     c = qI.shape[3] * (2 if fp4 else 1)
@@ -191,23 +192,26 @@ def csa_index(qI, w, K, m, q_pos, qI_sf=None, K_sf=None, scores=None):
     dt = DT_E2M1_BLOCK16 if fp4 else _dt(qI)
     qp = positions(q_pos, B, Tq, qI.device)
     if scores is None:
-        scores = torch.empty((B, Tq, N), dtype=torch.float32, device=qI.device)
+        scores = torch.empty((B, Tq, N), dtype=score_dtype, device=qI.device)
     _check("csa_index", lib().csa_index(_p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(qp),
-                                        _p(scores), B, Tq, N, H, c, m, dt, _stream()))
+                                        _p(scores), _dt(scores), B, Tq, N, H, c, m, dt, _stream()))
     return scores
 
 
 def csa_topk(scores, k, m, q_pos, idx=None):
-    """Selected entry indices [B, Tq, k] int32, ascending, -1 padded."""
+    """Selected entry indices [B, Tq, k] int32, ascending, -1 padded (float32 or
+    bf16 scores)."""
     B, Tq, N = scores.shape
     qp = positions(q_pos, B, Tq, scores.device)
     if idx is None:
         idx = torch.empty((B, Tq, k), dtype=torch.int32, device=scores.device)
-    _check("csa_topk", lib().csa_topk(_p(scores), _p(qp), _p(idx), B, Tq, N, k, m, _stream()))
+    _check("csa_topk", lib().csa_topk(_p(scores), _dt(scores), _p(qp), _p(idx), B, Tq, N, k, m,
+                                      _stream()))
     return idx
 
 
-def csa_index_topk(qI, w, K, k, m, q_pos, qI_sf=None, K_sf=None, scores=None, idx=None, ws=None):
+def csa_index_topk(qI, w, K, k, m, q_pos, qI_sf=None, K_sf=None, scores=None, idx=None, ws=None,
+                   score_dtype=torch.float32):
     """Indexer scores and the top-k index sets of one call (same results as
     csa_index then csa_topk); returns (scores, idx, ws).
 
@@ -220,15 +224,15 @@ def csa_index_topk(qI, w, K, k, m, q_pos, qI_sf=None, K_sf=None, scores=None, id
     N = K.shape[1]
     dt = DT_E2M1_BLOCK16 if fp4 else _dt(qI)
     if scores is None:
-        scores = torch.empty((B, Tq, N), dtype=torch.float32, device=qI.device)
+        scores = torch.empty((B, Tq, N), dtype=score_dtype, device=qI.device)
     if idx is None:
         idx = torch.empty((B, Tq, k), dtype=torch.int32, device=qI.device)
     qp = positions(q_pos, B, Tq, qI.device)
     nbytes = lib().csa_index_topk_workspace_size(B, Tq, N, dt)
     ws = _workspace(ws, nbytes, qI.device, zero=True)   # histograms start zero; calls leave them zero
     _check("csa_index_topk", lib().csa_index_topk(
-        _p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(qp), _p(scores), _p(idx), B, Tq, N, H, c, m,
-        k, dt, _p(ws) if nbytes else None, nbytes, _stream()))
+        _p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(qp), _p(scores), _dt(scores), _p(idx), B, Tq,
+        N, H, c, m, k, dt, _p(ws) if nbytes else None, nbytes, _stream()))
     return scores, idx, ws
 
 

@@ -204,12 +204,13 @@ csa_status_t plan_index(csa::IndexTcArgs& a, int QT, int B, int Tq, int N) {
 
 template <int H>
 csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w, const void* K,
-                              const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
-                              int N, int m, uint32_t* hist, cudaStream_t stream) {
+                              const void* K_sf, const int32_t* q_pos, void* scores, int scores_bf16,
+                              int B, int Tq, int N, int m, uint32_t* hist, cudaStream_t stream) {
   csa::IndexFp4Args fa;
   memset(&fa, 0, sizeof(fa));
   csa::IndexTcArgs& a = fa.t;
-  a.w = w; a.scores = scores; a.q_pos = q_pos; a.B = B; a.Tq = Tq; a.N = N; a.m = m;
+  a.w = w; a.scores = scores; a.scores_bf16 = scores_bf16; a.q_pos = q_pos;
+  a.B = B; a.Tq = Tq; a.N = N; a.m = m;
   csa_status_t st = plan_index(a, 128 / H, B, Tq, N);
   if (st != CSA_OK) return st;
   if ((long long)B * N >= 0x7fffffffLL || (long long)B * Tq * H >= 0x7fffffffLL)
@@ -242,12 +243,13 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
 
 template <int H, int C>
 csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, const int32_t* q_pos,
-                             float* scores, int B, int Tq, int N, int m, uint32_t* hist,
-                             cudaStream_t stream, unsigned long long wait_ns = 0,
+                             void* scores, int scores_bf16, int B, int Tq, int N, int m,
+                             uint32_t* hist, cudaStream_t stream, unsigned long long wait_ns = 0,
                              int skip_load_plus1 = 0) {
   csa::IndexTcArgs a;
   memset(&a, 0, sizeof(a));
-  a.w = w; a.scores = scores; a.q_pos = q_pos; a.B = B; a.Tq = Tq; a.N = N; a.m = m;
+  a.w = w; a.scores = scores; a.scores_bf16 = scores_bf16; a.q_pos = q_pos;
+  a.B = B; a.Tq = Tq; a.N = N; a.m = m;
   a.wait_ns = wait_ns;
   a.skip_load_plus1 = skip_load_plus1;
   csa_status_t st = plan_index(a, 256 / H, B, Tq, N);
@@ -380,10 +382,10 @@ bool tc_attend_shape(int n_h, int d, int r, int kv_dtype) {
          (kv_dtype == CSA_DT_BF16 || kv_dtype == CSA_DT_E4M3_BF16ROPE);
 }
 
-template <int NT, int CL, int BITS1>
+template <int NT, int CL, int BITS1, int KEYLO>
 csa_status_t launch_topk2_cfg(const csa::Topk2Args& a, int rows, size_t smem, cudaStream_t st,
                               bool pdl) {
-  auto kern = csa::topk2_kernel<NT, CL, BITS1>;
+  auto kern = csa::topk2_kernel<NT, CL, BITS1, KEYLO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "csa_topk attr");
   if (CL > 8) {
@@ -409,16 +411,23 @@ csa_status_t launch_topk2_cfg(const csa::Topk2Args& a, int rows, size_t smem, cu
   return CSA_OK;
 }
 
-template <int NT, int BITS1>
+template <int NT, int BITS1, int KEYLO>
 csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t smem, cudaStream_t st,
                              bool pdl) {
   switch (CL) {
-    case 1: return launch_topk2_cfg<NT, 1, BITS1>(a, rows, smem, st, pdl);
-    case 2: return launch_topk2_cfg<NT, 2, BITS1>(a, rows, smem, st, pdl);
-    case 4: return launch_topk2_cfg<NT, 4, BITS1>(a, rows, smem, st, pdl);
-    case 8: return launch_topk2_cfg<NT, 8, BITS1>(a, rows, smem, st, pdl);
-    default: return launch_topk2_cfg<NT, 16, BITS1>(a, rows, smem, st, pdl);
+    case 1: return launch_topk2_cfg<NT, 1, BITS1, KEYLO>(a, rows, smem, st, pdl);
+    case 2: return launch_topk2_cfg<NT, 2, BITS1, KEYLO>(a, rows, smem, st, pdl);
+    case 4: return launch_topk2_cfg<NT, 4, BITS1, KEYLO>(a, rows, smem, st, pdl);
+    case 8: return launch_topk2_cfg<NT, 8, BITS1, KEYLO>(a, rows, smem, st, pdl);
+    default: return launch_topk2_cfg<NT, 16, BITS1, KEYLO>(a, rows, smem, st, pdl);
   }
+}
+
+template <int BITS1, int KEYLO>
+csa_status_t launch_topk2_keys(const csa::Topk2Args& a, bool wide, int CL, int rows, size_t smem,
+                               cudaStream_t st, bool pdl) {
+  return wide ? launch_topk2_nt<1024, BITS1, KEYLO>(a, CL, rows, smem, st, pdl)
+              : launch_topk2_nt<512, BITS1, KEYLO>(a, CL, rows, smem, st, pdl);
 }
 
 // Cluster size for a few decode rows of 8K..32K keys whose first histogram the
@@ -431,8 +440,8 @@ csa_status_t launch_topk2_nt(const csa::Topk2Args& a, int CL, int rows, size_t s
 // CTAs (rows up to 16 x 32768 entries); 1024 threads per CTA when few CTAs
 // run, else 512.  `hist` (optional): per-row histograms of the first
 // IDX_HBITS key bits of the visible scores, built by the index kernel.
-csa_status_t launch_topk2(const float* scores, const int32_t* q_pos, int32_t* idx, int rows, int Tq,
-                          int N, int k, int m, uint32_t* hist, cudaStream_t st) {
+csa_status_t launch_topk2(const void* scores, int scores_bf16, const int32_t* q_pos, int32_t* idx,
+                          int rows, int Tq, int N, int k, int m, uint32_t* hist, cudaStream_t st) {
   int CL = 1;
   if (N > 32768) {
     CL = 8;
@@ -454,10 +463,10 @@ csa_status_t launch_topk2(const float* scores, const int32_t* q_pos, int32_t* id
   csa::Topk2Args a{scores, idx, q_pos, Tq, N, k, m, slice, cand_cap, hist};
   const bool wide = (long long)rows * CL <= 2LL * sm_count();
   const bool pdl = kProgrammaticLaunch;
-  if (hist) return wide ? launch_topk2_nt<1024, csa::IDX_HBITS>(a, CL, rows, smem, st, pdl)
-                        : launch_topk2_nt<512, csa::IDX_HBITS>(a, CL, rows, smem, st, pdl);
-  return wide ? launch_topk2_nt<1024, csa::TK2_BITS1>(a, CL, rows, smem, st, pdl)
-              : launch_topk2_nt<512, csa::TK2_BITS1>(a, CL, rows, smem, st, pdl);
+  if (hist) return scores_bf16 ? launch_topk2_keys<csa::IDX_HBITS, 16>(a, wide, CL, rows, smem, st, pdl)
+                               : launch_topk2_keys<csa::IDX_HBITS, 0>(a, wide, CL, rows, smem, st, pdl);
+  return scores_bf16 ? launch_topk2_keys<csa::TK2_BITS1, 16>(a, wide, CL, rows, smem, st, pdl)
+                     : launch_topk2_keys<csa::TK2_BITS1, 0>(a, wide, CL, rows, smem, st, pdl);
 }
 
 }  // namespace
@@ -555,55 +564,58 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
 
 // ---------------------------------------------------------------------------
 static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w, const void* K,
-                              const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
-                              int N, int H, int c, int m, int dtype, uint32_t* hist, void* stream) {
+                              const void* K_sf, const int32_t* q_pos, void* scores, int score_dtype,
+                              int B, int Tq, int N, int H, int c, int m, int dtype, uint32_t* hist,
+                              void* stream) {
   if (B < 0 || Tq < 0 || N < 0 || H <= 0 || c <= 0 || m <= 0) return CSA_ERR_INVALID_ARG;
+  if (score_dtype != CSA_DT_F32 && score_dtype != CSA_DT_BF16) return CSA_ERR_UNSUPPORTED;
+  const int sb = score_dtype == CSA_DT_BF16 ? 1 : 0;
   if (B == 0 || Tq == 0 || N == 0) return CSA_OK;
   if (!qI || !w || !K || !scores) return CSA_ERR_INVALID_ARG;
-  if (q_pos && !aligned(q_pos, 4)) return CSA_ERR_INVALID_ARG;
+  if ((q_pos && !aligned(q_pos, 4)) || !aligned(scores, sb ? 2 : 4)) return CSA_ERR_INVALID_ARG;
   if (dtype == CSA_DT_F32) {
     if (c > 256) return CSA_ERR_UNSUPPORTED;
     csa::IndexF32Args a{reinterpret_cast<const float*>(qI), w, reinterpret_cast<const float*>(K),
-                        scores, q_pos, Tq, N, H, c, m};
+                        scores, q_pos, sb, Tq, N, H, c, m};
     dim3 grid((N + 7) / 8, B * Tq);
     cudaError_t e = launch_ex(csa::index_f32_kernel, grid, dim3(256), 0, S(stream), 1, a);
     if (e != cudaSuccess) return cuda_fail(e, "csa_index f32 launch");
     return CSA_OK;
   }
   if (dtype == CSA_DT_BF16) {
-    if (!aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4) || !aligned(scores, 4))
-      return CSA_ERR_INVALID_ARG;
+    if (!aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4)) return CSA_ERR_INVALID_ARG;
     if (H == 64 && c == 128)
-      return launch_index_tc<64, 128>(qI, w, K, q_pos, scores, B, Tq, N, m, hist, S(stream));
+      return launch_index_tc<64, 128>(qI, w, K, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     if (H == 64 && c == 64)
-      return launch_index_tc<64, 64>(qI, w, K, q_pos, scores, B, Tq, N, m, hist, S(stream));
+      return launch_index_tc<64, 64>(qI, w, K, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     if (H == 32 && c == 128)
-      return launch_index_tc<32, 128>(qI, w, K, q_pos, scores, B, Tq, N, m, hist, S(stream));
+      return launch_index_tc<32, 128>(qI, w, K, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     if (H == 128 && c == 128)
-      return launch_index_tc<128, 128>(qI, w, K, q_pos, scores, B, Tq, N, m, hist, S(stream));
+      return launch_index_tc<128, 128>(qI, w, K, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
   if (dtype == CSA_DT_E2M1_BLOCK16) {
     if (!qI_sf || !K_sf) return CSA_ERR_INVALID_ARG;
     if (!aligned(qI, 16) || !aligned(K, 16) || !aligned(qI_sf, 16) || !aligned(K_sf, 16) ||
-        !aligned(w, 4) || !aligned(scores, 4))
+        !aligned(w, 4))
       return CSA_ERR_INVALID_ARG;
     if (c != csa::FP4_C) return CSA_ERR_UNSUPPORTED;
     if (H == 64)
-      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, m, hist, S(stream));
+      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     if (H == 32)
-      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, m, hist, S(stream));
+      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     if (H == 128)
-      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, m, hist, S(stream));
+      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
   return CSA_ERR_UNSUPPORTED;
 }
 
 csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
-                       const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
-                       int N, int H, int c, int m, int dtype, void* stream) {
-  return index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, H, c, m, dtype, nullptr, stream);
+                       const void* K_sf, const int32_t* q_pos, void* scores, int score_dtype,
+                       int B, int Tq, int N, int H, int c, int m, int dtype, void* stream) {
+  return index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, score_dtype, B, Tq, N, H, c, m, dtype,
+                    nullptr, stream);
 }
 
 csa_status_t csa_selftest_wait_timeout(const void* qI, const float* w, const void* K,
@@ -614,7 +626,7 @@ csa_status_t csa_selftest_wait_timeout(const void* qI, const float* w, const voi
   if (!qI || !w || !K || !scores || !aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4) ||
       !aligned(scores, 4) || (q_pos && !aligned(q_pos, 4)))
     return CSA_ERR_INVALID_ARG;
-  return launch_index_tc<64, 128>(qI, w, K, q_pos, scores, B, Tq, N, m, nullptr, S(stream),
+  return launch_index_tc<64, 128>(qI, w, K, q_pos, scores, 0, B, Tq, N, m, nullptr, S(stream),
                                   1000ull * (unsigned long long)limit_us, 1);
 }
 
@@ -630,14 +642,15 @@ size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype) {
 }
 
 csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, const void* K,
-                            const void* K_sf, const int32_t* q_pos, float* scores, int32_t* idx,
-                            int B, int Tq, int N, int H, int c, int m, int k, int dtype, void* ws,
-                            size_t ws_bytes, void* stream) {
+                            const void* K_sf, const int32_t* q_pos, void* scores, int score_dtype,
+                            int32_t* idx, int B, int Tq, int N, int H, int c, int m, int k,
+                            int dtype, void* ws, size_t ws_bytes, void* stream) {
   if (k < 1 || k > 4096) return CSA_ERR_INVALID_ARG;
   if (!index_topk_fused(B, Tq, N, dtype)) {
-    csa_status_t st = csa_index(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, H, c, m, dtype, stream);
+    csa_status_t st = csa_index(qI, qI_sf, w, K, K_sf, q_pos, scores, score_dtype, B, Tq, N, H, c,
+                                m, dtype, stream);
     if (st != CSA_OK) return st;
-    return csa_topk(scores, q_pos, idx, B, Tq, N, k, m, stream);
+    return csa_topk(scores, score_dtype, q_pos, idx, B, Tq, N, k, m, stream);
   }
   if (!idx || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
   const size_t need = csa_index_topk_workspace_size(B, Tq, N, dtype);
@@ -645,26 +658,31 @@ csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, c
   // the histograms start zero (caller's first use) and the selector clears each
   // row's after reading it, so no clearing pass runs here
   uint32_t* hist = reinterpret_cast<uint32_t*>(ws);
-  csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, B, Tq, N, H, c, m, dtype, hist,
-                               stream);
+  csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, score_dtype, B, Tq, N, H, c,
+                               m, dtype, hist, stream);
   if (st != CSA_OK) return st;
-  return launch_topk2(scores, q_pos, idx, B * Tq, Tq, N, k, m, hist, S(stream));
+  return launch_topk2(scores, score_dtype == CSA_DT_BF16, q_pos, idx, B * Tq, Tq, N, k, m, hist,
+                      S(stream));
 }
 
 // ---------------------------------------------------------------------------
-csa_status_t csa_topk(const float* scores, const int32_t* q_pos, int32_t* idx, int B, int Tq,
-                      int N, int k, int m, void* stream) {
+csa_status_t csa_topk(const void* scores, int score_dtype, const int32_t* q_pos, int32_t* idx, int B,
+                      int Tq, int N, int k, int m, void* stream) {
   if (B < 0 || Tq < 0 || N < 0 || k < 1 || k > 4096 || m <= 0) return CSA_ERR_INVALID_ARG;
+  if (score_dtype != CSA_DT_F32 && score_dtype != CSA_DT_BF16) return CSA_ERR_UNSUPPORTED;
+  const int sb = score_dtype == CSA_DT_BF16 ? 1 : 0;
   if (B == 0 || Tq == 0) return CSA_OK;
   if (!idx || (N > 0 && !scores)) return CSA_ERR_INVALID_ARG;
-  if (!aligned(scores, 4) || !aligned(idx, 4) || (q_pos && !aligned(q_pos, 4)))
+  if (!aligned(scores, sb ? 2 : 4) || !aligned(idx, 4) || (q_pos && !aligned(q_pos, 4)))
     return CSA_ERR_INVALID_ARG;
   const int rows = B * Tq;
   // few long decode rows up to 32768 entries: 8-bit radix passes over a 16-CTA
   // cluster; everything else up to 16 x 32768 entries: the candidate-filtering
   // selector (measured faster there: many short rows, and rows past 32768)
-  if (!(N > 8192 && N <= 32768 && rows < 64) && N <= 16 * 32768)
-    return launch_topk2(scores, q_pos, idx, rows, Tq, N, k, m, nullptr, S(stream));
+  // (bf16 scores always take the candidate-filtering selector)
+  if ((sb || !(N > 8192 && N <= 32768 && rows < 64)) && N <= 16 * 32768)
+    return launch_topk2(scores, sb, q_pos, idx, rows, Tq, N, k, m, nullptr, S(stream));
+  if (sb) return CSA_ERR_UNSUPPORTED;   // the 8-bit radix selector below reads float32 scores
   // rows longer than 16 slices of 32768 keys: 8-bit radix passes over up to 16 SMs
   int CL = 1;
   if (N > 8192 && rows < 64) CL = rows <= 9 ? 16 : 8;
@@ -672,7 +690,7 @@ csa_status_t csa_topk(const float* scores, const int32_t* q_pos, int32_t* idx, i
   slice = (slice + 3) & ~3;
   const size_t smem = (size_t)slice * sizeof(uint32_t);
   if (smem > 200 * 1024) return CSA_ERR_UNSUPPORTED;
-  csa::TopkArgs a{scores, idx, q_pos, Tq, N, k, m, slice};
+  csa::TopkArgs a{reinterpret_cast<const float*>(scores), idx, q_pos, Tq, N, k, m, slice};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows * CL);
   cfg.blockDim = dim3(csa::TOPK_THREADS);

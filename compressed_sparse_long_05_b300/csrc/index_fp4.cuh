@@ -349,7 +349,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
       ++nitem;
       for (int j = x.j0; j < x.j1; ++j) {
         const int s = j * IDX_TILE + q4 * 32 + lane;
-        float* srow = a.scores + ((size_t)x.b * a.Tq + x.t0) * a.N + s;
+        const size_t srow = ((size_t)x.b * a.Tq + x.t0) * a.N + s;   // element of this lane's first score
         if (j < x.jv) {
           const uint32_t mine = (iacc & 1) == (uint32_t)grp;
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
@@ -361,15 +361,15 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           for (int qi = 0; qi < x.nq; ++qi) {
             const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
             const int vis = item_vis(a, x, qi);
-            if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
-            if (a.hist) hist_add(wh, acc, s < vis);
+            if (s < a.N) store_score(a.scores, a.scores_bf16, srow + (size_t)qi * a.N, s < vis ? acc : -INFINITY);
+            if (a.hist) hist_add(wh, stored_score(a.scores_bf16, acc), s < vis);
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + buf);
         } else if ((j & 1) == grp) {
           for (int qi = 0; qi < x.nq; ++qi)
-            if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
+            if (s < a.N) store_score(a.scores, a.scores_bf16, srow + (size_t)qi * a.N, -INFINITY);
         }
       }
       if (a.hist) {

@@ -31,7 +31,8 @@ constexpr int IDX_TILE = 128;   // entries per tile (MMA M)
 
 struct IndexTcArgs {
   const float* w;        // [B, Tq, H]
-  float* scores;         // [B, Tq, N]
+  void* scores;          // [B, Tq, N] float32, or bf16 when scores_bf16
+  int scores_bf16;       // 1 = scores rounded to bf16 (the histogram counts the rounded values)
   const int32_t* q_pos;  // [B, Tq] query positions (null: t = i)
   int B, Tq, N, m;
   int QT;                // queries per group (QT * H <= 256)
@@ -53,6 +54,16 @@ struct IndexTcArgs {
 // top-k selector: bin = top IDX_HBITS bits of the order-preserving key.
 constexpr int IDX_HBITS = 11;
 constexpr int IDX_HBINS = 1 << IDX_HBITS;
+
+// Store one score (float32, or rounded to bf16) at element e of the score rows.
+CSA_DEVINL void store_score(void* scores, int bf16, size_t e, float v) {
+  if (bf16) reinterpret_cast<__nv_bfloat16*>(scores)[e] = __float2bfloat16_rn(v);
+  else reinterpret_cast<float*>(scores)[e] = v;
+}
+// The value a stored score holds (bf16 scores: the rounded value), for the histogram.
+CSA_DEVINL float stored_score(int bf16, float v) {
+  return bf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
 
 // One warp's visible scores of one tile into its shared histogram.
 CSA_DEVINL void hist_add(uint32_t* wh, float score, bool visible) {
@@ -318,7 +329,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
       __syncwarp();
       for (int j = x.j0; j < x.j1; ++j) {
         const int s = j * IDX_TILE + q4 * 32 + lane;
-        float* srow = a.scores + ((size_t)x.b * a.Tq + x.t0) * a.N + s;
+        const size_t srow = ((size_t)x.b * a.Tq + x.t0) * a.N + s;   // element of this lane's first score
         if (j < x.jv) {
           const uint32_t mine = (iacc & 1) == (uint32_t)grp;
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
@@ -330,8 +341,8 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           for (int qi = 0; qi < x.nq; ++qi) {
             const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
             const int vis = item_vis(a, x, qi);
-            if (s < a.N) srow[(size_t)qi * a.N] = s < vis ? acc : -INFINITY;
-            if (a.hist) hist_add(wh, acc, s < vis);
+            if (s < a.N) store_score(a.scores, a.scores_bf16, srow + (size_t)qi * a.N, s < vis ? acc : -INFINITY);
+            if (a.hist) hist_add(wh, stored_score(a.scores_bf16, acc), s < vis);
           }
           tc_fence_before();
           __syncwarp();
@@ -339,7 +350,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           if (ew == 0 && lane == 0) CSA_TRACE_MARK(iacc <= 2 ? 38 : 39);
         } else if ((j & 1) == grp) {
           for (int qi = 0; qi < x.nq; ++qi)
-            if (s < a.N) srow[(size_t)qi * a.N] = -INFINITY;
+            if (s < a.N) store_score(a.scores, a.scores_bf16, srow + (size_t)qi * a.N, -INFINITY);
         }
       }
       if (ew == 0 && lane == 0) CSA_TRACE_MARK(40);

@@ -14,8 +14,9 @@ namespace csa {
 // indexer: one warp per (row, entry s); lanes split the H*c products
 // ----------------------------------------------------------------------------
 struct IndexF32Args {
-  const float* q; const float* w; const float* K; float* scores;
+  const float* q; const float* w; const float* K; void* scores;
   const int32_t* q_pos;            // [B, Tq] (null: t = i)
+  int scores_bf16;                 // 1 = scores stored as bf16
   int Tq, N, H, c, m;
 };
 
@@ -29,9 +30,12 @@ __global__ void __launch_bounds__(256) index_f32_kernel(IndexF32Args a) {
   const int b = row / a.Tq, i = row % a.Tq;
   const long long t = query_pos(a.q_pos, row, i);
   if (t < 0 && s == 0 && lane == 0) csa_flag_error(ERRBIT_BAD_INDEX);
-  float* out = a.scores + (size_t)row * a.N + s;
+  const size_t out = (size_t)row * a.N + s;
   if (t < 0 || (long long)(s + 1) * a.m > t + 1) {   // not visible
-    if (lane == 0) *out = -INFINITY;
+    if (lane == 0) {
+      if (a.scores_bf16) reinterpret_cast<__nv_bfloat16*>(a.scores)[out] = __float2bfloat16_rn(-INFINITY);
+      else reinterpret_cast<float*>(a.scores)[out] = -INFINITY;
+    }
     return;
   }
   const float* qr = a.q + (size_t)row * a.H * a.c;
@@ -45,7 +49,10 @@ __global__ void __launch_bounds__(256) index_f32_kernel(IndexF32Args a) {
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     acc = fmaf(wr[h], fmaxf(dot, 0.f), acc);
   }
-  if (lane == 0) *out = acc;
+  if (lane == 0) {
+    if (a.scores_bf16) reinterpret_cast<__nv_bfloat16*>(a.scores)[out] = __float2bfloat16_rn(acc);
+    else reinterpret_cast<float*>(a.scores)[out] = acc;
+  }
 }
 
 // ----------------------------------------------------------------------------

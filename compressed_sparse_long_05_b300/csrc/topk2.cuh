@@ -13,8 +13,10 @@
 //     selected outright, krem = k - #(keys above b1) remain.
 //  3. Keys in b1 are copied to a candidate list (if it fits; otherwise the
 //     remaining passes filter the whole slice by the b1 prefix).
-//  4. Three radix passes (7, 7 and 6 bits) over the candidates find the exact
-//     k-th largest key T and the number of keys equal to T to take.
+//  4. Radix passes of 7 bits (the last one narrower) over the candidates find
+//     the exact k-th largest key T and the number of keys equal to T to take:
+//     three for float32 scores, one for bf16 scores (their keys have 16 bits,
+//     so only 16 - BITS1 remain below the first digit).
 //  5. Two ballot sweeps write every key > T and the lowest-index keys == T in
 //     ascending index order: warp totals -> one block scan -> cluster prefix.
 // Ties are broken toward the lower entry index.
@@ -29,7 +31,7 @@ constexpr int TK2_BITS1 = 12;                 // first digit when the kernel bui
 constexpr int TK2_MAXBINS = 1 << TK2_BITS1;
 
 struct Topk2Args {
-  const float* scores;
+  const void* scores;     // [rows][N] float32, or bf16 for the KEYLO = 16 kernels
   int32_t* idx;
   const int32_t* q_pos;   // [rows] query positions (null: t = i)
   int Tq, N, k, m;
@@ -76,7 +78,9 @@ CSA_DEVINL int tk2_block_scan(int x, int* sh, int* total) {
   return r;
 }
 
-template <int NT, int CL, int BITS1>
+// KEYLO: the lowest key bit the scores carry (0: float32 scores; 16: bf16
+// scores, read as the upper half of a float32 whose lower half is zero).
+template <int NT, int CL, int BITS1, int KEYLO = 0>
 __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   if (threadIdx.x == 0) { CSA_TRACE_WALL(48); CSA_TRACE_MARK(49); }
   pdl_enter();
@@ -99,7 +103,8 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   const long long t = query_pos(a.q_pos, row, i);
   int vis = t < 0 ? 0 : (int)min((long long)a.N, (t + 1) / a.m);
   if (t < 0 && rank == 0 && threadIdx.x == 0) csa_flag_error(ERRBIT_BAD_INDEX);
-  const float* srow = a.scores + (size_t)row * a.N;
+  const float* srow = reinterpret_cast<const float*>(a.scores) + (size_t)row * a.N;   // KEYLO = 0
+  const uint16_t* hrow = reinterpret_cast<const uint16_t*>(a.scores) + (size_t)row * a.N;   // KEYLO = 16
   int32_t* orow = a.idx + (size_t)row * a.k;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
@@ -149,17 +154,33 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   if (tid == 0) CSA_TRACE_MARK(50);
   // ---- 1. load the slice (every copy in flight at once), then keys + first-digit histogram ----
   {
-    const bool vec = ((lo & 3) == 0) && ((reinterpret_cast<uintptr_t>(srow) & 15) == 0);
-    const int n4 = vec ? (n >> 2) : 0;
-    const uint32_t kbase = (uint32_t)__cvta_generic_to_shared(keys);
-    for (int j = tid; j < n4; j += NT)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kbase + 16u * j),
-                   "l"(srow + lo + 4 * j) : "memory");
-    for (int j = 4 * n4 + tid; j < n; j += NT)
-      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(kbase + 4u * j),
-                   "l"(srow + lo + j) : "memory");
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if constexpr (KEYLO == 0) {
+      const bool vec = ((lo & 3) == 0) && ((reinterpret_cast<uintptr_t>(srow) & 15) == 0);
+      const int n4 = vec ? (n >> 2) : 0;
+      const uint32_t kbase = (uint32_t)__cvta_generic_to_shared(keys);
+      for (int j = tid; j < n4; j += NT)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kbase + 16u * j),
+                     "l"(srow + lo + 4 * j) : "memory");
+      for (int j = 4 * n4 + tid; j < n; j += NT)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(kbase + 4u * j),
+                     "l"(srow + lo + j) : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    } else {
+      // bf16 scores: 8 per 16-byte load, widened to the float32 bit pattern
+      const bool vec = ((lo & 7) == 0) && ((reinterpret_cast<uintptr_t>(hrow) & 15) == 0);
+      const int n8 = vec ? (n >> 3) : 0;
+      for (int j = tid; j < n8; j += NT) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(hrow + lo) + j);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          keys[8 * j + 2 * e] = w[e] << 16;
+          keys[8 * j + 2 * e + 1] = w[e] & 0xffff0000u;
+        }
+      }
+      for (int j = 8 * n8 + tid; j < n; j += NT) keys[j] = (uint32_t)__ldg(hrow + lo + j) << 16;
+    }
     __syncthreads();
     for (int j0 = s0; j0 < s1; j0 += 32) {
       const int j = j0 + lane;
@@ -167,6 +188,7 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
       uint32_t key = 0u;
       if (act) {
         key = float_to_key(__uint_as_float(keys[j]));
+        if constexpr (KEYLO == 16) key &= 0xffff0000u;   // a negative score's flip fills the low half
         keys[j] = key;
       }
       if (hist_in) continue;                          // the index kernel built the histogram
@@ -275,11 +297,13 @@ __global__ void __launch_bounds__(NT) topk2_kernel(const Topk2Args a) {
   // ---- 4. three radix passes over the candidates (or the b1-filtered slice) ----
   uint32_t prefix = b1 << SHIFT1;
   uint32_t pmask = 0xffffffffu << SHIFT1;
+  // the bits [KEYLO, SHIFT1) below the first digit, 7 at a time from the top
+  constexpr int NPASS = (SHIFT1 - KEYLO + 6) / 7;
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    // the SHIFT1 (20 or 21) remaining bits as digits of 7, 7 and 6 or 7 bits
-    const int sh = pass == 0 ? SHIFT1 - 7 : (pass == 1 ? SHIFT1 - 14 : 0);
-    const int wd = pass == 2 ? SHIFT1 - 14 : 7;
+  for (int pass = 0; pass < NPASS; ++pass) {
+    const int hi_bit = SHIFT1 - 7 * pass;
+    const int wd = hi_bit - KEYLO < 7 ? hi_bit - KEYLO : 7;
+    const int sh = hi_bit - wd;
     const uint32_t dmask = (1u << wd) - 1u;
     uint32_t* h = hist2[pass];
     for (int j0 = 0; j0 < list_n; j0 += NT) {

@@ -134,24 +134,28 @@ csa_status_t csa_compress_ex(const void* Ca, const void* Cb, const void* Za, con
  *   dtype F32 / BF16: qI [B, Tq, H, c], K [B, N, c]; qI_sf, K_sf unused (NULL).
  *   dtype E2M1_BLOCK16: qI [B, Tq, H, c/2] bytes, qI_sf [B, Tq, H, c/16] bytes,
  *                       K [B, N, c/2] bytes, K_sf [B, N, c/16] bytes.
- *   w: [B, Tq, H] float32.  scores: [B, Tq, N] float32 (every element written).
+ *   w: [B, Tq, H] float32.  scores: [B, Tq, N] (every element written), in
+ *   score_dtype F32, or BF16: each score rounded to bf16 (§3.4: index scores
+ *   quantised from FP32 to BF16 for a faster top-k selector; the selection
+ *   then ranks the rounded scores, ties toward the lower index).
  *   BF16 needs (H, c) in {(64,128), (64,64), (32,128), (128,128)}; E2M1 needs
  *   H in {32,64,128}, c == 128; F32 any H, c <= 256.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
-                       const void* K_sf, const int32_t* q_pos, float* scores, int B, int Tq,
-                       int N, int H, int c, int m, int dtype, void* stream);
+                       const void* K_sf, const int32_t* q_pos, void* scores, int score_dtype,
+                       int B, int Tq, int N, int H, int c, int m, int dtype, void* stream);
 
 /* ---------------------------------------------------------------------------
  * csa_topk — per query row, the k visible entries with the largest scores
  * (§2.3.1 "top-k selector"; C_t = TopK_k(I_t,:)).  Ties are broken toward the
  * lower entry index.  idx[b,i,:] holds the min(k, vis) selected entry indices
  * in ascending order, then -1 up to k.
- *   scores: [B, Tq, N] float32 (only s < vis(t) is read); q_pos: [B, Tq] as
- *   above; idx: [B, Tq, k] int32.  Requires 1 <= k <= 4096.
+ *   scores: [B, Tq, N] in score_dtype F32 or BF16 (only s < vis(t) is read;
+ *   BF16 needs N <= 16 * 32768); q_pos: [B, Tq] as above; idx: [B, Tq, k]
+ *   int32.  Requires 1 <= k <= 4096.
  * ------------------------------------------------------------------------- */
-csa_status_t csa_topk(const float* scores, const int32_t* q_pos, int32_t* idx, int B, int Tq,
-                      int N, int k, int m, void* stream);
+csa_status_t csa_topk(const void* scores, int score_dtype, const int32_t* q_pos, int32_t* idx,
+                      int B, int Tq, int N, int k, int m, void* stream);
 
 /* ---------------------------------------------------------------------------
  * csa_index_topk — csa_index followed by csa_topk in one call, with the same
@@ -160,7 +164,9 @@ csa_status_t csa_topk(const float* scores, const int32_t* q_pos, int32_t* idx, i
  * kernel also counts each visible score's top 11 order-preserving key bits
  * into a per-row histogram, so the selector starts from the threshold bin
  * instead of building that histogram itself (§2.3.1 "Lightning Indexer" and
- * "top-k selector").  Other shapes run the two stages unchanged.
+ * "top-k selector").  Other shapes run the two stages unchanged.  With
+ * score_dtype BF16 the keys have 16 bits, so the selector needs one radix
+ * pass below that histogram's digit instead of three.
  *   ws / ws_bytes: scratch of csa_index_topk_workspace_size(B, Tq, N, dtype)
  *   bytes (16-byte aligned; may be NULL when that size is 0).  It holds the
  *   per-row histograms and must be ZERO-FILLED before its first use; every call
@@ -169,9 +175,9 @@ csa_status_t csa_topk(const float* scores, const int32_t* q_pos, int32_t* idx, i
  *   loop zero-fills it once.  After a failed call, zero-fill it again.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, const void* K,
-                            const void* K_sf, const int32_t* q_pos, float* scores, int32_t* idx,
-                            int B, int Tq, int N, int H, int c, int m, int k, int dtype, void* ws,
-                            size_t ws_bytes, void* stream);
+                            const void* K_sf, const int32_t* q_pos, void* scores, int score_dtype,
+                            int32_t* idx, int B, int Tq, int N, int H, int c, int m, int k,
+                            int dtype, void* ws, size_t ws_bytes, void* stream);
 size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype);
 
 /* ---------------------------------------------------------------------------

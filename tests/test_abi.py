@@ -55,13 +55,16 @@ def test_host_side_argument_errors(L):
     # unsupported dtype / width
     assert L.csa_compress(fake, None, fake, None, None, None, fake, 1, 8, 64, 4, 3, None) == 2
     assert L.csa_compress(fake, None, fake, None, None, None, fake, 1, 8, 60, 4, 1, None) == 2
-    # top-k: k out of range, negative sizes, misaligned positions
-    assert L.csa_topk(fake, None, fake, 1, 1, 100, 0, 4, None) == 1
-    assert L.csa_topk(fake, None, fake, 1, 1, 100, 5000, 4, None) == 1
-    assert L.csa_topk(fake, None, fake, -1, 1, 100, 5, 4, None) == 1
-    assert L.csa_topk(fake, mis, fake, 1, 1, 100, 5, 4, None) == 1
+    # top-k: k out of range, negative sizes, misaligned positions, unknown score type
+    assert L.csa_topk(fake, 0, None, fake, 1, 1, 100, 0, 4, None) == 1
+    assert L.csa_topk(fake, 0, None, fake, 1, 1, 100, 5000, 4, None) == 1
+    assert L.csa_topk(fake, 0, None, fake, -1, 1, 100, 5, 4, None) == 1
+    assert L.csa_topk(fake, 0, mis, fake, 1, 1, 100, 5, 4, None) == 1
+    assert L.csa_topk(fake, 3, None, fake, 1, 1, 100, 5, 4, None) == 2
+    # bf16 scores beyond 16 x 32768 keys per row: the 8-bit selector reads float32 only
+    assert L.csa_topk(fake, 1, None, fake, 1, 1, 600000, 5, 4, None) == 2
     # index: null scores
-    assert L.csa_index(fake, None, fake, fake, None, None, None, 1, 1, 8, 4, 32, 4, 0, None) == 1
+    assert L.csa_index(fake, None, fake, fake, None, None, None, 0, 1, 1, 8, 4, 32, 4, 0, None) == 1
     kv = KV(dtype=1, flags=0, data=0x10000)
     # attend: odd rope dims
     assert L.csa_attend(fake, kv, fake, kv, None, None, fake, fake, 1, 1, 8, 4, 128, 128, 512, 63,
@@ -80,7 +83,7 @@ def test_host_side_argument_errors(L):
     assert L.csa_attend(fake, kv, fake, kv, None, None, fake, fake, 1, 4096, 1024, 64, 4096, 128,
                         512, 64, 4, 128, 10000.0, None, 0, None) == 3
     # empty batch is a no-op
-    assert L.csa_topk(fake, None, fake, 0, 1, 100, 5, 4, None) == 0
+    assert L.csa_topk(fake, 0, None, fake, 0, 1, 100, 5, 4, None) == 0
 
 
 def test_workspace_sizes_follow_the_plan(L):
