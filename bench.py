@@ -429,6 +429,9 @@ def gpu_arm(args, cfg, rank, world, with_e2e=True):
                 for si, n in enumerate(names):
                     stage_ms[n].append(ev[si].elapsed_time(ev[si + 1]))
             else:
+                # keep the GPU busy while the host queues the stages, so the first
+                # stage's time does not include the host's launch latency
+                torch.cuda._sleep(2_000_000)
                 evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
                 evs[0].record()
                 for si, (_, f) in enumerate(steps[s % copies]):

@@ -5,7 +5,7 @@ The stages are C-ABI calls into ``lib/libcsa_b300.so`` (include/csa.h):
 ``path`` composes them into the prefill and decode passes of one layer.
 """
 
-from ._lib import (CsaError, attend_workspace_size, csa_attend, csa_attend_noalloc,  # noqa: F401
-                   csa_compress, csa_grouped_proj,
+from ._lib import (BlockPool, CsaError, Paged, attend_workspace_size, csa_attend,  # noqa: F401
+                   csa_attend_noalloc, csa_compress, csa_grouped_proj,
                    csa_index, csa_index_topk, csa_topk, device_error, hca_attend, lib)
 from . import path  # noqa: F401

@@ -30,15 +30,58 @@ class CsaError(RuntimeError):
         super().__init__(f"{fn}: {STATUS.get(status, status)}" + (f" ({detail})" if detail else ""))
 
 
+class Pages(ctypes.Structure):
+    """csa_pages_t: block table (device int32 [B, max_blocks]) of a paged row set."""
+    _fields_ = [("block_table", ctypes.c_void_p), ("max_blocks", ctypes.c_int32),
+                ("block_rows", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("ring", ctypes.c_int32)]
+
+
 class KV(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("flags", ctypes.c_int32), ("data", ctypes.c_void_p),
-                ("scale", ctypes.c_void_p), ("rope", ctypes.c_void_p)]
+                ("scale", ctypes.c_void_p), ("rope", ctypes.c_void_p), ("pages", Pages)]
 
 
 class CompressOpts(ctypes.Structure):
     _fields_ = [("rms_norm", ctypes.c_int32), ("norm_eps", ctypes.c_float),
                 ("norm_weight", ctypes.c_void_p), ("rope_dims", ctypes.c_int32),
-                ("rope_base", ctypes.c_float)]
+                ("rope_base", ctypes.c_float), ("out_pages", Pages), ("out_entry0", ctypes.c_void_p),
+                ("out_first", ctypes.c_int32)]
+
+
+class Paged:
+    """Rows of a paged cache, or of a per-sequence ring buffer.
+
+    ``pool``: the rows, [num_blocks * block_rows, d] (or the (e4m3, scale,
+    rope) tuple of pools for FP8 rows; for FP4 keys the packed bytes, with the
+    scale bytes passed separately); ``table``: int32 device tensor
+    [B, max_blocks] naming the physical block of each logical block, or None
+    for a flat [B, rows, d] ``pool``; ``rows``: logical rows per sequence (N,
+    or T_win); ``ring``: window rows, token p at logical row p mod rows.
+    """
+
+    def __init__(self, pool, table=None, block_rows=0, rows=None, ring=False):
+        self.pool, self.table, self.block_rows, self.ring = pool, table, block_rows, ring
+        first = pool[0] if isinstance(pool, (tuple, list)) else pool
+        if table is None:
+            self.B, self.rows = first.shape[0], first.shape[1]
+            self.num_blocks = 0
+        else:
+            if table.dtype != torch.int32 or table.dim() != 2 or not table.is_contiguous():
+                raise ValueError("table must be a contiguous int32 [B, max_blocks] tensor")
+            if rows is None:
+                raise ValueError("a paged row set needs its logical row count")
+            self.B, self.rows = table.shape[0], rows
+            self.num_blocks = first.shape[0] // block_rows
+        self.d = None if isinstance(pool, (tuple, list)) else first.shape[-1]
+        if isinstance(pool, (tuple, list)):
+            self.d = pool[0].shape[-1] + pool[2].shape[-1]
+
+    def pages(self):
+        if self.table is None:
+            return Pages(None, 0, 0, 0, 1 if self.ring else 0)
+        return Pages(self.table.data_ptr(), self.table.shape[1], self.block_rows, self.num_blocks,
+                     1 if self.ring else 0)
 
 
 KV_ROTATED = 1
@@ -61,12 +104,21 @@ _SIGS = {
     "csa_attend_workspace_size": [_I] * 13,
     "csa_selftest_wait_timeout": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
     "csa_grouped_proj": [_P, ctypes.c_int64, _P, _P, ctypes.c_int64, _I, _I, _I, _I, _P],
+    "csa_index_paged": [_P, _P, _P, _P, _P, ctypes.POINTER(Pages), _P, _P, _I] + [_I] * 7 + [_P],
+    "csa_index_topk_paged": [_P, _P, _P, _P, _P, ctypes.POINTER(Pages), _P, _P, _I, _P] + [_I] * 8
+                            + [_P, _Z, _P],
+    "csa_block_pool_create": [ctypes.c_int32],
+    "csa_block_pool_destroy": [_P],
+    "csa_block_pool_free_count": [_P],
+    "csa_block_pool_alloc": [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+    "csa_block_pool_release": [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
     "csa_device_error": [_P],
     "csa_status_string": [_I],
     "csa_last_cuda_error": [],
     "csa_version": [],
 }
-_RESTYPES = {"csa_attend_workspace_size": _Z, "csa_index_topk_workspace_size": _Z, "csa_status_string": ctypes.c_char_p,
+_RESTYPES = {"csa_block_pool_create": _P, "csa_block_pool_destroy": None,
+             "csa_block_pool_free_count": ctypes.c_int32, "csa_attend_workspace_size": _Z, "csa_index_topk_workspace_size": _Z, "csa_status_string": ctypes.c_char_p,
              "csa_last_cuda_error": ctypes.c_char_p}
 
 
@@ -112,13 +164,18 @@ def _dt(t):
 
 
 def _kv(rows, rotated=False):
-    """A row set: a float32/bf16 tensor [B, rows, d] or (e4m3 bytes, scale, bf16 rope);
-    ``rotated``: its RoPE dims are already rotated at each entry's position."""
+    """A row set: a float32/bf16 tensor [B, rows, d], (e4m3 bytes, scale, bf16 rope),
+    or a :class:`Paged` of either; ``rotated``: its RoPE dims are already
+    rotated at each entry's position."""
     fl = KV_ROTATED if rotated else 0
+    pg = Pages()
+    if isinstance(rows, Paged):
+        pg = rows.pages()
+        rows = rows.pool
     if isinstance(rows, (tuple, list)):
         nope, scale, rope = rows
-        return KV(DT_E4M3_BF16ROPE, fl, nope.data_ptr(), scale.data_ptr(), rope.data_ptr())
-    return KV(_dt(rows), fl, rows.data_ptr(), None, None)
+        return KV(DT_E4M3_BF16ROPE, fl, nope.data_ptr(), scale.data_ptr(), rope.data_ptr(), pg)
+    return KV(_dt(rows), fl, rows.data_ptr(), None, None, pg)
 
 
 def positions(q_pos, B, Tq, device):
@@ -148,6 +205,8 @@ def window_bases(win_base, B, device):
 
 
 def _rows_shape(rows):
+    if isinstance(rows, Paged):
+        return rows.B, rows.rows, rows.d
     if isinstance(rows, (tuple, list)):
         nope, _, rope = rows
         return nope.shape[0], nope.shape[1], nope.shape[2] + rope.shape[2]
@@ -158,22 +217,35 @@ def _rows_shape(rows):
 
 
 def csa_compress(Ca, Za, m, Cb=None, Zb=None, Ba=None, Bb=None, out=None, rms_norm=False,
-                 norm_eps=0.0, norm_weight=None, rope_dims=0, rope_base=10000.0):
+                 norm_eps=0.0, norm_weight=None, rope_dims=0, rope_base=10000.0, out_entry0=None,
+                 out_first=0):
     """Compressed entries [B, T//m, d] (Cb = Zb = None: HCA, no overlap).
 
     ``rms_norm`` / ``rope_dims``: the optional epilogue of csa_compress_ex
     (RMSNorm of every entry, then RoPE of its last rope_dims dims at its
-    position m(i+1)-1)."""
+    position).  ``out`` may be a :class:`Paged` pool: entry i >= out_first of
+    sequence b then goes to logical row out_entry0[b] + i - out_first
+    (``out_entry0``: int32 [B] device tensor, None = 0; negative: nothing
+    written for that sequence)."""
     B, T, d = Ca.shape
     if out is None:
         out = torch.empty((B, T // m, d), dtype=Ca.dtype, device=Ca.device)
+    if isinstance(out, Paged):
+        opts = CompressOpts(1 if rms_norm else 0, norm_eps,
+                            None if norm_weight is None else norm_weight.data_ptr(), rope_dims,
+                            rope_base, out.pages(), None if out_entry0 is None else out_entry0.data_ptr(),
+                            out_first)
+        _check("csa_compress_ex", lib().csa_compress_ex(
+            _p(Ca), _p(Cb), _p(Za), _p(Zb), _p(Ba), _p(Bb), _p(out.pool), B, T, d, m, _dt(Ca),
+            ctypes.byref(opts), _stream()))
+        return out
     if not rms_norm and not rope_dims:
         _check("csa_compress", lib().csa_compress(_p(Ca), _p(Cb), _p(Za), _p(Zb), _p(Ba), _p(Bb),
                                                   _p(out), B, T, d, m, _dt(Ca), _stream()))
         return out
     opts = CompressOpts(1 if rms_norm else 0, norm_eps,
                         None if norm_weight is None else norm_weight.data_ptr(), rope_dims,
-                        rope_base)
+                        rope_base, Pages(), None, 0)
     _check("csa_compress_ex", lib().csa_compress_ex(
         _p(Ca), _p(Cb), _p(Za), _p(Zb), _p(Ba), _p(Bb), _p(out), B, T, d, m, _dt(Ca),
         ctypes.byref(opts), _stream()))
@@ -188,14 +260,22 @@ def csa_index(qI, w, K, m, q_pos, qI_sf=None, K_sf=None, scores=None, score_dtyp
     fp4 = qI.dtype == torch.uint8
     B, Tq, H = qI.shape[:3]
     c = qI.shape[3] * (2 if fp4 else 1)
-    N = K.shape[1]
+    Kt, kpg, N = _keys(K)
     dt = DT_E2M1_BLOCK16 if fp4 else _dt(qI)
     qp = positions(q_pos, B, Tq, qI.device)
     if scores is None:
         scores = torch.empty((B, Tq, N), dtype=score_dtype, device=qI.device)
-    _check("csa_index", lib().csa_index(_p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(qp),
-                                        _p(scores), _dt(scores), B, Tq, N, H, c, m, dt, _stream()))
+    _check("csa_index", lib().csa_index_paged(
+        _p(qI), _p(qI_sf), _p(w), _p(Kt), _p(K_sf), kpg, _p(qp), _p(scores), _dt(scores), B, Tq, N,
+        H, c, m, dt, _stream()))
     return scores
+
+
+def _keys(K):
+    """(key tensor or pool, csa_pages_t pointer or None, keys per sequence)."""
+    if isinstance(K, Paged):
+        return K.pool, (ctypes.byref(K.pages()) if K.table is not None else None), K.rows
+    return K, None, K.shape[1]
 
 
 def csa_topk(scores, k, m, q_pos, idx=None):
@@ -221,7 +301,7 @@ def csa_index_topk(qI, w, K, k, m, q_pos, qI_sf=None, K_sf=None, scores=None, id
     fp4 = qI.dtype == torch.uint8
     B, Tq, H = qI.shape[:3]
     c = qI.shape[3] * (2 if fp4 else 1)
-    N = K.shape[1]
+    Kt, kpg, N = _keys(K)
     dt = DT_E2M1_BLOCK16 if fp4 else _dt(qI)
     if scores is None:
         scores = torch.empty((B, Tq, N), dtype=score_dtype, device=qI.device)
@@ -230,9 +310,9 @@ def csa_index_topk(qI, w, K, k, m, q_pos, qI_sf=None, K_sf=None, scores=None, id
     qp = positions(q_pos, B, Tq, qI.device)
     nbytes = lib().csa_index_topk_workspace_size(B, Tq, N, dt)
     ws = _workspace(ws, nbytes, qI.device, zero=True)   # histograms start zero; calls leave them zero
-    _check("csa_index_topk", lib().csa_index_topk(
-        _p(qI), _p(qI_sf), _p(w), _p(K), _p(K_sf), _p(qp), _p(scores), _dt(scores), _p(idx), B, Tq,
-        N, H, c, m, k, dt, _p(ws) if nbytes else None, nbytes, _stream()))
+    _check("csa_index_topk", lib().csa_index_topk_paged(
+        _p(qI), _p(qI_sf), _p(w), _p(Kt), _p(K_sf), kpg, _p(qp), _p(scores), _dt(scores), _p(idx), B,
+        Tq, N, H, c, m, k, dt, _p(ws) if nbytes else None, nbytes, _stream()))
     return scores, idx, ws
 
 
@@ -332,3 +412,37 @@ def csa_grouped_proj(A, W, C=None, G=None, lda=None, ldc=None):
 def device_error():
     """Reads and clears the library's sticky device error word; raises if it was set."""
     _check("csa_device_error", lib().csa_device_error(_stream()))
+
+
+class BlockPool:
+    """Host-side allocator of the physical blocks of a paged cache
+    (csa_block_pool_*): ids 0 .. num_blocks-1, handed out and taken back."""
+
+    def __init__(self, num_blocks):
+        self._h = lib().csa_block_pool_create(num_blocks)
+        if not self._h:
+            raise CsaError("csa_block_pool_create", 1, f"num_blocks={num_blocks}")
+        self.num_blocks = num_blocks
+
+    def free_count(self):
+        return int(lib().csa_block_pool_free_count(self._h))
+
+    def alloc(self, n):
+        ids = (ctypes.c_int32 * max(n, 1))()
+        _check("csa_block_pool_alloc", lib().csa_block_pool_alloc(self._h, n, ids))
+        return [int(ids[i]) for i in range(n)]
+
+    def release(self, ids):
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check("csa_block_pool_release", lib().csa_block_pool_release(self._h, len(ids), arr))
+
+    def close(self):
+        if self._h:
+            lib().csa_block_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -92,6 +92,7 @@ struct AttendTcArgs {
   int kv_mixed;                  // 1 = e4m3 + scale + bf16 rope rows
   int cl_reduce;                 // 1 = the nch chunks of a head group are one cluster and merge over DSMEM
   int ent_rotated;               // 1 = entries stored with their RoPE dims already rotated at m(s+1)-1
+  RowPages ent_pg, win_pg;       // paged / ring row maps (no table: flat)
   float scale_log2;              // log2(e) / sqrt(d)
   RopeFreqs rf;
 };
@@ -546,8 +547,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
           if (rr < x.nsel) {
             int s = a.idx ? __ldg(a.idx + ((size_t)x.b * a.Tq + x.i) * a.k + rr) : rr;
             if (s >= a.N) { csa_flag_error(ERRBIT_BAD_INDEX); s = -1; }
-            if (s >= 0) {
-              const size_t row = (size_t)x.b * a.N + s;
+            const long long prow = s >= 0 ? page_row(a.ent_pg, x.b, s, a.N) : -1;
+            if (s >= 0 && prow < 0) csa_flag_error(ERRBIT_BAD_INDEX);   // block outside the pool
+            if (prow >= 0) {
+              const size_t row = (size_t)prow;
               if (a.kv_mixed) {
                 src = reinterpret_cast<const uint8_t*>(a.ent) + row * (ATT_D - ATT_R);
                 rsrc = a.ent_rope + row * ATT_R;
@@ -559,8 +562,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
             }
           } else {
             const long long tok = x.w0 + (rr - x.nsel);
-            if (tok >= x.wbase && tok < x.wbase + a.T_win) {
-              const size_t row = (size_t)x.b * a.T_win + (size_t)(tok - x.wbase);
+            const long long prow =
+                (tok >= x.wbase && tok < x.wbase + a.T_win)
+                    ? page_row(a.win_pg, x.b, window_row(a.win_pg, tok, x.wbase, a.T_win), a.T_win)
+                    : -1;
+            if (prow >= 0) {
+              const size_t row = (size_t)prow;
               if (a.kv_mixed) {
                 src = reinterpret_cast<const uint8_t*>(a.win) + row * (ATT_D - ATT_R);
                 rsrc = a.win_rope + row * ATT_R;
@@ -570,7 +577,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
               }
               pos = tok;
             } else {
-              csa_flag_error(ERRBIT_BAD_INDEX);   // outside this batch row's window buffer
+              csa_flag_error(ERRBIT_BAD_INDEX);   // outside this batch row's window buffer or pool
             }
           }
         }
@@ -1134,6 +1141,7 @@ struct RotateArgs {
   int rows_per_b;
   int m;                          // >0: compressed entries (pos = m(s+1)-1); 0: tokens
   const int32_t* base;            // tokens: [B] token position of each batch row's row 0 (null: 0)
+  RowPages pg;                    // row map of src; dst is always flat (logical order)
   RopeFreqs rf;
 };
 
@@ -1145,14 +1153,20 @@ __global__ void __launch_bounds__(256) rope_rotate_rows_kernel(const RotateArgs 
   // one thread per 16-byte unit; 64 units per 512-dim row
   const long long u_all = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u_all >= a.rows * 64) return;
-  const long long row = u_all >> 6;
+  const long long row = u_all >> 6;               // logical: b * rows_per_b + s
   const int u = (int)(u_all & 63);
-  uint4 v = __ldg(reinterpret_cast<const uint4*>(a.src + row * ATT_D + u * 8));
-  if (u >= (ATT_D - ATT_R) / 8) {
-    const long long s = row % a.rows_per_b;
-    const long long pos = a.m > 0 ? (long long)a.m * (s + 1) - 1
-                                  : window_base(a.base, (int)(row / a.rows_per_b)) + s;
-    v = rope_unit(v, pos, F, (u - (ATT_D - ATT_R) / 8) * 4);
+  const int b = (int)(row / a.rows_per_b);
+  const long long s = row - (long long)b * a.rows_per_b;
+  const long long pos = a.m > 0 ? (long long)a.m * (s + 1) - 1 : window_base(a.base, b) + s;
+  // source row: entry s, or the window row that holds token pos
+  const long long j = (a.m == 0 && a.pg.ring) ? (pos >= 0 ? pos % a.rows_per_b : -1) : s;
+  const long long src = j >= 0 ? page_row(a.pg, b, j, a.rows_per_b) : -1;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (src >= 0) {
+    v = __ldg(reinterpret_cast<const uint4*>(a.src + src * ATT_D + u * 8));
+    if (u >= (ATT_D - ATT_R) / 8) v = rope_unit(v, pos, F, (u - (ATT_D - ATT_R) / 8) * 4);
+  } else if (j >= 0 && u == 0) {
+    csa_flag_error(ERRBIT_BAD_INDEX);             // block outside the pool
   }
   *reinterpret_cast<uint4*>(a.dst + row * ATT_D + u * 8) = v;
 }

@@ -13,7 +13,7 @@ __device__ unsigned int g_csa_error_word;
 
 enum : unsigned int {
   ERRBIT_TIMEOUT = 1u,      // a bounded mbarrier wait gave up
-  ERRBIT_BAD_INDEX = 2u,    // an index list held an entry >= N
+  ERRBIT_BAD_INDEX = 2u,    // an index >= N, a negative position, or a row outside its buffer or pool
   ERRBIT_TMEM = 4u,         // tensor-memory allocation returned an unusable address
   ERRBIT_HIST = 8u          // a key-digit histogram disagreed with the scores it describes
 };
@@ -66,6 +66,33 @@ CSA_DEVINL long long query_pos(const int32_t* q_pos, long long row, int i) {
 // Window buffer base token of batch row b (0 without a base array).
 CSA_DEVINL long long window_base(const int32_t* win_base, int b) {
   return win_base ? (long long)__ldg(win_base + b) : 0LL;
+}
+
+// Paged rows (the block-table layout of the KV cache, DeepSeek-V4 report,
+// Chinese translation, blog.uika.cn, §3.6.1): logical row j of sequence b sits
+// in block table[b * max_blocks + j / block_rows] of a pool shared by every
+// sequence, at row j % block_rows of that block.  No table: the flat layout,
+// row b * rows + j.  ring (window buffers): token p is logical row p mod rows.
+struct RowPages {
+  const int32_t* table;
+  int max_blocks, block_rows, num_blocks, ring;
+};
+
+// Physical row of logical row j (>= 0) of sequence b, rows per sequence in the
+// flat layout; -1 when the block-table entry is outside the pool (the caller
+// flags it and leaves the row out).
+CSA_DEVINL long long page_row(const RowPages& p, int b, long long j, long long rows) {
+  if (!p.table) return (long long)b * rows + j;
+  const long long blk_l = j / p.block_rows;
+  if (blk_l >= p.max_blocks) return -1;
+  const int blk = __ldg(p.table + (size_t)b * p.max_blocks + blk_l);
+  if (blk < 0 || blk >= p.num_blocks) return -1;
+  return (long long)blk * p.block_rows + (j - blk_l * p.block_rows);
+}
+
+// Logical row of window token tok (tokens base .. base + rows - 1 present).
+CSA_DEVINL long long window_row(const RowPages& p, long long tok, long long base, long long rows) {
+  return p.ring ? tok % rows : tok - base;
 }
 
 // Programmatic dependent launch.  Every kernel lets the next launch in the

@@ -54,6 +54,12 @@ struct CompressArgs {
   float norm_eps;
   int rope_dims;              // r > 0: rotate the last r dims at the entry's position m(i+1)-1
   RopeFreqs rf;
+  // paged output (no table: out is [B, N, d]): entry i >= out_first of batch
+  // row b goes to logical row out_entry0[b] + i - out_first of the pool; a
+  // negative out_entry0[b] writes nothing for that batch row
+  RowPages out_pg;
+  const int32_t* out_entry0;
+  int out_first;
 };
 
 template <typename T>
@@ -66,6 +72,20 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
   const int v = threadIdx.x % a.vecs;  // channel vector
   const int g = threadIdx.x / a.vecs;  // row group
   const int c0 = v * VEC;
+
+  // where this entry goes (the whole CTA leaves at once when it writes nothing)
+  long long li = i;                    // logical entry index: RoPE position m(li+1)-1
+  long long orow = (long long)b * a.N + i;
+  if (a.out_pg.table) {
+    const long long e0 = a.out_entry0 ? (long long)__ldg(a.out_entry0 + b) : 0LL;
+    if (e0 < 0 || i < a.out_first) return;
+    li = e0 + (i - a.out_first);
+    orow = page_row(a.out_pg, b, li, 0);
+    if (orow < 0) {
+      if (threadIdx.x == 0) csa_flag_error(ERRBIT_BAD_INDEX);   // block outside the pool
+      return;
+    }
+  }
 
   const size_t seq = (size_t)b * a.T * a.d;
   const T* Ca = reinterpret_cast<const T*>(a.Ca) + seq;
@@ -155,7 +175,7 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
   if (a.rope_dims > 0 && c0 >= a.d - a.rope_dims) {
     // RoPE of the last r dims at the entry's position (the last token it
     // summarises), so consumers can take the entry as already rotated
-    const long long pos = (long long)a.m * (i + 1) - 1;
+    const long long pos = (long long)a.m * (li + 1) - 1;
     const int j0 = (c0 - (a.d - a.rope_dims)) >> 1;
 #pragma unroll
     for (int p = 0; p < VEC / 2; ++p) {
@@ -166,7 +186,7 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
       res[2 * p + 1] = x0 * sn + x1 * cs;
     }
   }
-  T* out = reinterpret_cast<T*>(a.out) + ((size_t)b * a.N + i) * a.d + c0;
+  T* out = reinterpret_cast<T*>(a.out) + (size_t)orow * a.d + c0;
   V::store(out, res);
 }
 

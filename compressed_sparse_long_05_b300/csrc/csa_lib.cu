@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
+#include <vector>
 
 #include "../../include/csa.h"
 #include "common.cuh"
@@ -202,10 +204,33 @@ csa_status_t plan_index(csa::IndexTcArgs& a, int QT, int B, int Tq, int N) {
   return CSA_OK;
 }
 
+// Host checks of a row map (csa_pages_t) into its device form.  rows: logical
+// rows per sequence the call may read; ring_ok: window rows; pow2: tiled key
+// loads need block_rows a power of two >= 8.
+csa_status_t check_pages(const csa_pages_t* p, long long rows, bool ring_ok, bool pow2,
+                         RowPages* out) {
+  memset(out, 0, sizeof(*out));
+  if (!p) return CSA_OK;
+  if (p->ring && !ring_ok) return CSA_ERR_INVALID_ARG;
+  out->ring = p->ring ? 1 : 0;
+  if (!p->block_table) return CSA_OK;
+  if (!aligned(p->block_table, 4) || p->block_rows < 1 || p->num_blocks < 1 || p->max_blocks < 1)
+    return CSA_ERR_INVALID_ARG;
+  if ((rows + p->block_rows - 1) / p->block_rows > p->max_blocks) return CSA_ERR_INVALID_ARG;
+  if ((long long)p->num_blocks * p->block_rows >= 0x7fffffffLL) return CSA_ERR_UNSUPPORTED;
+  if (pow2 && (p->block_rows < 8 || (p->block_rows & (p->block_rows - 1)))) return CSA_ERR_UNSUPPORTED;
+  out->table = p->block_table;
+  out->max_blocks = p->max_blocks;
+  out->block_rows = p->block_rows;
+  out->num_blocks = p->num_blocks;
+  return CSA_OK;
+}
+
 template <int H>
 csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w, const void* K,
-                              const void* K_sf, const int32_t* q_pos, void* scores, int scores_bf16,
-                              int B, int Tq, int N, int m, uint32_t* hist, cudaStream_t stream) {
+                              const void* K_sf, const RowPages& kpg, const int32_t* q_pos,
+                              void* scores, int scores_bf16, int B, int Tq, int N, int m,
+                              uint32_t* hist, cudaStream_t stream) {
   csa::IndexFp4Args fa;
   memset(&fa, 0, sizeof(fa));
   csa::IndexTcArgs& a = fa.t;
@@ -215,7 +240,6 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
   if (st != CSA_OK) return st;
   if ((long long)B * N >= 0x7fffffffLL || (long long)B * Tq * H >= 0x7fffffffLL)
     return CSA_ERR_UNSUPPORTED;
-  fa.sf_rows = (long long)B * N;
   a.hist = a.QT == 1 ? hist : nullptr;
   const int nqh = a.QT * H;
   a.tmem_cols = 512;
@@ -223,11 +247,24 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
   // epilogue groups take alternate buffers
   a.nbuf = 4 * nqh <= 256 ? 4 : 2;
   CUtensorMap tmK, tmq, tmKs, tmqs;
-  if (!tmap_u8_3d_sw64(&tmK, K, csa::FP4_ROWB, N, B, csa::FP4_ROWB, (uint64_t)N * csa::FP4_ROWB,
-                       csa::IDX_TILE) ||
+  bool ok;
+  if (kpg.table) {
+    // paged keys: maps over the pool, one copy per min(block_rows, 128) rows
+    a.k_pg = kpg;
+    a.k_piece = kpg.block_rows < csa::IDX_TILE ? kpg.block_rows : csa::IDX_TILE;
+    const uint64_t P = (uint64_t)kpg.block_rows, nb = (uint64_t)kpg.num_blocks;
+    fa.k_sf = reinterpret_cast<const uint8_t*>(K_sf);   // scale rows by untiled bulk copies
+    ok = tmap_u8_3d_sw64(&tmK, K, csa::FP4_ROWB, P, nb, csa::FP4_ROWB, P * csa::FP4_ROWB,
+                         (uint32_t)a.k_piece) &&
+         tmap_u64_1d(&tmKs, K_sf, P * nb, (uint32_t)a.k_piece);   // prefetched, not copied from
+  } else {
+    ok = tmap_u8_3d_sw64(&tmK, K, csa::FP4_ROWB, N, B, csa::FP4_ROWB, (uint64_t)N * csa::FP4_ROWB,
+                         csa::IDX_TILE) &&
+         tmap_u64_1d(&tmKs, K_sf, (uint64_t)B * N, csa::FP4_SF_BOX);
+  }
+  if (!ok ||
       !tmap_u8_3d_sw64(&tmq, qI, csa::FP4_ROWB, (uint64_t)Tq * H, B, csa::FP4_ROWB,
                        (uint64_t)Tq * H * csa::FP4_ROWB, nqh) ||
-      !tmap_u64_1d(&tmKs, K_sf, (uint64_t)B * N, csa::FP4_SF_BOX) ||
       !tmap_u64_1d(&tmqs, qI_sf, (uint64_t)B * Tq * H, nqh))
     return CSA_ERR_UNSUPPORTED;
   const int smem = csa::IndexFp4Smem::BYTES;
@@ -242,10 +279,10 @@ csa_status_t launch_index_fp4(const void* qI, const void* qI_sf, const float* w,
 }
 
 template <int H, int C>
-csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, const int32_t* q_pos,
-                             void* scores, int scores_bf16, int B, int Tq, int N, int m,
-                             uint32_t* hist, cudaStream_t stream, unsigned long long wait_ns = 0,
-                             int skip_load_plus1 = 0) {
+csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, const RowPages& kpg,
+                             const int32_t* q_pos, void* scores, int scores_bf16, int B, int Tq,
+                             int N, int m, uint32_t* hist, cudaStream_t stream,
+                             unsigned long long wait_ns = 0, int skip_load_plus1 = 0) {
   csa::IndexTcArgs a;
   memset(&a, 0, sizeof(a));
   a.w = w; a.scores = scores; a.scores_bf16 = scores_bf16; a.q_pos = q_pos;
@@ -263,7 +300,17 @@ csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, cons
   while (cols < (uint32_t)(a.nbuf * nqh)) cols <<= 1;
   a.tmem_cols = cols;
   CUtensorMap tmK, tmq;
-  if (!tmap_bf16_3d(&tmK, K, C, N, B, (uint64_t)C * 2, (uint64_t)N * C * 2, 64, csa::IDX_TILE) ||
+  bool ok;
+  if (kpg.table) {
+    // paged keys: a map over the pool, one copy per min(block_rows, 128) rows
+    a.k_pg = kpg;
+    a.k_piece = kpg.block_rows < csa::IDX_TILE ? kpg.block_rows : csa::IDX_TILE;
+    ok = tmap_bf16_3d(&tmK, K, C, (uint64_t)kpg.block_rows, (uint64_t)kpg.num_blocks, (uint64_t)C * 2,
+                      (uint64_t)kpg.block_rows * C * 2, 64, (uint32_t)a.k_piece);
+  } else {
+    ok = tmap_bf16_3d(&tmK, K, C, N, B, (uint64_t)C * 2, (uint64_t)N * C * 2, 64, csa::IDX_TILE);
+  }
+  if (!ok ||
       !tmap_bf16_3d(&tmq, qI, C, (uint64_t)Tq * H, B, (uint64_t)C * 2, (uint64_t)Tq * H * C * 2,
                     64, nqh))
     return CSA_ERR_UNSUPPORTED;
@@ -522,6 +569,13 @@ csa_status_t csa_compress_ex(const void* Ca, const void* Cb, const void* Za, con
       (o.rope_dims > 0 && !(o.rope_base > 0.f)))
     return CSA_ERR_INVALID_ARG;
   if (o.rope_dims % vec) return CSA_ERR_UNSUPPORTED;
+  RowPages out_pg;
+  {
+    csa_status_t st = check_pages(&o.out_pages, 0, false, false, &out_pg);
+    if (st != CSA_OK) return st;
+    if (out_pg.table && (o.out_first < 0 || (o.out_entry0 && !aligned(o.out_entry0, 4))))
+      return CSA_ERR_INVALID_ARG;
+  }
   if (B == 0 || T / m == 0) return CSA_OK;   // nothing to compress (outputs may be empty)
   if (!Ca || !Za || !out) return CSA_ERR_INVALID_ARG;
   const void* ptrs[] = {Ca, Cb, Za, Zb, out};
@@ -539,6 +593,9 @@ csa_status_t csa_compress_ex(const void* Ca, const void* Cb, const void* Za, con
   a.norm_eps = o.norm_eps;
   a.rope_dims = o.rope_dims;
   if (o.rope_dims > 0) a.rf = make_rope(o.rope_dims, o.rope_base);
+  a.out_pg = out_pg;
+  a.out_entry0 = out_pg.table ? o.out_entry0 : nullptr;
+  a.out_first = out_pg.table ? o.out_first : 0;
   int rows = overlap ? 2 * m : m;
   int groups = 256 / a.vecs;
   if (groups > rows) groups = rows;
@@ -564,19 +621,22 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
 
 // ---------------------------------------------------------------------------
 static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w, const void* K,
-                              const void* K_sf, const int32_t* q_pos, void* scores, int score_dtype,
-                              int B, int Tq, int N, int H, int c, int m, int dtype, uint32_t* hist,
-                              void* stream) {
+                              const void* K_sf, const csa_pages_t* K_pages, const int32_t* q_pos,
+                              void* scores, int score_dtype, int B, int Tq, int N, int H, int c,
+                              int m, int dtype, uint32_t* hist, void* stream) {
   if (B < 0 || Tq < 0 || N < 0 || H <= 0 || c <= 0 || m <= 0) return CSA_ERR_INVALID_ARG;
   if (score_dtype != CSA_DT_F32 && score_dtype != CSA_DT_BF16) return CSA_ERR_UNSUPPORTED;
   const int sb = score_dtype == CSA_DT_BF16 ? 1 : 0;
+  RowPages kpg;
+  csa_status_t pst = check_pages(K_pages, N, false, dtype != CSA_DT_F32, &kpg);
+  if (pst != CSA_OK) return pst;
   if (B == 0 || Tq == 0 || N == 0) return CSA_OK;
   if (!qI || !w || !K || !scores) return CSA_ERR_INVALID_ARG;
   if ((q_pos && !aligned(q_pos, 4)) || !aligned(scores, sb ? 2 : 4)) return CSA_ERR_INVALID_ARG;
   if (dtype == CSA_DT_F32) {
     if (c > 256) return CSA_ERR_UNSUPPORTED;
     csa::IndexF32Args a{reinterpret_cast<const float*>(qI), w, reinterpret_cast<const float*>(K),
-                        scores, q_pos, sb, Tq, N, H, c, m};
+                        scores, q_pos, sb, kpg, Tq, N, H, c, m};
     dim3 grid((N + 7) / 8, B * Tq);
     cudaError_t e = launch_ex(csa::index_f32_kernel, grid, dim3(256), 0, S(stream), 1, a);
     if (e != cudaSuccess) return cuda_fail(e, "csa_index f32 launch");
@@ -585,13 +645,13 @@ static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w
   if (dtype == CSA_DT_BF16) {
     if (!aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4)) return CSA_ERR_INVALID_ARG;
     if (H == 64 && c == 128)
-      return launch_index_tc<64, 128>(qI, w, K, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
+      return launch_index_tc<64, 128>(qI, w, K, kpg, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     if (H == 64 && c == 64)
-      return launch_index_tc<64, 64>(qI, w, K, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
+      return launch_index_tc<64, 64>(qI, w, K, kpg, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     if (H == 32 && c == 128)
-      return launch_index_tc<32, 128>(qI, w, K, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
+      return launch_index_tc<32, 128>(qI, w, K, kpg, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     if (H == 128 && c == 128)
-      return launch_index_tc<128, 128>(qI, w, K, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
+      return launch_index_tc<128, 128>(qI, w, K, kpg, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
   if (dtype == CSA_DT_E2M1_BLOCK16) {
@@ -601,11 +661,14 @@ static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w
       return CSA_ERR_INVALID_ARG;
     if (c != csa::FP4_C) return CSA_ERR_UNSUPPORTED;
     if (H == 64)
-      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
+      return launch_index_fp4<64>(qI, qI_sf, w, K, K_sf, kpg, q_pos, scores, sb, B, Tq, N, m, hist,
+                                   S(stream));
     if (H == 32)
-      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
+      return launch_index_fp4<32>(qI, qI_sf, w, K, K_sf, kpg, q_pos, scores, sb, B, Tq, N, m, hist,
+                                   S(stream));
     if (H == 128)
-      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, q_pos, scores, sb, B, Tq, N, m, hist, S(stream));
+      return launch_index_fp4<128>(qI, qI_sf, w, K, K_sf, kpg, q_pos, scores, sb, B, Tq, N, m, hist,
+                                   S(stream));
     return CSA_ERR_UNSUPPORTED;
   }
   return CSA_ERR_UNSUPPORTED;
@@ -614,8 +677,16 @@ static csa_status_t index_impl(const void* qI, const void* qI_sf, const float* w
 csa_status_t csa_index(const void* qI, const void* qI_sf, const float* w, const void* K,
                        const void* K_sf, const int32_t* q_pos, void* scores, int score_dtype,
                        int B, int Tq, int N, int H, int c, int m, int dtype, void* stream) {
-  return index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, score_dtype, B, Tq, N, H, c, m, dtype,
-                    nullptr, stream);
+  return index_impl(qI, qI_sf, w, K, K_sf, nullptr, q_pos, scores, score_dtype, B, Tq, N, H, c, m,
+                    dtype, nullptr, stream);
+}
+
+csa_status_t csa_index_paged(const void* qI, const void* qI_sf, const float* w, const void* K,
+                             const void* K_sf, const csa_pages_t* K_pages, const int32_t* q_pos,
+                             void* scores, int score_dtype, int B, int Tq, int N, int H, int c,
+                             int m, int dtype, void* stream) {
+  return index_impl(qI, qI_sf, w, K, K_sf, K_pages, q_pos, scores, score_dtype, B, Tq, N, H, c, m,
+                    dtype, nullptr, stream);
 }
 
 csa_status_t csa_selftest_wait_timeout(const void* qI, const float* w, const void* K,
@@ -626,7 +697,8 @@ csa_status_t csa_selftest_wait_timeout(const void* qI, const float* w, const voi
   if (!qI || !w || !K || !scores || !aligned(qI, 16) || !aligned(K, 16) || !aligned(w, 4) ||
       !aligned(scores, 4) || (q_pos && !aligned(q_pos, 4)))
     return CSA_ERR_INVALID_ARG;
-  return launch_index_tc<64, 128>(qI, w, K, q_pos, scores, 0, B, Tq, N, m, nullptr, S(stream),
+  const RowPages flat{};
+  return launch_index_tc<64, 128>(qI, w, K, flat, q_pos, scores, 0, B, Tq, N, m, nullptr, S(stream),
                                   1000ull * (unsigned long long)limit_us, 1);
 }
 
@@ -645,10 +717,19 @@ csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, c
                             const void* K_sf, const int32_t* q_pos, void* scores, int score_dtype,
                             int32_t* idx, int B, int Tq, int N, int H, int c, int m, int k,
                             int dtype, void* ws, size_t ws_bytes, void* stream) {
+  return csa_index_topk_paged(qI, qI_sf, w, K, K_sf, nullptr, q_pos, scores, score_dtype, idx, B, Tq,
+                              N, H, c, m, k, dtype, ws, ws_bytes, stream);
+}
+
+csa_status_t csa_index_topk_paged(const void* qI, const void* qI_sf, const float* w,
+                                  const void* K, const void* K_sf, const csa_pages_t* K_pages,
+                                  const int32_t* q_pos, void* scores, int score_dtype,
+                                  int32_t* idx, int B, int Tq, int N, int H, int c, int m, int k,
+                                  int dtype, void* ws, size_t ws_bytes, void* stream) {
   if (k < 1 || k > 4096) return CSA_ERR_INVALID_ARG;
   if (!index_topk_fused(B, Tq, N, dtype)) {
-    csa_status_t st = csa_index(qI, qI_sf, w, K, K_sf, q_pos, scores, score_dtype, B, Tq, N, H, c,
-                                m, dtype, stream);
+    csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, K_pages, q_pos, scores, score_dtype, B, Tq,
+                                 N, H, c, m, dtype, nullptr, stream);
     if (st != CSA_OK) return st;
     return csa_topk(scores, score_dtype, q_pos, idx, B, Tq, N, k, m, stream);
   }
@@ -658,8 +739,8 @@ csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, c
   // the histograms start zero (caller's first use) and the selector clears each
   // row's after reading it, so no clearing pass runs here
   uint32_t* hist = reinterpret_cast<uint32_t*>(ws);
-  csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, q_pos, scores, score_dtype, B, Tq, N, H, c,
-                               m, dtype, hist, stream);
+  csa_status_t st = index_impl(qI, qI_sf, w, K, K_sf, K_pages, q_pos, scores, score_dtype, B, Tq, N,
+                               H, c, m, dtype, hist, stream);
   if (st != CSA_OK) return st;
   return launch_topk2(scores, score_dtype == CSA_DT_BF16, q_pos, idx, B * Tq, Tq, N, k, m, hist,
                       S(stream));
@@ -760,6 +841,12 @@ csa_status_t attend_validate(const AttendCall& c, AttPlan* plan, bool* empty) {
   if (c.N > 0 && !c.ent.data) return CSA_ERR_INVALID_ARG;
   if ((c.ent.flags & ~CSA_KV_ROTATED) || (c.win.flags & ~CSA_KV_ROTATED)) return CSA_ERR_INVALID_ARG;
   if (c.win.flags) return CSA_ERR_UNSUPPORTED;   // window rows are stored unrotated
+  {
+    RowPages pg;
+    csa_status_t st = check_pages(&c.ent.pages, c.N, false, false, &pg);
+    if (st == CSA_OK) st = check_pages(&c.win.pages, c.T_win, true, false, &pg);
+    if (st != CSA_OK) return st;
+  }
   if (c.B == 0 || c.Tq == 0) {
     *empty = true;
     return CSA_OK;
@@ -794,6 +881,9 @@ csa_status_t attend_validate(const AttendCall& c, AttPlan* plan, bool* empty) {
 csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void* stream) {
   const RopeFreqs rf = make_rope(c.r, c.rope_base);
   cudaStream_t st = S(stream);
+  RowPages ent_pg, win_pg;      // checked in attend_validate
+  check_pages(&c.ent.pages, c.N, false, false, &ent_pg);
+  check_pages(&c.win.pages, c.T_win, true, false, &win_pg);
   if (c.ent.dtype == CSA_DT_F32 && c.win.dtype == CSA_DT_F32) {
     csa::AttendF32Args a;
     memset(&a, 0, sizeof(a));
@@ -808,6 +898,7 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
     a.n_h = c.n_h; a.d = c.d; a.r = c.r; a.m = c.m; a.n_win = c.n_win;
     a.dense = c.dense;
     a.ent_rotated = (c.ent.flags & CSA_KV_ROTATED) ? 1 : 0;
+    a.ent_pg = ent_pg; a.win_pg = win_pg;
     a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
     a.rf = rf;
     const size_t smem = ((size_t)2 * c.n_h * c.d + c.d + 5 * c.n_h) * sizeof(float);
@@ -838,6 +929,7 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
   a.cl_reduce = p.cl_reduce;
   a.rel_rope = p.rel_rope;
   a.ent_rotated = (c.ent.flags & CSA_KV_ROTATED) ? 1 : 0;
+  a.ent_pg = ent_pg; a.win_pg = win_pg;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.d));
   a.rf = rf;
   if (!p.rotate_rows) {
@@ -849,19 +941,23 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
       ra.src = reinterpret_cast<const __nv_bfloat16*>(c.ent.data);
       ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_ent);
       ra.rows = (long long)c.B * c.N; ra.rows_per_b = c.N; ra.m = c.m; ra.base = nullptr;
+      ra.pg = ent_pg;
       cudaError_t e = launch_ex(csa::rope_rotate_rows_kernel, dim3((unsigned)((ra.rows * 64 + 255) / 256)),
                                 dim3(256), 0, st, 1, ra);
       if (e != cudaSuccess) return cuda_fail(e, "csa_attend rotate entries");
       a.ent = ra.dst;
+      memset(&a.ent_pg, 0, sizeof(a.ent_pg));     // the rotated copy is flat
     }
     if (c.T_win > 0) {
       ra.src = reinterpret_cast<const __nv_bfloat16*>(c.win.data);
       ra.dst = reinterpret_cast<__nv_bfloat16*>(wsb + p.off_rot_win);
       ra.rows = (long long)c.B * c.T_win; ra.rows_per_b = c.T_win; ra.m = 0; ra.base = c.win_base;
+      ra.pg = win_pg;
       cudaError_t e = launch_ex(csa::rope_rotate_rows_kernel, dim3((unsigned)((ra.rows * 64 + 255) / 256)),
                                 dim3(256), 0, st, 1, ra);
       if (e != cudaSuccess) return cuda_fail(e, "csa_attend rotate window");
       a.win = ra.dst;
+      memset(&a.win_pg, 0, sizeof(a.win_pg));     // flat, token order from win_base
     }
   }
   if (p.nch > 1 && !p.cl_reduce) {
@@ -1086,6 +1182,69 @@ extern "C" csa_status_t csa_grouped_proj(const void* A, int64_t lda, const void*
   e = launch_ex(csa::gemm_grouped_kernel, dim3(grid), dim3(csa::GEMM_THREADS), smem, S(stream), 1,
                 tmA, tmW, a);
   if (e != cudaSuccess) return cuda_fail(e, "csa_grouped_proj launch");
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Block pool: the free physical blocks of a paged cache, as a stack of ids
+// (host memory only).  `used` marks allocated ids so that a release of an id
+// that is free, out of range or repeated is refused whole.
+struct csa_block_pool {
+  std::vector<int32_t> free_ids;     // top of the stack = next id handed out
+  std::vector<uint8_t> used;
+};
+
+extern "C" csa_block_pool_t* csa_block_pool_create(int32_t num_blocks) {
+  if (num_blocks < 1 || num_blocks > (1 << 30)) return nullptr;
+  csa_block_pool_t* p = new (std::nothrow) csa_block_pool_t();
+  if (!p) return nullptr;
+  try {
+    p->used.assign((size_t)num_blocks, 0);
+    p->free_ids.resize((size_t)num_blocks);
+    for (int32_t i = 0; i < num_blocks; ++i) p->free_ids[(size_t)i] = num_blocks - 1 - i;
+  } catch (...) {
+    delete p;
+    return nullptr;
+  }
+  return p;
+}
+
+extern "C" void csa_block_pool_destroy(csa_block_pool_t* pool) { delete pool; }
+
+extern "C" int32_t csa_block_pool_free_count(const csa_block_pool_t* pool) {
+  return pool ? (int32_t)pool->free_ids.size() : 0;
+}
+
+extern "C" csa_status_t csa_block_pool_alloc(csa_block_pool_t* pool, int32_t n, int32_t* ids) {
+  if (!pool || n < 0 || (n > 0 && !ids)) return CSA_ERR_INVALID_ARG;
+  if ((size_t)n > pool->free_ids.size()) return CSA_ERR_WORKSPACE;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t id = pool->free_ids.back();
+    pool->free_ids.pop_back();
+    pool->used[(size_t)id] = 1;
+    ids[i] = id;
+  }
+  return CSA_OK;
+}
+
+extern "C" csa_status_t csa_block_pool_release(csa_block_pool_t* pool, int32_t n,
+                                               const int32_t* ids) {
+  if (!pool || n < 0 || (n > 0 && !ids)) return CSA_ERR_INVALID_ARG;
+  const size_t nb = pool->used.size();
+  int32_t i = 0;
+  for (; i < n; ++i) {                 // check every id first (2 marks a repeat)
+    const int32_t id = ids[i];
+    if (id < 0 || (size_t)id >= nb || pool->used[(size_t)id] != 1) break;
+    pool->used[(size_t)id] = 2;
+  }
+  if (i < n) {                         // refused: undo the marks
+    for (int32_t j = 0; j < i; ++j) pool->used[(size_t)ids[j]] = 1;
+    return CSA_ERR_INVALID_ARG;
+  }
+  for (int32_t j = n - 1; j >= 0; --j) {
+    pool->used[(size_t)ids[j]] = 0;
+    pool->free_ids.push_back(ids[j]);
+  }
   return CSA_OK;
 }
 

@@ -123,7 +123,7 @@ CSA_DEVINL void build_scale_atoms(const uint8_t* raw, uint8_t* atoms, int nrows,
 
 struct IndexFp4Args {
   IndexTcArgs t;           // shared work split (QT * H <= 128)
-  long long sf_rows;       // B * N scale rows in the K scale map
+  const uint8_t* k_sf;     // paged keys: the scale-byte pool (8 bytes per key row)
 };
 
 template <int H>
@@ -210,6 +210,28 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           if (!mbar_wait(empty + st, ph ^ 1, abort_flag)) return false;
           // scale rows of entries j*128 .. j*128+127 of batch row b, from an even
           // (16-byte aligned) flat row index
+          if (a.k_pg.table) {
+            // paged keys: one K copy and one scale-row copy per k_piece rows from
+            // its own block; the scale rows (k_piece * 8 bytes, 64 at the least)
+            // come by untiled bulk copy, whose addresses need 16-byte alignment
+            // only (a tensor copy's shared destination would need 128), and land
+            // from the start of the stage
+            const int np = IDX_TILE / a.k_piece, off = key_block_off(a, j);
+            uint32_t mask = 0;
+            for (int q = 0; q < np; ++q)
+              if (key_block(a, x.b, j, q, true) >= 0) mask |= 1u << q;
+            mbar_arrive_expect_tx(full + st, (uint32_t)(__popc(mask) * a.k_piece * (FP4_ROWB + 8)));
+            for (int q = 0; q < np; ++q) {
+              if (!(mask >> q & 1u)) continue;
+              const int blk = key_block(a, x.b, j, q, false);
+              tma_load_3d(sA + st * L::A_BYTES + q * a.k_piece * FP4_ROWB, &tm_K, full + st, 0, off, blk);
+              const size_t sx = (size_t)blk * a.k_pg.block_rows + off;
+              bulk_load(rawA + st * L::RAW_PITCH + q * a.k_piece * 8, fa.k_sf + sx * 8,
+                        (uint32_t)(a.k_piece * 8), full + st);
+            }
+            ++ia;
+            return true;
+          }
           const long long r0 = (long long)x.b * a.N + (long long)j * IDX_TILE;
           const int sx = (int)(r0 & ~1LL);
           mbar_arrive_expect_tx(full + st, L::A_BYTES + L::RAW_BYTES);
@@ -309,7 +331,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
         const uint32_t st = ia % FP4_STAGES, ph = (ia / FP4_STAGES) & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(full + st, ph, abort_flag))) { ok = false; break; }
         const long long r0 = (long long)x.b * a.N + (long long)j * IDX_TILE;
-        const uint8_t* raw = rawA + st * L::RAW_PITCH + (r0 & 1) * 8;
+        const uint8_t* raw = rawA + st * L::RAW_PITCH + (a.k_pg.table ? 0 : (r0 & 1) * 8);
         const int nrows = (int)min((long long)IDX_TILE, (long long)a.N - (long long)j * IDX_TILE);
         build_scale_atoms(raw, atomA + st * 1024, nrows, lane);
         fence_proxy_async();

@@ -45,6 +45,8 @@ struct IndexTcArgs {
   uint32_t tmem_cols;    // allocated TMEM columns (power of 2 >= nbuf * QT * H)
   int nbuf;              // accumulator buffers in tensor memory (2 or 4)
   uint32_t* hist;        // optional [B * Tq][IDX_HBINS] key-digit histograms (QT == 1), zeroed
+  RowPages k_pg;         // paged keys: the K map spans {c, block_rows, num_blocks} (no table: flat)
+  int k_piece;           // paged keys: rows per TMA copy, min(block_rows, 128)
   // Failure-detection test hooks (zero in every normal launch):
   unsigned long long wait_ns;   // limit of every wait in ns (0: WAIT_LIMIT_NS)
   int skip_load_plus1;          // n > 0: CTA 0's producer leaves out its K-tile copy number n-1
@@ -54,6 +56,28 @@ struct IndexTcArgs {
 // top-k selector: bin = top IDX_HBITS bits of the order-preserving key.
 constexpr int IDX_HBITS = 11;
 constexpr int IDX_HBINS = 1 << IDX_HBITS;
+
+// Paged keys: entry tile j of batch row b arrives as IDX_TILE / k_piece TMA
+// copies, copy q from the block that holds logical rows j*IDX_TILE + q*k_piece
+// onwards.  key_block gives that block, or -1 when the copy is left out: its
+// logical block lies past the sequence's keys (those rows are not visible, so
+// their scores are never stored as computed), or the table names a block
+// outside the pool (flagged when `flag`).
+CSA_DEVINL int key_block(const IndexTcArgs& a, int b, int j, int q, bool flag) {
+  const int P = a.k_pg.block_rows;
+  const long long lb = ((long long)j * IDX_TILE + (long long)q * a.k_piece) / P;
+  if (lb >= ((long long)a.N + P - 1) / P) return -1;
+  const int blk = __ldg(a.k_pg.table + (size_t)b * a.k_pg.max_blocks + lb);
+  if (blk < 0 || blk >= a.k_pg.num_blocks) {
+    if (flag) csa_flag_error(ERRBIT_BAD_INDEX);
+    return -1;
+  }
+  return blk;
+}
+// Row offset of tile j inside its block (nonzero only when block_rows > IDX_TILE).
+CSA_DEVINL int key_block_off(const IndexTcArgs& a, int j) {
+  return (int)(((long long)j * IDX_TILE) % a.k_pg.block_rows);
+}
 
 // Store one score (float32, or rounded to bf16) at element e of the score rows.
 CSA_DEVINL void store_score(void* scores, int bf16, size_t e, float v) {
@@ -242,6 +266,23 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
           if (!mbar_wait(empty + st, ph ^ 1, abort_flag, lim)) return false;
           if (blockIdx.x == 0 && a.skip_load_plus1 == (int)ia + 1) {
             ++ia;          // test hook: this stage never fills, its consumer's wait runs out
+            return true;
+          }
+          if (a.k_pg.table) {
+            // paged keys: one copy per k_piece rows from its own block
+            const int np = IDX_TILE / a.k_piece, off = key_block_off(a, j);
+            uint32_t mask = 0;
+            for (int q = 0; q < np; ++q)
+              if (key_block(a, x.b, j, q, true) >= 0) mask |= 1u << q;
+            mbar_arrive_expect_tx(full + st, (uint32_t)(__popc(mask) * a.k_piece * 128 * L.KCH));
+            for (int q = 0; q < np; ++q) {
+              if (!(mask >> q & 1u)) continue;
+              const int blk = key_block(a, x.b, j, q, false);
+              for (int kc = 0; kc < L.KCH; ++kc)
+                tma_load_3d(sA + st * L.A_BYTES + kc * (IDX_TILE * 128) + q * a.k_piece * 128, &tm_K,
+                            full + st, kc * 64, off, blk);
+            }
+            ++ia;
             return true;
           }
           mbar_arrive_expect_tx(full + st, L.A_BYTES);

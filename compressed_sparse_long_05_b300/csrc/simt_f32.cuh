@@ -17,6 +17,7 @@ struct IndexF32Args {
   const float* q; const float* w; const float* K; void* scores;
   const int32_t* q_pos;            // [B, Tq] (null: t = i)
   int scores_bf16;                 // 1 = scores stored as bf16
+  RowPages k_pg;                   // paged keys (no table: flat)
   int Tq, N, H, c, m;
 };
 
@@ -39,7 +40,12 @@ __global__ void __launch_bounds__(256) index_f32_kernel(IndexF32Args a) {
     return;
   }
   const float* qr = a.q + (size_t)row * a.H * a.c;
-  const float* kr = a.K + ((size_t)b * a.N + s) * a.c;
+  const long long krow = page_row(a.k_pg, b, s, a.N);
+  if (krow < 0) {                                    // block outside the pool
+    if (lane == 0) csa_flag_error(ERRBIT_BAD_INDEX);
+    return;
+  }
+  const float* kr = a.K + (size_t)krow * a.c;
   const float* wr = a.w + (size_t)row * a.H;
   float acc = 0.f;
   for (int h = 0; h < a.H; ++h) {
@@ -67,6 +73,7 @@ struct AttendF32Args {
   int Tq, N, k, T_win, n_h, d, r, m, n_win;
   int dense;        // 1 = HCA: every visible entry, idx unused
   int ent_rotated;  // 1 = entries stored with their RoPE dims already rotated
+  RowPages ent_pg, win_pg;   // paged / ring row maps (no table: flat)
   float inv_sqrt_d;
   RopeFreqs rf;
 };
@@ -126,7 +133,9 @@ __global__ void __launch_bounds__(ATT_F32_THREADS) attend_f32_kernel(AttendF32Ar
       int s = a.dense ? jr : irow[jr];
       if (s < 0) continue;                       // uniform across the block
       if (s >= a.N) { if (tid == 0) csa_flag_error(ERRBIT_BAD_INDEX); continue; }
-      src = a.ent + ((size_t)b * a.N + s) * d;
+      const long long prow = page_row(a.ent_pg, b, s, a.N);
+      if (prow < 0) { if (tid == 0) csa_flag_error(ERRBIT_BAD_INDEX); continue; }
+      src = a.ent + (size_t)prow * d;
       pos = a.ent_rotated ? 0 : (long long)a.m * (s + 1) - 1;   // a turn by 0 leaves the row as stored
     } else {
       const long long tok = w0 + (jr - nsel);
@@ -134,7 +143,9 @@ __global__ void __launch_bounds__(ATT_F32_THREADS) attend_f32_kernel(AttendF32Ar
         if (tid == 0) csa_flag_error(ERRBIT_BAD_INDEX);
         continue;
       }
-      src = a.win + ((size_t)b * a.T_win + (size_t)(tok - wbase)) * d;
+      const long long prow = page_row(a.win_pg, b, window_row(a.win_pg, tok, wbase, a.T_win), a.T_win);
+      if (prow < 0) { if (tid == 0) csa_flag_error(ERRBIT_BAD_INDEX); continue; }
+      src = a.win + (size_t)prow * d;
       pos = tok;
     }
     for (int x = tid; x < d; x += ATT_F32_THREADS) er[x] = src[x];

@@ -260,3 +260,157 @@ class PipelinedForward:
     def wait(self, step: int):
         """Blocks until step ``step``'s output is in its host buffer."""
         self.ev_out[step % 2].synchronize()
+
+
+class PagedKVCache:
+    """The heterogeneous KV cache of one CSA and one HCA layer (DeepSeek-V4
+    report, Chinese translation, blog.uika.cn, §3.6.1).
+
+    Every block covers lcm(m, m') raw tokens, so it holds lcm/m CSA entries,
+    as many indexer keys, and lcm/m' HCA entries (32, 32 and 1 at m = 4,
+    m' = 128).  One block table per sequence (int32 [B, max_blocks] on the
+    device, mirrored on the host) addresses all three pools; the physical
+    blocks come from a native :class:`~._lib.BlockPool`.  The state cache is a
+    ring of T_win window rows per sequence (token p at row p mod T_win), which
+    takes each new token in place.  The raw tokens of a block that has not
+    closed yet stay with the caller; :meth:`compress` writes the entries they
+    produce straight into the pools (a whole prefill, or, in decode, the entry
+    of each block that just closed).
+
+    ``storage`` "bf16": bf16 entries and keys; "mixed": FP8 entries with bf16
+    RoPE dims and FP4 keys with e4m3 block scales (§2.3.4, §3.4).  The
+    :meth:`views` dict replaces the cache tensors of an input dict for
+    :func:`forward`.
+    """
+
+    def __init__(self, B, max_tokens, num_blocks, d=512, r=64, c_I=128, T_win=128, m=4, m_hca=128,
+                 storage="bf16", device="cuda"):
+        import math
+        import torch
+        self.B, self.d, self.r, self.c_I, self.T_win = B, d, r, c_I, T_win
+        self.m, self.m_hca, self.storage, self.device = m, m_hca, storage, device
+        self.block_tokens = math.lcm(m, m_hca)
+        self.csa_rows = self.block_tokens // m          # CSA entries (and keys) per block
+        self.hca_rows = self.block_tokens // m_hca      # HCA entries per block
+        self.max_blocks = -(-max_tokens // self.block_tokens)
+        self.num_blocks = num_blocks
+        self.pool = L.BlockPool(num_blocks)
+        self.blocks = [[] for _ in range(B)]
+        self.table = torch.zeros((B, self.max_blocks), dtype=torch.int32, device=device)
+        nc, nh = num_blocks * self.csa_rows, num_blocks * self.hca_rows
+        u8, bf = torch.uint8, torch.bfloat16
+        if storage == "bf16":
+            self.ent = torch.zeros((nc, d), dtype=bf, device=device)
+            self.hca = torch.zeros((nh, d), dtype=bf, device=device)
+            self.keys = torch.zeros((nc, c_I), dtype=bf, device=device)
+            self.keys_sf = None
+            self.win = torch.zeros((B, T_win, d), dtype=bf, device=device)
+        elif storage == "mixed":
+            def rows(lead):      # (e4m3 dims, float32 scale, bf16 RoPE dims)
+                return (torch.zeros(lead + (d - r,), dtype=u8, device=device),
+                        torch.zeros(lead, dtype=torch.float32, device=device),
+                        torch.zeros(lead + (r,), dtype=bf, device=device))
+            self.ent = rows((nc,))
+            self.hca = rows((nh,))
+            self.keys = torch.zeros((nc, c_I // 2), dtype=u8, device=device)
+            self.keys_sf = torch.zeros((nc, c_I // 16), dtype=u8, device=device)
+            self.win = rows((B, T_win))
+        else:
+            raise ValueError(f"storage {storage!r}: 'bf16' or 'mixed'")
+
+    # ---------------- blocks ----------------
+    def reserve(self, b, tokens):
+        """Gives sequence b enough blocks for its first ``tokens`` raw tokens."""
+        import torch
+        need = -(-tokens // self.block_tokens)
+        if need > self.max_blocks:
+            raise ValueError(f"{tokens} tokens need {need} blocks; the table holds {self.max_blocks}")
+        have = len(self.blocks[b])
+        if need > have:
+            new = self.pool.alloc(need - have)
+            self.blocks[b] += new
+            self.table[b, have:need] = torch.tensor(new, dtype=torch.int32).to(self.device)
+
+    def release(self, b):
+        """Returns sequence b's blocks to the pool."""
+        if self.blocks[b]:
+            self.pool.release(self.blocks[b])
+        self.blocks[b] = []
+
+    # ---------------- views for the kernels ----------------
+    def entries(self, N):
+        return L.Paged(self.ent, self.table, self.csa_rows, N)
+
+    def hca_entries(self, N):
+        return L.Paged(self.hca, self.table, self.hca_rows, N)
+
+    def index_keys(self, N):
+        return L.Paged(self.keys, self.table, self.csa_rows, N)
+
+    def window(self):
+        return L.Paged(self.win, None, 0, self.T_win, ring=True)
+
+    def views(self, kind, N):
+        """Replacements for the cache tensors of an input dict of :func:`forward`
+        (``kind`` "csa" or "hca"; N entries per sequence)."""
+        v = {"win": self.window()}
+        if kind == "hca":
+            v["entries"] = self.hca_entries(N)
+            return v
+        v["entries"] = self.entries(N)
+        if self.storage == "mixed":
+            v["K_fp4"] = self.index_keys(N)
+            v["K_sf"] = self.keys_sf
+        else:
+            v["K"] = self.index_keys(N)
+        return v
+
+    # ---------------- writes ----------------
+    def _rows_of(self, b, n, per_block):
+        """Physical pool rows of logical rows 0..n-1 of sequence b (host side)."""
+        import torch
+        j = torch.arange(n)
+        blk = torch.tensor(self.blocks[b], dtype=torch.int64)[j // per_block]
+        return (blk * per_block + j % per_block).to(self.device)
+
+    def load(self, kind, b, rows, sf=None):
+        """Copies sequence b's logical rows 0..n-1 (a [n, ...] tensor, or the
+        (e4m3, scale, rope) tuple) into its blocks; ``kind`` "entries", "hca" or
+        "keys" (``sf``: the keys' e4m3 scale bytes)."""
+        per = self.hca_rows if kind == "hca" else self.csa_rows
+        pool = {"entries": self.ent, "hca": self.hca, "keys": self.keys}[kind]
+        n = (rows[0] if isinstance(rows, (tuple, list)) else rows).shape[0]
+        idx = self._rows_of(b, n, per)
+        if isinstance(pool, tuple):
+            for p, src in zip(pool, rows):
+                p[idx] = src
+        else:
+            pool[idx] = rows
+        if sf is not None:
+            self.keys_sf[idx] = sf
+
+    def load_window(self, b, rows, base):
+        """Puts sequence b's window tokens base .. base+n-1 (rows [n, ...], or the
+        (e4m3, scale, rope) tuple) at their ring rows."""
+        import torch
+        n = (rows[0] if isinstance(rows, (tuple, list)) else rows).shape[0]
+        ring = (torch.arange(n) + base) % self.T_win
+        ring = ring.to(self.device)
+        if isinstance(self.win, tuple):
+            for p, src in zip(self.win, rows):
+                p[b][ring] = src
+        else:
+            self.win[b][ring] = rows
+
+    def compress(self, kind, Ca, Za, Cb=None, Zb=None, entry0=None, first=0, **opts):
+        """Compresses raw rows [B, T, d] straight into the bf16 pool of ``kind``
+        ("entries", "hca" or "keys"): entry i >= first of sequence b goes to
+        logical row entry0[b] + i - first (int32 [B] device tensor, None = 0;
+        negative: nothing written).  ``opts``: the csa_compress epilogue."""
+        if self.storage != "bf16":
+            raise ValueError("compression writes bf16 pools")
+        per = self.hca_rows if kind == "hca" else self.csa_rows
+        pool = {"entries": self.ent, "hca": self.hca, "keys": self.keys}[kind]
+        m = self.m_hca if kind == "hca" else self.m
+        out = L.Paged(pool, self.table, per, self.max_blocks * per)
+        L.csa_compress(Ca, Za, m, Cb=Cb, Zb=Zb, out=out, out_entry0=entry0, out_first=first, **opts)

@@ -68,10 +68,40 @@ typedef enum {
                                 16 consecutive elements (§3.4 FP4 indexer QK path) */
 } csa_dtype_t;
 
+/* ---------------------------------------------------------------------------
+ * Paged rows — the heterogeneous KV-cache layout of §3.6.1 (inference
+ * framework): the cache is cut into blocks of lcm(m, m') raw tokens, so one
+ * block holds lcm/m CSA entries (and as many indexer keys) and lcm/m' HCA
+ * entries, and one block table per sequence addresses every pool; the sliding
+ * window and the not-yet-compressed tail live in a fixed-size state cache.
+ * A csa_pages_t maps the logical rows j of sequence b (entry index s, or the
+ * window row of a token) to rows of a pool shared by all sequences:
+ *   block_table == NULL: flat layout, row b * rows + j (rows = N or T_win);
+ *   otherwise pool row block_table[b * max_blocks + j / block_rows] * block_rows
+ *            + j % block_rows (block_table: DEVICE int32 [B, max_blocks]).
+ *   ring (window rows only): token p sits at logical row p mod T_win, so a
+ *            fixed buffer of T_win rows per sequence takes one new token per
+ *            decode step in place; the tokens present are still
+ *            win_base[b] .. win_base[b] + T_win - 1.
+ * A block-table entry outside [0, num_blocks) read on the device sets the
+ * bad-index bit of the device error word, and its rows are left out (index:
+ * left unread, their scores undefined).  Only the table entries of logical
+ * blocks the call reads are read (entries: blocks < ceil(N / block_rows)).
+ * A zero-filled csa_pages_t is the flat layout. */
+typedef struct {
+  const int32_t* block_table;
+  int32_t max_blocks;
+  int32_t block_rows;
+  int32_t num_blocks;
+  int32_t ring;
+} csa_pages_t;
+
 /* A set of key=value rows (compressed entries or raw window tokens).
  *   dtype F32 / BF16 : data = [B, rows, d]; scale, rope unused.
  *   dtype E4M3_BF16ROPE : data = e4m3 [B, rows, d-r], scale = float32 [B, rows],
  *                         rope = bf16 [B, rows, r].
+ *   With pages.block_table set, data / scale / rope are pools of
+ *   num_blocks * block_rows rows in the same per-row formats.
  *   flags: 0, or CSA_KV_ROTATED for compressed entries whose last r dims are
  *          already rotated at their own position m*(s+1)-1 (csa_compress_ex
  *          with rope_dims = r writes them so); the attention then does not
@@ -83,7 +113,27 @@ typedef struct {
   const void* data;
   const float* scale;
   const void* rope;
+  csa_pages_t pages;
 } csa_kv_t;
+
+/* ---------------------------------------------------------------------------
+ * Block pool — host-side allocator of the physical blocks behind a paged
+ * cache (§3.6.1).  Blocks are ids 0 .. num_blocks-1; the pool hands out free
+ * ids and takes them back, and refuses to take back an id that is not
+ * allocated.  Host memory only: these calls touch no GPU.  A pool is not
+ * thread-safe; guard it if several host threads share it.
+ * ------------------------------------------------------------------------- */
+typedef struct csa_block_pool csa_block_pool_t;
+/* NULL when num_blocks is not in [1, 2^30] or memory runs out. */
+csa_block_pool_t* csa_block_pool_create(int32_t num_blocks);
+void csa_block_pool_destroy(csa_block_pool_t* pool);
+int32_t csa_block_pool_free_count(const csa_block_pool_t* pool);
+/* n ids into ids[0..n) (HOST array), lowest free ids first after creation;
+ * CSA_ERR_WORKSPACE (nothing taken) when fewer than n are free. */
+csa_status_t csa_block_pool_alloc(csa_block_pool_t* pool, int32_t n, int32_t* ids);
+/* Returns n ids; CSA_ERR_INVALID_ARG (nothing returned) if any id is out of
+ * range, not allocated, or repeated. */
+csa_status_t csa_block_pool_release(csa_block_pool_t* pool, int32_t n, const int32_t* ids);
 
 /* ---------------------------------------------------------------------------
  * csa_compress — softmax-weighted block compression of per-token entries.
@@ -114,6 +164,20 @@ csa_status_t csa_compress(const void* Ca, const void* Cb, const void* Za, const 
  * The same call with d = c_I compresses the indexer keys (K^IComp of §2.3.1).
  * rope_dims must be even, <= min(d, 128), and a multiple of 8 (BF16) or 4
  * (F32).
+ *
+ * out_pages: where the entries go (zero-filled: out is [B, floor(T/m), d]).
+ * With out_pages.block_table set, out is a pool of num_blocks * block_rows
+ * rows, and compressed entry i >= out_first of sequence b is written to
+ * logical row e = out_entry0[b] + i - out_first (out_entry0: DEVICE int32 [B],
+ * NULL = 0) and rotated (rope_dims > 0) at position m*(e+1)-1.  A prefill
+ * writes its entries straight into the paged cache (out_first = 0,
+ * out_entry0 = NULL).  A decode step passes each sequence's last 2m raw rows
+ * (T = 2m) with out_first = 1, so the entry of the block that just closed
+ * (local entry 1: its a-rows and the previous block's b-rows) lands at its
+ * logical row; a negative out_entry0[b] writes nothing for sequence b (its
+ * block did not close).  For a sequence's first block the previous block's
+ * b-row logits are -inf, which gives the entry-0 rule.  out_entry0 and
+ * out_first are ignored for the flat layout; the ring flag must be 0.
  * ------------------------------------------------------------------------- */
 typedef struct {
   int32_t rms_norm;
@@ -121,6 +185,9 @@ typedef struct {
   const float* norm_weight;
   int32_t rope_dims;
   float rope_base;
+  csa_pages_t out_pages;
+  const int32_t* out_entry0;
+  int32_t out_first;
 } csa_compress_opts_t;
 
 csa_status_t csa_compress_ex(const void* Ca, const void* Cb, const void* Za, const void* Zb,
@@ -181,6 +248,26 @@ csa_status_t csa_index_topk(const void* qI, const void* qI_sf, const float* w, c
 size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype);
 
 /* ---------------------------------------------------------------------------
+ * csa_index_paged / csa_index_topk_paged — csa_index / csa_index_topk with
+ * the keys K (and their scales K_sf) read through K_pages (a HOST pointer;
+ * NULL, or a NULL block_table, is the flat layout): K is then a pool of
+ * num_blocks * block_rows key rows (K_sf the matching scale rows), addressed
+ * by the same block table as the compressed entries of §3.6.1.  BF16 and
+ * E2M1_BLOCK16 keys need block_rows a power of two >= 8; F32 any
+ * block_rows >= 1; ring must be 0.  Results are identical to the flat calls
+ * on the same logical keys.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_index_paged(const void* qI, const void* qI_sf, const float* w, const void* K,
+                             const void* K_sf, const csa_pages_t* K_pages, const int32_t* q_pos,
+                             void* scores, int score_dtype, int B, int Tq, int N, int H, int c,
+                             int m, int dtype, void* stream);
+csa_status_t csa_index_topk_paged(const void* qI, const void* qI_sf, const float* w,
+                                  const void* K, const void* K_sf, const csa_pages_t* K_pages,
+                                  const int32_t* q_pos, void* scores, int score_dtype,
+                                  int32_t* idx, int B, int Tq, int N, int H, int c, int m, int k,
+                                  int dtype, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * csa_attend — shared-KV multi-query core attention (§2.3.1 "Shared KV MQA",
  * §2.3.3).  For query row i at position t and head h:
  *   rows J = {compressed entries idx[b,i,:] >= 0} U {raw tokens max(0,t-n_win+1)..t}
@@ -190,9 +277,14 @@ size_t csa_index_topk_workspace_size(int B, int Tq, int N, int dtype);
  *   logits = q.row / sqrt(d); p = exp(logit) / (sum exp(logits) + exp(sink[h]));
  *   o = sum p * rotated row; out = o with its last r dims rotated by -t.
  *   q: [B, Tq, n_h, d] (F32 or BF16); out: same shape and dtype as q.
- *   entries: [B, N, d] rows (F32, BF16 or E4M3_BF16ROPE).
- *   win: [B, T_win, d] rows; row j of batch row b holds raw token
- *        win_base[b] + j (win_base: device int32 [B], NULL = 0).
+ *   entries: [B, N, d] rows (F32, BF16 or E4M3_BF16ROPE), or paged through
+ *        entries.pages (any block_rows >= 1; ring must be 0).
+ *   win: [B, T_win, d] rows; batch row b holds raw tokens win_base[b] ..
+ *        win_base[b] + T_win - 1 (win_base: device int32 [B], NULL = 0),
+ *        token p at row p - win_base[b], or at row p mod T_win with
+ *        win.pages.ring (the state-cache ring of §3.6.1); the rows may be paged
+ *        through win.pages as well (one block of T_win rows per sequence is
+ *        the usual state slot).
  *   q_pos: device int32 [B, Tq] query positions (NULL: t = i).
  *   idx: [B, Tq, k] int32 from csa_topk (-1 entries are skipped).
  *   sink: [n_h] float32.

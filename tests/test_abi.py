@@ -21,13 +21,15 @@ def L():
 def declared(root):
     txt = open(os.path.join(root, "include", "csa.h")).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    names = re.findall(r"^\s*(?:csa_status_t|size_t|int|const char\*)\s+(\w+)\s*\(", txt, flags=re.M)
+    names = re.findall(r"^\s*(?:csa_status_t|size_t|int|int32_t|void|const char\*|csa_block_pool_t\*)"
+                       r"\s+(\w+)\s*\(", txt, flags=re.M)
     return sorted(set(names))
 
 
 def test_exports_every_declared_symbol(L, root):
     names = declared(root)
     assert "csa_attend" in names and "csa_topk" in names and len(names) >= 10
+    assert "csa_block_pool_alloc" in names and "csa_index_topk_paged" in names
     for n in names:
         assert hasattr(L, n), n
 
@@ -104,3 +106,68 @@ def test_workspace_sizes_follow_the_plan(L):
     assert ws >= (8192 + 32768) * 1024
     # shapes the tensor-core path does not take need no workspace
     assert L.csa_attend_workspace_size(1, 1, 100, 16, 16, 4, 128, 32, 4, 16, 0, 0, 0) == 0
+
+
+def test_paged_argument_errors(L):
+    # row maps (csa_pages_t) are checked on the host before any launch
+    from compressed_sparse_long_05_b300._lib import KV, CompressOpts, Pages
+    fake = _p(0x10000)
+    mis = 0x10002
+    tab = 0x20000
+    kv = KV(dtype=1, flags=0, data=0x10000)
+    def att(ent_pages, win_pages):
+        e = KV(dtype=1, flags=0, data=0x10000, pages=ent_pages)
+        w = KV(dtype=1, flags=0, data=0x10000, pages=win_pages)
+        return L.csa_attend(fake, e, fake, w, None, None, fake, fake, 1, 1, 1000, 64, 128, 128,
+                            512, 64, 4, 128, 10000.0, None, 0, None)
+    # too few table columns for N = 1000 entries of 128 rows per block
+    assert att(Pages(tab, 7, 128, 64, 0), Pages()) == 1
+    # misaligned table, zero block rows, empty pool
+    assert att(Pages(mis, 10, 128, 64, 0), Pages()) == 1
+    assert att(Pages(tab, 10, 0, 64, 0), Pages()) == 1
+    assert att(Pages(tab, 10, 128, 0, 0), Pages()) == 1
+    # ring order applies to window rows only
+    assert att(Pages(tab, 10, 128, 64, 1), Pages()) == 1
+    # index keys: tiled loads need power-of-two block rows >= 8 (bf16)
+    for rows, want in ((12, 2), (4, 2)):
+        pg = Pages(tab, 1000, rows, 64, 0)
+        assert L.csa_index_paged(fake, None, fake, fake, None, ctypes.byref(pg), None, fake, 0, 1, 1,
+                                 1000, 64, 128, 4, 1, None) == want
+    # compress into pages: negative first entry, misaligned entry offsets
+    o = CompressOpts(out_pages=Pages(tab, 10, 32, 64, 0), out_first=-1)
+    assert L.csa_compress_ex(fake, fake, fake, fake, None, None, fake, 1, 8, 64, 4, 1,
+                             ctypes.byref(o), None) == 1
+    o = CompressOpts(out_pages=Pages(tab, 10, 32, 64, 0), out_entry0=mis)
+    assert L.csa_compress_ex(fake, fake, fake, fake, None, None, fake, 1, 8, 64, 4, 1,
+                             ctypes.byref(o), None) == 1
+    o = CompressOpts(out_pages=Pages(tab, 10, 32, 64, 1))
+    assert L.csa_compress_ex(fake, fake, fake, fake, None, None, fake, 1, 8, 64, 4, 1,
+                             ctypes.byref(o), None) == 1
+
+
+def test_block_pool():
+    # host-only allocator of the paged cache's physical blocks (no GPU involved)
+    from compressed_sparse_long_05_b300._lib import BlockPool, CsaError
+    p = BlockPool(6)
+    assert p.free_count() == 6
+    a = p.alloc(4)
+    assert a == [0, 1, 2, 3] and p.free_count() == 2
+    with pytest.raises(CsaError) as e:
+        p.alloc(3)                              # only 2 free: nothing is taken
+    assert e.value.status == 3 and p.free_count() == 2
+    for bad in ([4], [0, 0], [7], [-1], [1, 5]):  # free, repeated, out of range, mixed
+        with pytest.raises(CsaError) as e:
+            p.release(bad)
+        assert e.value.status == 1
+    assert p.free_count() == 2                  # refused releases change nothing
+    p.release([2, 0])
+    assert p.free_count() == 4
+    b = p.alloc(4)
+    assert sorted(b) == [0, 2, 4, 5] and p.free_count() == 0
+    p.release(a[1:2] + a[3:] + b)
+    assert p.free_count() == 6 and sorted(p.alloc(6)) == list(range(6))
+    p.close()
+    from compressed_sparse_long_05_b300._lib import lib
+    lib().csa_block_pool_create.restype = ctypes.c_void_p
+    assert lib().csa_block_pool_create(0) is None
+    assert lib().csa_block_pool_create((1 << 30) + 1) is None
