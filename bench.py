@@ -446,6 +446,8 @@ def gpu_arm(args, cfg, rank, world, with_e2e=True):
     e2e = e2e_leg(K, cfg, xs[0], bufs[0], stream, args, dev) if with_e2e else None
     bf16 = (bf16_scores_leg(K, cfg, xs[0], dev)
             if cfg["kind"] == "csa_decode" and cfg["dtype"] != "f32" else None)
+    paged = (paged_leg(K, cfg, xs[0], dev)
+             if cfg["kind"].endswith("decode") and cfg["dtype"] != "f32" else None)
 
     ms_step = ms_total / args.steps
     tokens_per_step = cfg["B"] * cfg["Tq"] * world
@@ -491,6 +493,8 @@ def gpu_arm(args, cfg, rank, world, with_e2e=True):
     }
     if bf16:
         line["bf16_scores"] = bf16
+    if paged:
+        line["paged_kv_cache"] = paged
     x_first = xs[0]
     del xs, bufs, steps, cycle, singles, inst_graphs
     torch.cuda.synchronize()
@@ -604,6 +608,49 @@ def bf16_scores_leg(K, cfg, x, dev, reps=200):
     res["note"] = ("one decode batch of the workload replayed on the same inputs (its 34 MB of keys stay "
                    "in L2), so these are warm-cache times; the pages report a 2x faster selector at 99.7% "
                    "recall on the trained model's scores")
+    return res
+
+
+def paged_leg(K, cfg, x, dev, reps=200):
+    """One decode step of the workload through the paged KV cache (blocks of
+    lcm(m, m') = 128 raw tokens handed out in scrambled order, window rows in a
+    per-sequence ring) against the flat layout on the same inputs: the time of
+    each (CUDA-graph replays, events on the launching stream) and whether the
+    outputs are identical."""
+    from compressed_sparse_long_05_b300 import path as P
+    cache, views = P.PagedKVCache.from_inputs(cfg, x)
+    xp = dict(x)
+    xp.update(views)
+    stream = torch.cuda.Stream(device=dev)
+    res, outs = {}, {}
+    for name, xx in (("flat", x), ("paged", xp)):
+        buf = P.Buffers()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                P.forward(cfg, xx, buf)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            P.forward(cfg, xx, buf)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(10):
+                g.replay()
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+        e1.synchronize()
+        res[name + "_step_ms"] = round(e0.elapsed_time(e1) / reps, 5)
+        outs[name] = buf.out.clone()
+        del g
+    K.device_error()
+    res["identical_output"] = bool(torch.equal(outs["flat"], outs["paged"]))
+    res["blocks"] = {"raw_tokens": cache.block_tokens, "csa_rows": cache.csa_rows,
+                     "hca_rows": cache.hca_rows, "allocated": cache.num_blocks - cache.pool.free_count()}
+    res["note"] = ("the same decode batch replayed on the same inputs for both layouts (warm L2); "
+                   "blocks handed out round-robin over the sequences in shuffled order")
+    cache.pool.close()
     return res
 
 

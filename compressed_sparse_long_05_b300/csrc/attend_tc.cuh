@@ -533,6 +533,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
     bool ok = true;
     for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
       const AttRow x = att_item(a, it);
+      if (n == 0 && gw == 0 && lane == 0) CSA_TRACE_MARK(31);
       if (x.t < 0 && gw == 0 && lane == 0 && x.c == 0 && x.hg == 0) csa_flag_error(ERRBIT_BAD_INDEX);
       if (x.r1 <= x.r0) continue;
       // ---- tiles ----
@@ -749,6 +750,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
       const uint32_t e_base = smem_u32(sE), q_base = smem_u32(sQ), p_base = smem_u32(sP);
       for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
         const AttRow x = att_item(a, it);
+        if (nitem == 0) CSA_TRACE_MARK(29);
         if (x.r1 <= x.r0) continue;
         {
           // queries of this head group: 8 boxes of [64 heads x 64 dims], 128-byte swizzled
@@ -756,7 +758,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
           mbar_arrive_expect_tx(q_full, ATT_HG * ATT_D * 2);
           const int qrow = (x.b * a.Tq + x.i) * a.n_h + x.hg * ATT_HG;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) tma_load_3d(sQ + c * 8192, &tm_q, q_full, c * 64, qrow, 0);
+          for (int c = 0; c < 8; ++c) {
+            tma_load_3d(sQ + c * 8192, &tm_q, q_full, c * 64, qrow, 0);
+            if (nitem == 0 && c == 0) CSA_TRACE_MARK(30);
+          }
           if (nitem == 0) CSA_TRACE_MARK(3);
         }
         if (!mbar_wait(a.rel_rope ? q_full : q_ready, nitem & 1, abort_flag)) { ok = false; break; }

@@ -76,23 +76,34 @@ CSA_DEVINL long long window_base(const int32_t* win_base, int b) {
 struct RowPages {
   const int32_t* table;
   int max_blocks, block_rows, num_blocks, ring;
+  int shift;          // log2(block_rows) when it is a power of two, else -1
 };
 
-// Physical row of logical row j (>= 0) of sequence b, rows per sequence in the
-// flat layout; -1 when the block-table entry is outside the pool (the caller
-// flags it and leaves the row out).
+// Physical row of logical row j (0 <= j < 2^31) of sequence b, rows per
+// sequence in the flat layout; -1 when the block-table entry is outside the
+// pool (the caller flags it and leaves the row out).  32-bit arithmetic, and a
+// shift for power-of-two blocks: one lane may map many rows.
 CSA_DEVINL long long page_row(const RowPages& p, int b, long long j, long long rows) {
   if (!p.table) return (long long)b * rows + j;
-  const long long blk_l = j / p.block_rows;
-  if (blk_l >= p.max_blocks) return -1;
+  const unsigned int ju = (unsigned int)j;
+  unsigned int blk_l, off;
+  if (p.shift >= 0) {
+    blk_l = ju >> p.shift;
+    off = ju & ((1u << p.shift) - 1u);
+  } else {
+    blk_l = ju / (unsigned int)p.block_rows;
+    off = ju - blk_l * (unsigned int)p.block_rows;
+  }
+  if (blk_l >= (unsigned int)p.max_blocks) return -1;
   const int blk = __ldg(p.table + (size_t)b * p.max_blocks + blk_l);
   if (blk < 0 || blk >= p.num_blocks) return -1;
-  return (long long)blk * p.block_rows + (j - blk_l * p.block_rows);
+  return (long long)blk * p.block_rows + off;
 }
 
-// Logical row of window token tok (tokens base .. base + rows - 1 present).
+// Logical row of window token tok (tokens base .. base + rows - 1 present; tok
+// and rows below 2^31).
 CSA_DEVINL long long window_row(const RowPages& p, long long tok, long long base, long long rows) {
-  return p.ring ? tok % rows : tok - base;
+  return p.ring ? (long long)((unsigned int)tok % (unsigned int)rows) : tok - base;
 }
 
 // Programmatic dependent launch.  Every kernel lets the next launch in the

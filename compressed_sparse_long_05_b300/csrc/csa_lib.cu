@@ -210,6 +210,7 @@ csa_status_t plan_index(csa::IndexTcArgs& a, int QT, int B, int Tq, int N) {
 csa_status_t check_pages(const csa_pages_t* p, long long rows, bool ring_ok, bool pow2,
                          RowPages* out) {
   memset(out, 0, sizeof(*out));
+  out->shift = -1;
   if (!p) return CSA_OK;
   if (p->ring && !ring_ok) return CSA_ERR_INVALID_ARG;
   out->ring = p->ring ? 1 : 0;
@@ -223,6 +224,11 @@ csa_status_t check_pages(const csa_pages_t* p, long long rows, bool ring_ok, boo
   out->max_blocks = p->max_blocks;
   out->block_rows = p->block_rows;
   out->num_blocks = p->num_blocks;
+  out->shift = -1;
+  if ((p->block_rows & (p->block_rows - 1)) == 0) {
+    out->shift = 0;
+    while ((1 << out->shift) < p->block_rows) ++out->shift;
+  }
   return CSA_OK;
 }
 

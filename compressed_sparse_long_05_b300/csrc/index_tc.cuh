@@ -64,9 +64,10 @@ constexpr int IDX_HBINS = 1 << IDX_HBITS;
 // their scores are never stored as computed), or the table names a block
 // outside the pool (flagged when `flag`).
 CSA_DEVINL int key_block(const IndexTcArgs& a, int b, int j, int q, bool flag) {
-  const int P = a.k_pg.block_rows;
-  const long long lb = ((long long)j * IDX_TILE + (long long)q * a.k_piece) / P;
-  if (lb >= ((long long)a.N + P - 1) / P) return -1;
+  // block_rows is a power of two for paged keys: shifts, 32-bit (N < 2^31)
+  const int sh = a.k_pg.shift;
+  const unsigned int lb = ((unsigned int)j * IDX_TILE + (unsigned int)(q * a.k_piece)) >> sh;
+  if (lb >= (((unsigned int)a.N + (1u << sh) - 1u) >> sh)) return -1;
   const int blk = __ldg(a.k_pg.table + (size_t)b * a.k_pg.max_blocks + lb);
   if (blk < 0 || blk >= a.k_pg.num_blocks) {
     if (flag) csa_flag_error(ERRBIT_BAD_INDEX);
@@ -76,7 +77,7 @@ CSA_DEVINL int key_block(const IndexTcArgs& a, int b, int j, int q, bool flag) {
 }
 // Row offset of tile j inside its block (nonzero only when block_rows > IDX_TILE).
 CSA_DEVINL int key_block_off(const IndexTcArgs& a, int j) {
-  return (int)(((long long)j * IDX_TILE) % a.k_pg.block_rows);
+  return (int)(((unsigned int)j * IDX_TILE) & ((1u << a.k_pg.shift) - 1u));
 }
 
 // Store one score (float32, or rounded to bf16) at element e of the score rows.
@@ -259,6 +260,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
       bool ok = true, b_issued = false;
       for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
         const IdxItem x = idx_item(a, it);
+        if (nitem == 0) CSA_TRACE_MARK(45);
         if (x.jv <= x.j0) continue;
         const int ntl = x.jv - x.j0;
         auto load_a = [&](int j) -> bool {
@@ -295,7 +297,11 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         };
         // prefetch the first tiles of this item, then swap in its query group
         const int pre = min(ntl, S);
-        for (int jj = 0; jj < pre && ok; ++jj) ok = load_a(x.j0 + jj);
+        for (int jj = 0; jj < pre && ok; ++jj) {
+          ok = load_a(x.j0 + jj);
+          if (nitem == 0 && jj == 0) CSA_TRACE_MARK(46);
+        }
+        if (nitem == 0) CSA_TRACE_MARK(47);
         if (!ok) break;
         if (nitem > 0 && !mbar_wait(b_free, (nitem - 1) & 1, abort_flag, lim)) { ok = false; break; }
         mbar_arrive_expect_tx(b_full, B_BYTES);

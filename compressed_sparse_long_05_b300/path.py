@@ -414,3 +414,37 @@ class PagedKVCache:
         m = self.m_hca if kind == "hca" else self.m
         out = L.Paged(pool, self.table, per, self.max_blocks * per)
         L.csa_compress(Ca, Za, m, Cb=Cb, Zb=Zb, out=out, out_entry0=entry0, out_first=first, **opts)
+
+    @classmethod
+    def from_inputs(cls, cfg: dict, x: dict, extra_blocks=16, seed=0):
+        """A cache holding a decode workload's flat cache tensors (the input dict
+        of :func:`forward`), its blocks handed out round-robin over the
+        sequences in a shuffled order (so no sequence's blocks are contiguous);
+        returns (cache, views) with ``views`` as from :meth:`views`."""
+        import numpy as np
+        B, L, m = cfg["B"], cfg["L"], cfg["m"]
+        kind = "csa" if cfg["kind"].startswith("csa") else "hca"
+        lengths = cfg.get("lengths") or [L] * B
+        mixed = cfg["dtype"] == "mixed"
+        cache = cls(B, L, B * -(-L // 128) + extra_blocks, d=cfg["d"], r=cfg["r"],
+                    c_I=cfg.get("c_I", 128), T_win=cfg["T_win"], m=4, m_hca=128,
+                    storage="mixed" if mixed else "bf16", device=x["q"].device)
+        rng = np.random.default_rng(seed)
+        for j in range(-(-L // cache.block_tokens)):
+            for b in rng.permutation(B):
+                if j * cache.block_tokens < lengths[b]:
+                    cache.reserve(int(b), min(lengths[b], (j + 1) * cache.block_tokens))
+        for b, Lb in enumerate(lengths):
+            Nb = Lb // m
+            if mixed:
+                cache.load("entries", b, (x["ent_nope"][b, :Nb], x["ent_scale"][b, :Nb],
+                                          x["ent_rope"][b, :Nb]))
+                cache.load("keys", b, x["K_fp4"][b, :Nb], sf=x["K_sf"][b, :Nb])
+                cache.load_window(b, (x["win_nope"][b], x["win_scale"][b], x["win_rope"][b]),
+                                  int(x["win_base"][b]))
+            else:
+                cache.load("hca" if kind == "hca" else "entries", b, x["entries"][b, :Nb])
+                if kind == "csa":
+                    cache.load("keys", b, x["K"][b, :Nb])
+                cache.load_window(b, x["win"][b], int(x["win_base"][b]))
+        return cache, cache.views(kind, cfg["N"])

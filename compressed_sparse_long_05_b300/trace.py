@@ -23,6 +23,9 @@ import numpy as np
 KERNELS = {
     "index (index_tc_kernel)": (32, 33, 44, 43, {
         34: "barriers + TMEM allocated",
+        45: "producer: first item's tiles known",
+        46: "producer: first K-tile copy issued",
+        47: "producer: first item's prefetch copies issued",
         35: "producer: first item's query group issued",
         36: "MMA: first K tile landed",
         37: "MMA: every MMA of the first item issued",
@@ -41,7 +44,10 @@ KERNELS = {
     }),
     "attention (attend_tc_kernel)": (0, 1, 22, 21, {
         2: "barriers + TMEM allocated",
+        29: "MMA warp: first item's rows known",
+        30: "MMA warp: first q box issued",
         3: "q TMA issued (MMA warp)",
+        31: "gather warp 4: first item's rows known",
         4: "q landed (MMA warp)",
         5: "traced tile: row sources known (gather warp 4)",
         6: "traced tile: every row copy issued",
@@ -87,6 +93,8 @@ def main():
                     help="which tile of each attention CTA its per-tile marks describe")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=INT",
                     help="override a size of the workload")
+    ap.add_argument("--paged", action="store_true",
+                    help="decode through the paged KV cache (blocks in shuffled order)")
     args = ap.parse_args()
     build.build(trace=True)
     L = _lib.lib()
@@ -95,6 +103,9 @@ def main():
     L.csa_trace_set_tile.argtypes = [ctypes.c_int]
     L.csa_trace_set_tile(args.tile)
     x = synth.make_inputs(cfg, seed=0, device="cuda")
+    if args.paged:
+        cache, views = P.PagedKVCache.from_inputs(cfg, x)
+        x.update(views)
     buf = P.Buffers()
     P.forward(cfg, x, buf)                          # every stage once (sizes buffers)
     torch.cuda.synchronize()
