@@ -485,6 +485,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) { CSA_TRACE_WALL(0); CSA_TRACE_MARK(1); }
+  if (threadIdx.x == 32 && (int)blockIdx.x < a.items) {
+    // the first item's position and window base (read by every role's first item)
+    const int rest = (int)blockIdx.x / a.nch / a.HG;
+    const int qi = rest % a.Tq, qb = rest / a.Tq;
+    if (a.q_pos) prefetch_l1(a.q_pos + (size_t)qb * a.Tq + qi);
+    if (a.win_base) prefetch_l1(a.win_base + qb);
+  }
 
   if (threadIdx.x == 0) {
     for (int c = 0; c < 8; ++c) mbar_init(chunk_full + c, 4);

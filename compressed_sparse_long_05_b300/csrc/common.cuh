@@ -63,6 +63,11 @@ __device__ int g_csa_trace_tile;   // which tile of a CTA the per-tile marks des
 CSA_DEVINL long long query_pos(const int32_t* q_pos, long long row, int i) {
   return q_pos ? (long long)__ldg(q_pos + row) : (long long)i;
 }
+// Hint: bring the line of p into L1 (no wait; the first item's small reads
+// issued at kernel entry so their latency overlaps the set-up).
+CSA_DEVINL void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 // Window buffer base token of batch row b (0 without a base array).
 CSA_DEVINL long long window_base(const int32_t* win_base, int b) {
   return win_base ? (long long)__ldg(win_base + b) : 0LL;

@@ -190,6 +190,14 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_K); prefetch_tmap(&tm_q); prefetch_tmap(&tm_Ksf); prefetch_tmap(&tm_qsf);
   }
+  if (warp == 2 && lane == 0 && (int)blockIdx.x < a.items) {
+    // the first item's query positions and head weights
+    int b0, j0, j1;
+    idx_chunk(a, blockIdx.x, b0, j0, j1);
+    const int t0 = ((int)blockIdx.x % (a.G * a.chunks)) / a.chunks * a.QT;
+    if (a.q_pos) prefetch_l1(a.q_pos + (size_t)b0 * a.Tq + t0);
+    prefetch_l1(a.w + ((size_t)b0 * a.Tq + t0) * H);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -395,14 +403,16 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
         }
       }
       if (a.hist) {
-        // both groups have added this item's scores: one group flushes (and clears)
-        // the shared per-quarter histograms; the next item's adds wait for that.
+        // both groups have added this item's scores: all eight warps flush (and
+        // clear) the shared per-quarter histograms; the next item's adds wait for that.
         // Bounded waits: a warp that gave up still arrives, and the flag ends the rest.
         __syncwarp();
         if (lane == 0) mbar_arrive(epi_sync);
         const bool s1 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
         ++nsync;
-        if (ok && s1 && grp == 0) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
+        if (ok && s1)
+          hist_flush(reinterpret_cast<uint32_t*>(smem + L::OFF_HIST),
+                     a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS, ew * 32 + lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(epi_sync);
         const bool s2 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));

@@ -99,13 +99,21 @@ CSA_DEVINL void hist_add(uint32_t* wh, float score, bool visible) {
     if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(wh + dig, (uint32_t)__popc(peers));
   }
 }
-// One warp adds its shared histogram into the row's global one and clears it.
-CSA_DEVINL void hist_flush(uint32_t* wh, uint32_t* gh) {
-  for (int b = threadIdx.x & 31; b < IDX_HBINS; b += 32) {
-    const uint32_t c = wh[b];
-    if (c) { atomicAdd(gh + b, c); wh[b] = 0; }
+// The eight epilogue warps (thread e of 256) add the four per-quarter shared
+// histograms into the row's global one and clear them: one global atomic per
+// nonzero bin of the CTA, eight bins per thread.
+CSA_DEVINL void hist_flush(uint32_t* h4, uint32_t* gh, int e) {
+#pragma unroll
+  for (int b = e; b < IDX_HBINS; b += 256) {
+    const uint32_t c = h4[b] + h4[IDX_HBINS + b] + h4[2 * IDX_HBINS + b] + h4[3 * IDX_HBINS + b];
+    if (c) {
+      atomicAdd(gh + b, c);
+      h4[b] = 0;
+      h4[IDX_HBINS + b] = 0;
+      h4[2 * IDX_HBINS + b] = 0;
+      h4[3 * IDX_HBINS + b] = 0;
+    }
   }
-  __syncwarp();
 }
 
 // Shared-memory layout, sized at launch: S K-tile stages (4, or 6 when the
@@ -181,6 +189,15 @@ CSA_DEVINL void check_item_pos(const IndexTcArgs& a, const IdxItem& x) {
       csa_flag_error(ERRBIT_BAD_INDEX);
 }
 
+// Tiles [j0, j1) of item `it` (its chunk of the entry range), which do not
+// depend on the query positions.
+CSA_DEVINL void idx_chunk(const IndexTcArgs& a, int it, int& b, int& j0, int& j1) {
+  b = it / (a.G * a.chunks);
+  const int c = (it % (a.G * a.chunks)) % a.chunks;
+  j0 = c * a.chunk_tiles;
+  j1 = min(a.tiles_max, j0 + a.chunk_tiles);
+}
+
 CSA_DEVINL IdxItem idx_item(const IndexTcArgs& a, int it) {
   IdxItem x;
   x.b = it / (a.G * a.chunks);
@@ -246,6 +263,14 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
     for (int b = threadIdx.x; b < 4 * IDX_HBINS; b += blockDim.x) h[b] = 0;
   }
   if (warp == 0 && lane == 0) { prefetch_tmap(&tm_K); prefetch_tmap(&tm_q); }
+  if (warp == 2 && lane == 0 && (int)blockIdx.x < a.items) {
+    // the first item's query positions and head weights
+    int b0, j0, j1;
+    idx_chunk(a, blockIdx.x, b0, j0, j1);
+    const int t0 = ((int)blockIdx.x % (a.G * a.chunks)) / a.chunks * a.QT;
+    if (a.q_pos) prefetch_l1(a.q_pos + (size_t)b0 * a.Tq + t0);
+    prefetch_l1(a.w + ((size_t)b0 * a.Tq + t0) * H);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -258,12 +283,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
     if (lane == 0) {
       uint32_t ia = 0, nitem = 0;
       bool ok = true, b_issued = false;
-      for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
-        const IdxItem x = idx_item(a, it);
-        if (nitem == 0) CSA_TRACE_MARK(45);
-        if (x.jv <= x.j0) continue;
-        const int ntl = x.jv - x.j0;
-        auto load_a = [&](int j) -> bool {
+      auto load_a = [&](int b, int j) -> bool {
           const uint32_t st = ia % S, ph = (ia / S) & 1;
           if (!mbar_wait(empty + st, ph ^ 1, abort_flag, lim)) return false;
           if (blockIdx.x == 0 && a.skip_load_plus1 == (int)ia + 1) {
@@ -275,11 +295,11 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
             const int np = IDX_TILE / a.k_piece, off = key_block_off(a, j);
             uint32_t mask = 0;
             for (int q = 0; q < np; ++q)
-              if (key_block(a, x.b, j, q, true) >= 0) mask |= 1u << q;
+              if (key_block(a, b, j, q, true) >= 0) mask |= 1u << q;
             mbar_arrive_expect_tx(full + st, (uint32_t)(__popc(mask) * a.k_piece * 128 * L.KCH));
             for (int q = 0; q < np; ++q) {
               if (!(mask >> q & 1u)) continue;
-              const int blk = key_block(a, x.b, j, q, false);
+              const int blk = key_block(a, b, j, q, false);
               for (int kc = 0; kc < L.KCH; ++kc)
                 tma_load_3d(sA + st * L.A_BYTES + kc * (IDX_TILE * 128) + q * a.k_piece * 128, &tm_K,
                             full + st, kc * 64, off, blk);
@@ -291,16 +311,33 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
 #pragma unroll
           for (int kc = 0; kc < L.KCH; ++kc)
             tma_load_3d(sA + st * L.A_BYTES + kc * (IDX_TILE * 128), &tm_K, full + st, kc * 64,
-                        j * IDX_TILE, x.b);
+                        j * IDX_TILE, b);
           ++ia;
           return true;
         };
-        // prefetch the first tiles of this item, then swap in its query group
-        const int pre = min(ntl, S);
-        for (int jj = 0; jj < pre && ok; ++jj) {
-          ok = load_a(x.j0 + jj);
-          if (nitem == 0 && jj == 0) CSA_TRACE_MARK(46);
+      for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
+        // The CTA's first item: its first S tiles go out before the query
+        // positions are read (the copies do not depend on them), so the position
+        // read overlaps them.  Tiles that turn out invisible are waited out and
+        // released by the MMA warp.
+        int spec = 0;
+        if (it == (int)blockIdx.x) {
+          int b0, j0, j1;
+          idx_chunk(a, it, b0, j0, j1);
+          spec = max(0, min(S, j1 - j0));
+          for (int jj = 0; jj < spec && ok; ++jj) {
+            ok = load_a(b0, j0 + jj);
+            if (jj == 0) CSA_TRACE_MARK(46);
+          }
+          if (!ok) break;
         }
+        const IdxItem x = idx_item(a, it);
+        if (nitem == 0) CSA_TRACE_MARK(45);
+        if (x.jv <= x.j0) continue;
+        const int ntl = x.jv - x.j0;
+        // prefetch the first tiles of this item, then swap in its query group
+        const int pre = max(spec, min(ntl, S));
+        for (int jj = spec; jj < pre && ok; ++jj) ok = load_a(x.b, x.j0 + jj);
         if (nitem == 0) CSA_TRACE_MARK(47);
         if (!ok) break;
         if (nitem > 0 && !mbar_wait(b_free, (nitem - 1) & 1, abort_flag, lim)) { ok = false; break; }
@@ -310,7 +347,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
         b_issued = true;
         if (nitem == 0) CSA_TRACE_MARK(35);
         ++nitem;
-        for (int jj = pre; jj < ntl && ok; ++jj) ok = load_a(x.j0 + jj);
+        for (int jj = pre; jj < ntl && ok; ++jj) ok = load_a(x.b, x.j0 + jj);
       }
       // drain copies still in flight before the CTA may exit
       for (uint32_t k = (ia > (uint32_t)S ? ia - S : 0); k < ia; ++k)
@@ -325,33 +362,43 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
       const uint32_t idesc = idesc_bf16(IDX_TILE, NQH);
       for (int it = blockIdx.x; it < a.items && ok; it += gridDim.x) {
         const IdxItem x = idx_item(a, it);
-        if (x.jv <= x.j0) continue;
-        if (!mbar_wait(b_full, nitem & 1, abort_flag, lim)) { ok = false; break; }
-        for (int j = x.j0; j < x.jv; ++j) {
-          const uint32_t st = ia % S, ph = (ia / S) & 1;
-          const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
-          if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag, lim)) { ok = false; break; }
-          if (!mbar_wait(full + st, ph, abort_flag, lim)) { ok = false; break; }
-          if (ia == 0) CSA_TRACE_MARK(36);
-          tc_fence_after();
-          const uint32_t aBase = smem_u32(sA + st * L.A_BYTES);
-          const uint32_t bBase = smem_u32(sB);
-          const uint32_t d = tmem + buf * (uint32_t)NQH;
+        // first item: stages the producer filled ahead for tiles past the visible ones
+        const int extra = it == (int)blockIdx.x
+                              ? max(0, max(0, min(S, x.j1 - x.j0)) - max(0, x.jv - x.j0)) : 0;
+        if (x.jv > x.j0) {
+          if (!mbar_wait(b_full, nitem & 1, abort_flag, lim)) { ok = false; break; }
+          for (int j = x.j0; j < x.jv; ++j) {
+            const uint32_t st = ia % S, ph = (ia / S) & 1;
+            const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
+            if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag, lim)) { ok = false; break; }
+            if (!mbar_wait(full + st, ph, abort_flag, lim)) { ok = false; break; }
+            if (ia == 0) CSA_TRACE_MARK(36);
+            tc_fence_after();
+            const uint32_t aBase = smem_u32(sA + st * L.A_BYTES);
+            const uint32_t bBase = smem_u32(sB);
+            const uint32_t d = tmem + buf * (uint32_t)NQH;
 #pragma unroll
-          for (int kk = 0; kk < C / 16; ++kk) {
-            const uint32_t kc = kk / 4, ko = (kk % 4) * 32;
-            const uint64_t ad = sdesc_sw128(aBase + kc * (IDX_TILE * 128) + ko, 16, 1024);
-            const uint64_t bd = sdesc_sw128(bBase + kc * (NQH * 128) + ko, 16, 1024);
-            umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < C / 16; ++kk) {
+              const uint32_t kc = kk / 4, ko = (kk % 4) * 32;
+              const uint64_t ad = sdesc_sw128(aBase + kc * (IDX_TILE * 128) + ko, 16, 1024);
+              const uint64_t bd = sdesc_sw128(bBase + kc * (NQH * 128) + ko, 16, 1024);
+              umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(empty + st);
+            umma_commit(acc_full + buf);
+            ++ia;
+            ++iacc;
           }
-          umma_commit(empty + st);
-          umma_commit(acc_full + buf);
-          ++ia;
-          ++iacc;
+          if (!ok) break;
+          CSA_TRACE_MARK(37);
+          umma_commit(b_free);
+          ++nitem;
         }
-        CSA_TRACE_MARK(37);
-        umma_commit(b_free);
-        ++nitem;
+        for (int e = 0; e < extra; ++e, ++ia) {     // no MMA reads them: wait for the copy, release
+          const uint32_t st = ia % S, ph = (ia / S) & 1;
+          if (!mbar_wait(full + st, ph, abort_flag, lim)) { ok = false; break; }
+          mbar_arrive(empty + st);
+        }
       }
       umma_commit(mma_done);
       mbar_drain(mma_done, 0, lim);
@@ -402,15 +449,17 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant_
       }
       if (ew == 0 && lane == 0) CSA_TRACE_MARK(40);
       if (a.hist) {
-        // both groups have added this item's scores: one group flushes (and clears)
-        // the shared per-quarter histograms; the next item's adds wait for that.
+        // both groups have added this item's scores: all eight warps flush (and
+        // clear) the shared per-quarter histograms; the next item's adds wait for that.
         // Bounded waits: a warp that gave up still arrives, and the flag ends the rest.
         __syncwarp();
         if (lane == 0) mbar_arrive(epi_sync);
         const bool s1 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag, lim));
         ++nsync;
         if (ew == 0 && lane == 0) CSA_TRACE_MARK(41);
-        if (ok && s1 && grp == 0) hist_flush(wh, a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS);
+        if (ok && s1)
+          hist_flush(reinterpret_cast<uint32_t*>(smem + L.OFF_HIST),
+                     a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS, ew * 32 + lane);
         if (ew == 0 && lane == 0) CSA_TRACE_MARK(42);
         __syncwarp();
         if (lane == 0) mbar_arrive(epi_sync);
