@@ -90,7 +90,10 @@ struct AttendTcArgs {
   int rotate_rows;               // 1 = rotate gathered rows in shared memory
   int rel_rope;                  // 1 = rows rotated by (position - t): q and out stay unrotated
   int kv_mixed;                  // 1 = e4m3 + scale + bf16 rope rows
-  int cl_reduce;                 // 1 = the nch chunks of a head group are one cluster and merge over DSMEM
+  int cl_reduce;                 // 1 = clusters of ncs consecutive chunks merge over DSMEM
+  int ncs;                       // chunks per cluster (cl_reduce): nch, or a divisor of it
+  int cl_partial;                // 1 = each cluster merges its ncs chunks into one fp32 partial
+                                 //     (part_o / part_ml at index item / ncs) for the combine kernel
   int ent_rotated;               // 1 = entries stored with their RoPE dims already rotated at m(s+1)-1
   RowPages ent_pg, win_pg;       // paged / ring row maps (no table: flat)
   float scale_log2;              // log2(e) / sqrt(d)
@@ -332,7 +335,7 @@ CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint3
                                      uint64_t* merge_bar, uint64_t* ml_bar) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
-  const int nch = a.nch;
+  const int nch = a.ncs;                              // chunks merged by this cluster
   const int crank = (int)cl.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const AttRow x = att_item(a, blockIdx.x);
@@ -397,7 +400,26 @@ CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint3
   }
   // while the copies fly: the weight of every (chunk, head),
   // 2^(m_c - M_h) / (sum_c' l_c' 2^(m_c' - M_h) + 2^(z'_h - M_h)), written over m_c
-  if (threadIdx.x >= 32 && threadIdx.x < 32 + ATT_HG) {
+  if (a.cl_partial && threadIdx.x >= 32 && threadIdx.x < 32 + ATT_HG) {
+    // partial of this cluster's chunks: weights 2^(m_c - M), and (M, sum_c l_c 2^(m_c - M))
+    // for the combine kernel (no sink, no normalisation here)
+    const int h = threadIdx.x - 32;
+    float M = -INFINITY;
+    for (int k = 0; k < nch; ++k)
+      if (mlall[(k * ATT_HG + h) * 2 + 1] > 0.f) M = fmaxf(M, mlall[(k * ATT_HG + h) * 2]);
+    float L = 0.f;
+    for (int k = 0; k < nch; ++k) {
+      const float lk = mlall[(k * ATT_HG + h) * 2 + 1];
+      const float ek = lk > 0.f ? exp2f(mlall[(k * ATT_HG + h) * 2] - M) : 0.f;
+      mlall[(k * ATT_HG + h) * 2] = ek;
+      L += lk * ek;
+    }
+    if (crank == 0) {
+      float* pm = a.part_ml + ((size_t)(blockIdx.x / nch) * ATT_HG + h) * 2;
+      pm[0] = M;
+      pm[1] = L;
+    }
+  } else if (threadIdx.x >= 32 && threadIdx.x < 32 + ATT_HG) {
     const int h = threadIdx.x - 32;
     const float zs = reinterpret_cast<const float*>(smem + AttSmem::SINK)[h];
     float M = zs;
@@ -434,7 +456,14 @@ CSA_DEVINL void attend_cluster_merge(const AttendTcArgs& a, uint8_t* smem, uint3
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, f[e], acc[e]);
       }
-      *reinterpret_cast<uint4*>(a.out + (orow + h) * ATT_D + lo + 8 * g) = f_to_bf16x8(acc);
+      if (a.cl_partial) {
+        float4* po = reinterpret_cast<float4*>(
+            a.part_o + ((size_t)(blockIdx.x / nch) * ATT_HG + h) * ATT_D + lo + 8 * g);
+        po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+        *reinterpret_cast<uint4*>(a.out + (orow + h) * ATT_D + lo + 8 * g) = f_to_bf16x8(acc);
+      }
     }
   }
   if (threadIdx.x == 0) CSA_TRACE_MARK(26);
@@ -510,9 +539,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
     mbar_init(ml_bar, 1);
     if (a.cl_reduce) {
       // the merge receives nch (max, sum) sets and nch blocks of partials
-      const int pitch = merge_pitch(a.nch);
-      mbar_arrive_expect_tx(ml_bar, (uint32_t)(a.nch * ATT_HG * 8));
-      mbar_arrive_expect_tx(merge_bar, (uint32_t)(a.nch * ATT_HG * pitch * 2));
+      const int pitch = merge_pitch(a.ncs);
+      mbar_arrive_expect_tx(ml_bar, (uint32_t)(a.ncs * ATT_HG * 8));
+      mbar_arrive_expect_tx(merge_bar, (uint32_t)(a.ncs * ATT_HG * pitch * 2));
     }
     *abort_flag = 0;
     reinterpret_cast<volatile int*>(smem + AttSmem::MISC)[2] = 0;   // this CTA's O holds rows

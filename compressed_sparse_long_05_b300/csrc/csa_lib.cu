@@ -335,6 +335,8 @@ csa_status_t launch_index_tc(const void* qI, const float* w, const void* K, cons
 // Work split and scratch layout of the tensor-core attention path.
 struct AttPlan {
   int HG, nch, chunk_rows, items, rotate_rows, rel_rope, cl_reduce;
+  int ncs;          // chunks per merging cluster (cl_reduce)
+  int cl_partial;   // clusters merge into partials that the combine kernel finishes
   size_t off_part_o, off_part_ml, off_rot_ent, off_rot_win, bytes;
 };
 
@@ -413,12 +415,31 @@ AttPlan plan_attend(int B, int Tq, int N, int k, int T_win, int n_h, int n_win, 
   // the chunks of each head group merge inside a cluster when they all run at once
   p.cl_reduce = (p.nch > 1 && p.nch <= 16 && p.items <= sms && p.rel_rope &&
                  attend_max_clusters(p.nch) >= p.items / p.nch) ? 1 : 0;
+  p.ncs = p.cl_reduce ? p.nch : 0;
+  p.cl_partial = 0;
+  if (!p.cl_reduce && p.nch > 1 && p.items <= sms && p.rel_rope) {
+    // otherwise: clusters of ncs chunks (the largest size whose clusters all
+    // fit at once; the chunk count padded to a multiple with empty chunks)
+    // each merge into one partial, and the combine kernel merges those
+    for (int ncs = 16; ncs >= 2 && !p.cl_partial; --ncs) {
+      const int ncl = (p.nch + ncs - 1) / ncs;
+      if (ncl < 2) continue;
+      const long long items = units * (long long)ncl * ncs;
+      if (items > sms || attend_max_clusters(ncs) < items / ncs) continue;
+      p.nch = ncl * ncs;
+      p.items = (int)items;
+      p.ncs = ncs;
+      p.cl_reduce = 1;
+      p.cl_partial = 1;
+    }
+  }
   size_t off = 0;
-  if (p.nch > 1 && !p.cl_reduce) {
+  const long long parts = p.cl_partial ? (long long)p.items / p.ncs : (long long)p.items;
+  if (p.nch > 1 && (!p.cl_reduce || p.cl_partial)) {
     p.off_part_o = off;
-    off = align256(off + (size_t)p.items * csa::ATT_HG * csa::ATT_D * sizeof(float));
+    off = align256(off + (size_t)parts * csa::ATT_HG * csa::ATT_D * sizeof(float));
     p.off_part_ml = off;
-    off = align256(off + (size_t)p.items * csa::ATT_HG * 2 * sizeof(float));
+    off = align256(off + (size_t)parts * csa::ATT_HG * 2 * sizeof(float));
   }
   if (!p.rotate_rows) {
     p.off_rot_ent = off;
@@ -933,6 +954,8 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
   a.HG = p.HG; a.nch = p.nch; a.chunk_rows = p.chunk_rows; a.items = p.items;
   a.rotate_rows = p.rotate_rows; a.kv_mixed = mixed;
   a.cl_reduce = p.cl_reduce;
+  a.ncs = p.ncs;
+  a.cl_partial = p.cl_partial;
   a.rel_rope = p.rel_rope;
   a.ent_rotated = (c.ent.flags & CSA_KV_ROTATED) ? 1 : 0;
   a.ent_pg = ent_pg; a.win_pg = win_pg;
@@ -966,7 +989,7 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
       memset(&a.win_pg, 0, sizeof(a.win_pg));     // flat, token order from win_base
     }
   }
-  if (p.nch > 1 && !p.cl_reduce) {
+  if (p.nch > 1 && (!p.cl_reduce || p.cl_partial)) {
     a.part_o = reinterpret_cast<float*>(wsb + p.off_part_o);
     a.part_ml = reinterpret_cast<float*>(wsb + p.off_part_ml);
   }
@@ -981,21 +1004,22 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc attr");
   const int sms = sm_count();
   const int grid = p.items < sms ? p.items : sms;
-  if (p.cl_reduce && p.nch > 8) {
+  if (p.cl_reduce && p.ncs > 8) {
     e = cudaFuncSetAttribute(csa::attend_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_fail(e, "csa_attend cluster attr");
   }
   e = launch_ex_pdl(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st,
-                    p.cl_reduce ? p.nch : 1, kProgrammaticLaunch, tmq, a);
+                    p.cl_reduce ? p.ncs : 1, kProgrammaticLaunch, tmq, a);
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc launch");
-  if (p.nch > 1 && !p.cl_reduce) {
+  if (p.nch > 1 && (!p.cl_reduce || p.cl_partial)) {
     csa::CombineArgs ca;
     memset(&ca, 0, sizeof(ca));
     ca.part_o = a.part_o; ca.part_ml = a.part_ml; ca.sink = c.sink; ca.out = a.out;
     ca.q_pos = c.q_pos;
-    ca.Tq = c.Tq; ca.n_h = c.n_h; ca.HG = p.HG; ca.nch = p.nch; ca.rf = rf;
+    ca.Tq = c.Tq; ca.n_h = c.n_h; ca.HG = p.HG; ca.rf = rf;
+    ca.nch = p.cl_partial ? p.nch / p.ncs : p.nch;     // partials per (query row, head group)
     ca.rel_rope = p.rel_rope;
-    const size_t cmb_smem = (size_t)p.nch * csa::ATT_HG * 2 * sizeof(float);
+    const size_t cmb_smem = (size_t)ca.nch * csa::ATT_HG * 2 * sizeof(float);
     if (cmb_smem > 48 * 1024) {
       e = cudaFuncSetAttribute(csa::attend_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)cmb_smem);

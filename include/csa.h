@@ -330,10 +330,11 @@ size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h
  *     CSA_NOALLOC_SCRATCH_BYTES return CSA_ERR_WORKSPACE before any launch
  *     (csa_last_cuda_error() then gives both byte counts).  For scale: a
  *     decode row set whose chunks (at most 16) merge inside a thread-block
- *     cluster needs none (batch 4, k = 1024, V4-Pro shape); a split that
- *     does not keeps 128 KB of fp32 partials per CTA (8.7 MB for one
- *     sequence at k = 4096); many query rows over few stored rows keep one
- *     rotated copy of the rows (1 KB per row).
+ *     cluster needs none (batch 4, k = 1024, V4-Pro shape); chunks that
+ *     merge in smaller clusters keep 128 KB of fp32 partials per cluster;
+ *     a split with more work items than SMs keeps 128 KB per item (20 MB for
+ *     16 sequences at k = 4096); many query rows over few stored rows keep
+ *     one rotated copy of the rows (1 KB per row).
  *   - The first call on a device (with that device current) looks up the
  *     array's device address and caches it; make that first call before any
  *     stream capture.

@@ -120,7 +120,9 @@ def _raw_call(K, c, k, d=512, out=None):
 def test_noalloc_rejects_sizes_beyond_the_array():
     import compressed_sparse_long_05_b300 as K
     from compressed_sparse_long_05_b300 import _lib
-    c = _decode_case(K, lengths=[160000] * 4, N=40000, k=4096, seed=530)
+    # 16 sequences at k = 4096: 160 work items, more than one per SM, so every
+    # chunk keeps a 128 KB float32 partial (20 MB)
+    c = _decode_case(K, lengths=[160000] * 16, N=40000, k=4096, seed=530)
     assert _need(K, c) > SCRATCH_BYTES
     out = torch.zeros_like(c["q"])
     assert _raw_call(K, c, 4096, out=out) == 3          # CSA_ERR_WORKSPACE, before any launch
