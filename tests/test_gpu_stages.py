@@ -278,6 +278,22 @@ def test_hca_attend_bf16_decode(K):
                  dense=True, seed=90)
 
 
+def test_hca_attend_bf16_decode_cluster_partials(K):
+    # 33 row chunks per head group (8320 rows): more than one co-resident cluster
+    # can hold, so clusters of fewer chunks merge into partials that the combine
+    # kernel finishes.  The scratch size shows the plan: far fewer 128 KB
+    # partials than the 132 work items.
+    from compressed_sparse_long_05_b300 import _lib
+    N = 8192
+    L = 128 * N
+    ws = _lib.lib().csa_attend_workspace_size(2, 1, N, 0, 128, 128, 512, 64, 128, 128, 1, 1, 1)
+    part = 64 * 512 * 4
+    assert 0 < ws < 132 * part
+    assert ws // part < 66
+    _attend_case(K, B=2, Tq=1, N=N, k=0, q_pos0=L - 1, T_win=128, win_base=L - 128, m=128,
+                 dense=True, seed=95)
+
+
 def test_hca_attend_bf16_prefill(K):
     T = 1100
     _attend_case(K, B=1, Tq=T, N=T // 128, k=0, q_pos0=0, T_win=T, win_base=0, m=128, dense=True,
