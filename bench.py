@@ -42,12 +42,17 @@ L2_BYTES = 126 * 1024 * 1024
 
 
 def kernel_source_sha():
-    """First 12 hex digits of the sha256 over the kernel sources (csrc/*.cu, *.cuh)."""
+    """First 12 hex digits of the sha256 over the kernel sources (csrc/*.cu, *.cuh),
+    leaving out the lines that hold phase-trace marks (they compile to nothing
+    outside the -DCSA_TRACE build, so they do not change the measured kernels)."""
     import glob
     import hashlib
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "compressed_sparse_long_05_b300", "csrc", "*.cu*"))):
-        h.update(open(f, "rb").read())
+        for line in open(f, "rb"):
+            if b"CSA_TRACE_MARK(" in line or b"CSA_TRACE_WALL(" in line:
+                continue
+            h.update(line)
     return h.hexdigest()[:12]
 
 

@@ -133,6 +133,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
                  IndexFp4Args fa) {
   using L = IndexFp4Smem;
   const IndexTcArgs& a = fa.t;
+  if (threadIdx.x == 0) { CSA_TRACE_WALL(32); CSA_TRACE_MARK(33); }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem<1024>(smem_raw);
   uint8_t* sA = smem + L::OFF_A;
@@ -203,6 +204,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
+  if (threadIdx.x == 0) CSA_TRACE_MARK(34);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -267,8 +269,10 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
               : "memory");
         }
         b_issued = true;
+        if (nitem == 0) CSA_TRACE_MARK(35);
         ++nitem;
         for (int jj = pre; jj < ntl && ok; ++jj) ok = load_a(x.j0 + jj);
+        if (nitem == 1) CSA_TRACE_MARK(59);
       }
       for (uint32_t k = (ia > FP4_STAGES ? ia - FP4_STAGES : 0); k < ia; ++k)
         mbar_drain(full + (k % FP4_STAGES), (k / FP4_STAGES) & 1);
@@ -290,6 +294,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
           if (!mbar_wait(acc_empty + buf, aph ^ 1, abort_flag)) { ok = false; break; }
           if (!mbar_wait(sf_ready + st, ph, abort_flag)) { ok = false; break; }
+          if (ia == 0) CSA_TRACE_MARK(36);
           tc_fence_after();
           const uint32_t sfa = tmem + TM_SFA + st * 8;
           const uint32_t aBase = smem_u32(sA + st * L::A_BYTES);
@@ -304,6 +309,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           ++iacc;
         }
         if (!ok) break;
+        CSA_TRACE_MARK(37);
         umma_commit(b_free);
         ++nitem;
       }
@@ -350,6 +356,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           tmem_cp_32x128b_x4(sfa, sdesc_atom(smem_u32(atomA + st * 1024)));
           tmem_cp_32x128b_x4(sfa + 4, sdesc_atom(smem_u32(atomA + st * 1024 + 512)));
           umma_commit(sf_ready + st);
+          if (sw == 0) CSA_TRACE_MARK(ia == 0 ? 57 : 58);
         }
         __syncwarp();
       }
@@ -397,6 +404,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + buf);
+          if (ew == 0 && lane == 0) CSA_TRACE_MARK(iacc <= 2 ? 38 : 39);
         } else if ((j & 1) == grp) {
           for (int qi = 0; qi < x.nq; ++qi)
             if (s < a.N) store_score(a.scores, a.scores_bf16, srow + (size_t)qi * a.N, -INFINITY);
@@ -410,9 +418,11 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
         if (lane == 0) mbar_arrive(epi_sync);
         const bool s1 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
         ++nsync;
+        if (ew == 0 && lane == 0) CSA_TRACE_MARK(41);
         if (ok && s1)
           hist_flush(reinterpret_cast<uint32_t*>(smem + L::OFF_HIST),
                      a.hist + ((size_t)x.b * a.Tq + x.t0) * IDX_HBINS, ew * 32 + lane);
+        if (ew == 0 && lane == 0) CSA_TRACE_MARK(42);
         __syncwarp();
         if (lane == 0) mbar_arrive(epi_sync);
         const bool s2 = __all_sync(0xffffffffu, mbar_wait(epi_sync, nsync & 1, abort_flag));
@@ -426,6 +436,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0) { CSA_TRACE_MARK(44); CSA_TRACE_WALL(43); }
 }
 
 }  // namespace csa

@@ -21,7 +21,7 @@ import numpy as np
 
 # kernel -> (wall-clock entry slot, clock entry slot, clock exit slot, wall exit slot, phases)
 KERNELS = {
-    "index (index_tc_kernel)": (32, 33, 44, 43, {
+    "index (index_tc_kernel or index_fp4_kernel)": (32, 33, 44, 43, {
         34: "barriers + TMEM allocated",
         45: "producer: first item's tiles known",
         46: "producer: first K-tile copy issued",
@@ -34,6 +34,9 @@ KERNELS = {
         40: "epilogue warp 2: item's tiles done",
         41: "histogram flush start",
         42: "histogram flush end",
+        57: "FP4: scale warp 2, first tile's scale atoms in tensor memory",
+        58: "FP4: scale warp 2, last tile's scale atoms in tensor memory",
+        59: "FP4: producer, every copy of the first item issued",
     }),
     "top-k (topk2_kernel)": (48, 49, 56, 55, {
         50: "histogram read, cluster barrier passed",
