@@ -37,6 +37,10 @@ KERNELS = {
         57: "FP4: scale warp 2, first tile's scale atoms in tensor memory",
         58: "FP4: scale warp 2, last tile's scale atoms in tensor memory",
         59: "FP4: producer, every copy of the first item issued",
+        60: "FP4: epilogue warp 4, its 21st tile: waits for the accumulator",
+        61: "FP4: epilogue warp 4, its 21st tile: accumulator ready",
+        62: "FP4: epilogue warp 4, its 21st tile: heads folded",
+        63: "FP4: epilogue warp 4, its 21st tile: scores stored, histogram added, released",
     }),
     "top-k (topk2_kernel)": (48, 49, 56, 55, {
         50: "histogram read, cluster barrier passed",
