@@ -392,15 +392,14 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           const uint32_t buf = iacc % a.nbuf, aph = (iacc / a.nbuf) & 1;
           ++iacc;
           if (!mine) continue;
-          const bool traced = ew == 0 && lane == 0 && iacc == 41;
-          if (traced) CSA_TRACE_MARK(60);
+          if (ew == 0 && lane == 0 && iacc == 41) CSA_TRACE_MARK(60);   // traced tile
           if (!mbar_wait(acc_full + buf, aph, abort_flag)) { ok = false; break; }
-          if (traced) CSA_TRACE_MARK(61);
+          if (ew == 0 && lane == 0 && iacc == 41) CSA_TRACE_MARK(61);
           tc_fence_after();
           const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + buf * (uint32_t)NQH;
           for (int qi = 0; qi < x.nq; ++qi) {
             const float acc = fold_heads<H>(tbase + qi * H, ws + qi * H);
-            if (traced) CSA_TRACE_MARK(62);
+            if (ew == 0 && lane == 0 && iacc == 41) CSA_TRACE_MARK(62);
             const int vis = item_vis(a, x, qi);
             if (s < a.N) store_score(a.scores, a.scores_bf16, srow + (size_t)qi * a.N, s < vis ? acc : -INFINITY);
             if (a.hist) hist_add(wh, stored_score(a.scores_bf16, acc), s < vis);
@@ -408,7 +407,7 @@ index_fp4_kernel(const __grid_constant__ CUtensorMap tm_K, const __grid_constant
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + buf);
-          if (traced) CSA_TRACE_MARK(63);
+          if (ew == 0 && lane == 0 && iacc == 41) CSA_TRACE_MARK(63);
           if (ew == 0 && lane == 0) CSA_TRACE_MARK(iacc <= 2 ? 38 : 39);
         } else if ((j & 1) == grp) {
           for (int qi = 0; qi < x.nq; ++qi)
