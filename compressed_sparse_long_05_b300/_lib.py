@@ -107,6 +107,9 @@ _SIGS = {
     "csa_index_paged": [_P, _P, _P, _P, _P, ctypes.POINTER(Pages), _P, _P, _I] + [_I] * 7 + [_P],
     "csa_index_topk_paged": [_P, _P, _P, _P, _P, ctypes.POINTER(Pages), _P, _P, _I, _P] + [_I] * 8
                             + [_P, _Z, _P],
+    "csa_decode_step_host": [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(Pages), KV, KV, _P, _P]
+                            + [_I] * 12 + [_F, _P, _Z, _P],
+    "csa_decode_step_workspace_size": [_I] * 13,
     "csa_block_pool_create": [ctypes.c_int32],
     "csa_block_pool_destroy": [_P],
     "csa_block_pool_free_count": [_P],
@@ -117,7 +120,7 @@ _SIGS = {
     "csa_last_cuda_error": [],
     "csa_version": [],
 }
-_RESTYPES = {"csa_block_pool_create": _P, "csa_block_pool_destroy": None,
+_RESTYPES = {"csa_decode_step_workspace_size": _Z, "csa_block_pool_create": _P, "csa_block_pool_destroy": None,
              "csa_block_pool_free_count": ctypes.c_int32, "csa_attend_workspace_size": _Z, "csa_index_topk_workspace_size": _Z, "csa_status_string": ctypes.c_char_p,
              "csa_last_cuda_error": ctypes.c_char_p}
 
@@ -446,3 +449,72 @@ class BlockPool:
             self.close()
         except Exception:
             pass
+
+
+class DecodeStepHost:
+    """One CSA decode step through the C ABI from host buffers
+    (csa_decode_step_host): the step's inputs are copied from pinned host
+    tensors, the index, top-k and attention run against the device-resident
+    cache, and the output lands in a pinned host tensor.
+
+    ``cache``: device tensors or :class:`Paged` views as :func:`csa_attend`
+    takes them (``entries``, ``win``, ``K`` with ``K_sf`` for FP4 keys) plus
+    ``sink``; ``B`` sequences, ``k``, ``m``, ``n_win``, ``r`` as the layer's.
+    ``host`` holds pinned tensors ``q`` [B,1,n_h,d] bf16, ``qI`` (or ``qI_fp4``
+    and ``qI_sf``), ``w``, ``q_pos`` [B] int32 and ``win_base`` [B] int32; the
+    caller refreshes them in place between steps.  ``__call__`` queues one step
+    on the current stream, waits for it and returns the pinned output.  With
+    ``graph=True`` the call is captured once into a CUDA graph (it only queues
+    asynchronous work, so the copies from the same pinned buffers, the kernels
+    and the copy back replay as they were queued) and each step replays it.
+    """
+
+    def __init__(self, cache, host, k, m, n_win, r, rope_base=10000.0, graph=False):
+        self.cache, self.host = cache, host
+        self.k, self.m, self.n_win, self.r, self.rope_base = k, m, n_win, r, rope_base
+        q = host["q"]
+        self.B, _, self.n_h, self.d = q.shape
+        qI = host.get("qI", host.get("qI_fp4"))
+        self.fp4 = "qI_fp4" in host
+        self.H = qI.shape[2]
+        self.c = qI.shape[3] * (2 if self.fp4 else 1)
+        self.Kt, self.kpg, self.N = _keys(cache["K"])
+        self.T_win = _rows_shape(cache["win"])[1]
+        self.dt = DT_E2M1_BLOCK16 if self.fp4 else DT_BF16
+        self.ent_kv, self.win_kv = _kv(cache["entries"]), _kv(cache["win"])
+        nbytes = lib().csa_decode_step_workspace_size(self.B, self.N, self.H, self.c, k, self.T_win,
+                                                      self.n_h, self.d, r, m, n_win, self.dt,
+                                                      self.ent_kv.dtype)
+        if nbytes == 0:
+            raise CsaError("csa_decode_step_workspace_size", 1)
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device if q.is_cuda else "cuda")
+        self.out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for n, t in host.items()
+                             if n in ("q", "qI", "qI_fp4", "qI_sf", "w", "q_pos", "win_base"))
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+        self.graph = None
+        if graph:
+            self._queue()                          # sets kernel attributes, caches the plans
+            torch.cuda.current_stream().synchronize()
+            self.graph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            with torch.cuda.graph(self.graph, stream=side, capture_error_mode="relaxed"):
+                self._queue()
+
+    def __call__(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self._queue()
+        torch.cuda.current_stream().synchronize()
+        return self.out
+
+    def _queue(self):
+        h = self.host
+        st = _stream()
+        _check("csa_decode_step_host", lib().csa_decode_step_host(
+            _p(h["q"]), _p(h["qI_fp4"] if self.fp4 else h["qI"]), _p(h.get("qI_sf")), _p(h["w"]),
+            _p(h["q_pos"]), _p(h.get("win_base")), _p(self.Kt), _p(self.cache.get("K_sf")), self.kpg,
+            self.ent_kv, self.win_kv, _p(self.cache["sink"]), _p(self.out), self.B, self.N, self.H,
+            self.c, self.k, self.T_win, self.n_h, self.d, self.r, self.m, self.n_win, self.dt,
+            self.rope_base, _p(self.ws), self.ws.numel(), st))

@@ -1077,6 +1077,99 @@ size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// csa_decode_step_host: one decode step from host buffers.  Scratch layout:
+// staged inputs, float32 scores, indices, device output, the top-k histograms
+// (zero between calls), the attention's scratch; every part 256-byte aligned.
+struct StepLayout {
+  size_t q, qi, qisf, w, qpos, wb, scores, idx, out, hist, nhist, att, natt, bytes;
+};
+
+static bool step_layout(int B, int N, int H, int c, int k, int T_win, int n_h, int d, int r, int m,
+                        int n_win, int dtype, int kv_dtype, StepLayout* L) {
+  if (B <= 0 || N <= 0 || H <= 0 || c <= 0 || (c & 15) || k < 1 || k > 4096 || T_win < 0 ||
+      n_h <= 0 || d <= 0 || m <= 0 || n_win <= 0)
+    return false;
+  if (dtype != CSA_DT_BF16 && dtype != CSA_DT_E2M1_BLOCK16) return false;
+  if (kv_dtype != CSA_DT_BF16 && kv_dtype != CSA_DT_E4M3_BF16ROPE) return false;
+  const bool fp4 = dtype == CSA_DT_E2M1_BLOCK16;
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t o = off;
+    off = align256(off + n);
+    return o;
+  };
+  L->q = take((size_t)B * n_h * d * 2);
+  L->qi = take((size_t)B * H * (fp4 ? c / 2 : c * 2));
+  L->qisf = take(fp4 ? (size_t)B * H * (c / 16) : 0);
+  L->w = take((size_t)B * H * 4);
+  L->qpos = take((size_t)B * 4);
+  L->wb = take((size_t)B * 4);
+  L->scores = take((size_t)B * N * 4);
+  L->idx = take((size_t)B * k * 4);
+  L->out = take((size_t)B * n_h * d * 2);
+  L->nhist = csa_index_topk_workspace_size(B, 1, N, dtype);
+  L->hist = take(L->nhist);
+  L->natt = csa_attend_workspace_size(B, 1, N, k, T_win, n_h, d, r, m, n_win, CSA_DT_BF16, kv_dtype, 0);
+  L->att = take(L->natt);
+  L->bytes = off;
+  return true;
+}
+
+size_t csa_decode_step_workspace_size(int B, int N, int H, int c, int k, int T_win, int n_h, int d,
+                                      int r, int m, int n_win, int dtype, int kv_dtype) {
+  StepLayout L;
+  return step_layout(B, N, H, c, k, T_win, n_h, d, r, m, n_win, dtype, kv_dtype, &L) ? L.bytes : 0;
+}
+
+csa_status_t csa_decode_step_host(const void* q_h, const void* qI_h, const void* qI_sf_h,
+                                  const float* w_h, const int32_t* q_pos_h,
+                                  const int32_t* win_base_h, const void* K, const void* K_sf,
+                                  const csa_pages_t* K_pages, csa_kv_t entries, csa_kv_t win,
+                                  const float* sink, void* out_h, int B, int N, int H, int c, int k,
+                                  int T_win, int n_h, int d, int r, int m, int n_win, int dtype,
+                                  float rope_base, void* ws, size_t ws_bytes, void* stream) {
+  StepLayout L;
+  if (!step_layout(B, N, H, c, k, T_win, n_h, d, r, m, n_win, dtype, entries.dtype, &L))
+    return CSA_ERR_INVALID_ARG;
+  const bool fp4 = dtype == CSA_DT_E2M1_BLOCK16;
+  if (!q_h || !qI_h || !w_h || !q_pos_h || !out_h || !sink || !K || (fp4 && (!qI_sf_h || !K_sf)))
+    return CSA_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < L.bytes || !aligned(ws, 256)) return CSA_ERR_WORKSPACE;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  cudaStream_t st = S(stream);
+  // the step's new inputs, host -> device
+  const struct { size_t off; const void* src; size_t n; } in[] = {
+      {L.q, q_h, (size_t)B * n_h * d * 2},
+      {L.qi, qI_h, (size_t)B * H * (fp4 ? c / 2 : c * 2)},
+      {L.qisf, fp4 ? qI_sf_h : nullptr, fp4 ? (size_t)B * H * (c / 16) : 0},
+      {L.w, w_h, (size_t)B * H * 4},
+      {L.qpos, q_pos_h, (size_t)B * 4},
+      {L.wb, win_base_h, win_base_h ? (size_t)B * 4 : 0},
+  };
+  for (const auto& e : in) {
+    if (!e.n) continue;
+    const cudaError_t ce = cudaMemcpyAsync(wsb + e.off, e.src, e.n, cudaMemcpyHostToDevice, st);
+    if (ce != cudaSuccess) return cuda_fail(ce, "csa_decode_step_host copy in");
+  }
+  const int32_t* qpos = reinterpret_cast<const int32_t*>(wsb + L.qpos);
+  int32_t* idx = reinterpret_cast<int32_t*>(wsb + L.idx);
+  csa_status_t s = csa_index_topk_paged(
+      wsb + L.qi, fp4 ? wsb + L.qisf : nullptr, reinterpret_cast<const float*>(wsb + L.w), K,
+      fp4 ? K_sf : nullptr, K_pages, qpos, wsb + L.scores, CSA_DT_F32, idx, B, 1, N, H, c, m, k, dtype,
+      L.nhist ? wsb + L.hist : nullptr, L.nhist, stream);
+  if (s != CSA_OK) return s;
+  s = csa_attend(wsb + L.q, entries, idx, win, qpos,
+                 win_base_h ? reinterpret_cast<const int32_t*>(wsb + L.wb) : nullptr, sink, wsb + L.out,
+                 B, 1, N, k, T_win, n_h, d, r, m, n_win, rope_base, L.natt ? wsb + L.att : nullptr,
+                 L.natt, stream);
+  if (s != CSA_OK) return s;
+  const cudaError_t ce =
+      cudaMemcpyAsync(out_h, wsb + L.out, (size_t)B * n_h * d * 2, cudaMemcpyDeviceToHost, st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "csa_decode_step_host copy out");
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------------------
 // csa_attend_noalloc: csa_attend for callers that cannot allocate device
 // memory.  Its scratch is one fixed array in this library's device image.
 // ---------------------------------------------------------------------------

@@ -314,6 +314,40 @@ size_t csa_attend_workspace_size(int B, int Tq, int N, int k, int T_win, int n_h
                                  int m, int n_win, int q_dtype, int kv_dtype, int is_hca);
 
 /* ---------------------------------------------------------------------------
+ * csa_decode_step_host — one CSA decode step of one layer from HOST buffers,
+ * all on `stream` in this order: the step's new inputs are copied host ->
+ * device (one cudaMemcpyAsync each), csa_index_topk_paged and csa_attend run on
+ * them against the device-resident cache, and the output is copied device ->
+ * host.  The call returns once the work is queued: synchronise the stream
+ * before reading `out_h`.  Host buffers should be pinned for the copies to
+ * overlap; the pages define no such call (it is the boundary a serving loop
+ * with host-side inputs uses).
+ *   HOST: q_h [B, 1, n_h, d] bf16; qI_h [B, 1, H, c] bf16 (E2M1_BLOCK16: bytes
+ *         [B, 1, H, c/2] with qI_sf_h [B, 1, H, c/16]); w_h [B, 1, H] float32;
+ *         q_pos_h [B] int32 (each sequence's new token); win_base_h [B] int32
+ *         (NULL = 0); out_h [B, 1, n_h, d] bf16.
+ *   DEVICE (caller-owned, persistent): K, K_sf, K_pages (HOST pointer to the
+ *         row map, NULL = flat) as in csa_index_topk_paged; entries, win as in
+ *         csa_attend; sink [n_h] float32.
+ *   ws / ws_bytes: device scratch of csa_decode_step_workspace_size(...)
+ *         bytes, 256-byte aligned, ZERO-FILLED before its first use (it holds
+ *         csa_index_topk's histograms, which every successful call leaves
+ *         zero); the staged inputs, scores (float32), indices and the device
+ *         output live there too.
+ *   dtype: indexer dtype (BF16 or E2M1_BLOCK16); entries / win dtype as in
+ *   csa_attend (BF16 or E4M3_BF16ROPE).
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_decode_step_host(const void* q_h, const void* qI_h, const void* qI_sf_h,
+                                  const float* w_h, const int32_t* q_pos_h,
+                                  const int32_t* win_base_h, const void* K, const void* K_sf,
+                                  const csa_pages_t* K_pages, csa_kv_t entries, csa_kv_t win,
+                                  const float* sink, void* out_h, int B, int N, int H, int c, int k,
+                                  int T_win, int n_h, int d, int r, int m, int n_win, int dtype,
+                                  float rope_base, void* ws, size_t ws_bytes, void* stream);
+size_t csa_decode_step_workspace_size(int B, int N, int H, int c, int k, int T_win, int n_h,
+                                      int d, int r, int m, int n_win, int dtype, int kv_dtype);
+
+/* ---------------------------------------------------------------------------
  * csa_attend_noalloc — csa_attend without a caller-supplied workspace.  The
  * pages define no such call; it exists for callers that cannot allocate
  * device memory: code embedded in a host application or serving engine that

@@ -171,3 +171,23 @@ def test_block_pool():
     lib().csa_block_pool_create.restype = ctypes.c_void_p
     assert lib().csa_block_pool_create(0) is None
     assert lib().csa_block_pool_create((1 << 30) + 1) is None
+
+
+def test_decode_step_host_arguments(L):
+    # host-side checks of the host-buffer decode step (no device is touched)
+    from compressed_sparse_long_05_b300._lib import KV
+    L.csa_decode_step_workspace_size.restype = ctypes.c_size_t
+    args = (4, 32768, 64, 128, 1024, 128, 128, 512, 64, 4, 128)
+    n = L.csa_decode_step_workspace_size(*args, 1, 1)
+    # at least the staged queries, the float32 scores, the indices and the device output
+    assert n >= 4 * 128 * 512 * 2 * 2 + 4 * 32768 * 4 + 4 * 1024 * 4
+    assert L.csa_decode_step_workspace_size(*args, 0, 1) == 0        # float32 keys: not a decode format
+    assert L.csa_decode_step_workspace_size(0, *args[1:], 1, 1) == 0
+    fake = _p(0x10000)
+    kv = KV(dtype=1, flags=0, data=0x10000)
+    call = lambda q, ws, nbytes: L.csa_decode_step_host(
+        q, fake, None, fake, fake, None, fake, None, None, kv, kv, fake, fake, *args[:4], 1024, 128,
+        128, 512, 64, 4, 128, 1, ctypes.c_float(1e4), ws, ctypes.c_size_t(nbytes), None)
+    assert call(None, None, 0) == 1                    # no host queries
+    assert call(fake, None, 0) == 3                    # no workspace
+    assert call(fake, _p(0x10100), 16) == 3            # workspace too small
