@@ -406,6 +406,10 @@ def gpu_arm(args, cfg, rank, world, with_e2e=True):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with clocks, torch.cuda.stream(stream):
+        # keep the GPU busy while the host queues the timed steps, so that the
+        # host's launch latency of the first graph replays is not timed as idle
+        # device time (a short run of 20 steps would otherwise carry it)
+        torch.cuda._sleep(4_000_000)
         e0.record()
         run_steps(args.steps)
         e1.record()
