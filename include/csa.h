@@ -19,8 +19,10 @@
  *   - Argument, shape and alignment errors are returned before any launch.
  *     CSA_ERR_CUDA means a launch or runtime call failed (cudaGetLastError
  *     text via csa_last_cuda_error()).  Faults found on the device (a bounded
- *     wait that gave up, an out-of-range index) set a sticky device error word
- *     that csa_device_error() reads.
+ *     wait that gave up, an out-of-range index, a negative position, a window
+ *     token outside its buffer, a block-table entry outside its pool, a
+ *     histogram that disagrees with its scores) set a sticky device error
+ *     word that csa_device_error() reads; the offending rows are left out.
  *   - Query positions: q_pos is a DEVICE array int32 [B, Tq]; q_pos[b,i] is
  *     the absolute token position t of query row i of batch row b, so every
  *     sequence of a batch may sit at its own context length (§2.3.1: the
