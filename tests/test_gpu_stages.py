@@ -109,6 +109,7 @@ def _check_topk(scores, idx, k, m, q_pos0):
     (1, 64, 2048, 100, 8000, 7),     # ties from few distinct values
     (4, 1, 32768, 1024, 131071, 0),  # decode rows, cluster of 16 CTAs
     (3, 2, 40000, 1024, 159990, 3),  # several rows, ties, ragged slices
+    (1, 1, 40000, 4096, 159999, 3),  # the keys equal to the k-th span three ranks' slices
     (1, 40, 9000, 4096, 35990, 0),   # large k
     (2, 3, 20000, 7, 79999, 1),      # every score equal: lowest indices win
     (2, 1, 262144, 1024, 1048575, 0),   # 1M-context decode rows: 16-CTA clusters
@@ -385,7 +386,7 @@ def test_attend_mixed_rows(K, B, Tq, N, k, split):
 
 
 @pytest.mark.parametrize("fmt,B,N,k", [
-    ("bf16", 3, 32768, 1024),       # 128K-context decode rows, one CTA per row
+    ("bf16", 3, 32768, 1024),       # 128K-context decode rows over a 16-CTA cluster
     ("bf16", 2, 700, 1024),         # every visible entry selected (vis < k)
     ("bf16", 1, 5001, 333),         # odd N
     ("fp4", 2, 262144, 1024),       # 1M-context decode rows over an 8-CTA cluster
@@ -411,6 +412,23 @@ def test_index_topk_fused_matches_separate_calls(K, fmt, B, N, k):
     K.device_error()
     assert torch.equal(s, s_ref)
     assert torch.equal(i, i_ref)
+    _check_topk(s, i, k, m, q_pos0)
+
+
+def test_index_topk_every_score_equal(K):
+    # w = 0 makes every visible score 0: the first-digit bin the index kernel
+    # counted holds the whole row, every radix pass finds one digit, and the
+    # lowest indices win across the cluster's slices
+    m, H, c, k, B, N = 4, 64, 128, 1024, 2, 32768
+    q_pos0 = 4 * N - 1
+    w = torch.zeros((B, 1, H), device=DEV)
+    qI = _randn((B, 1, H, c), torch.bfloat16, 68, scale=c ** -0.5)
+    Kt = _randn((B, N, c), torch.bfloat16, 69, scale=c ** -0.5)
+    s, i, _ = K.csa_index_topk(qI, w, Kt, k, m, q_pos0)
+    torch.cuda.synchronize()
+    K.device_error()
+    assert int(s.count_nonzero()) == 0
+    assert torch.equal(i.cpu(), torch.arange(k, dtype=i.dtype).expand(B, 1, k))
     _check_topk(s, i, k, m, q_pos0)
 
 
