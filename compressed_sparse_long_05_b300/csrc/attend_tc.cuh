@@ -504,23 +504,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttSmem::MISC + 4);
   unsigned long long* ropeF = reinterpret_cast<unsigned long long*>(smem + AttSmem::ROPEF);
   if (threadIdx.x < 64) ropeF[threadIdx.x] = a.rf.F[threadIdx.x];
-  if (a.cl_reduce && threadIdx.x < ATT_HG) {
-    // the merge's sink logits, fetched now rather than on its critical path
-    // (parameters only: no grid dependency involved)
-    const int hg = (int)((blockIdx.x / a.nch) % a.HG);
-    reinterpret_cast<float*>(smem + AttSmem::SINK)[threadIdx.x] =
-        __ldg(a.sink + hg * ATT_HG + threadIdx.x) * 1.4426950408889634f;
-  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) { CSA_TRACE_WALL(0); CSA_TRACE_MARK(1); }
-  if (threadIdx.x == 32 && (int)blockIdx.x < a.items) {
-    // the first item's position and window base (read by every role's first item)
-    const int rest = (int)blockIdx.x / a.nch / a.HG;
-    const int qi = rest % a.Tq, qb = rest / a.Tq;
-    if (a.q_pos) prefetch_l1(a.q_pos + (size_t)qb * a.Tq + qi);
-    if (a.win_base) prefetch_l1(a.win_base + qb);
-  }
 
   if (threadIdx.x == 0) {
     for (int c = 0; c < 8; ++c) mbar_init(chunk_full + c, 4);
@@ -558,9 +544,19 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttendTcArgs a)
   // cluster merge: announce that this CTA runs (peers wait for it before their
   // first store into this CTA's shared memory)
   if (a.cl_reduce) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  pdl_enter();   // barriers and tensor memory are set up; inputs may still be in flight
+  // Barriers and tensor memory are set up; the previous kernel may still run
+  // (programmatic launch): no global memory is read before this wait.
+  pdl_enter();
   if (threadIdx.x == 0) CSA_TRACE_MARK(2);
   const uint32_t TM_O = 0, TM_S = 256;     // O^T blocks at 0..255, S^T buffers at 256..383
+  if (a.cl_reduce && threadIdx.x < ATT_HG) {
+    // the merge's sink logits, fetched now rather than on its critical path
+    // (softmax warps 0-1 have no S to read for microseconds yet); the barrier
+    // before the merge publishes them
+    const int hg = (int)((blockIdx.x / a.nch) % a.HG);
+    reinterpret_cast<float*>(smem + AttSmem::SINK)[threadIdx.x] =
+        __ldg(a.sink + hg * ATT_HG + threadIdx.x) * 1.4426950408889634f;
+  }
 
   if (warp >= 4 && warp < 8) {
     // ======================= gather warps =======================

@@ -83,7 +83,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 // early grids took the SMs the running one's clusters needed), and applied
 // only inside one layer forward (index -> top-k -> attention) the launch gaps
 // vanished but the early grids waited as long (63.4 vs 67.0 us per step).
+// Measured again on the current kernels: for the selector after the index
+// kernel still slower (decode 128K 46.9 -> 53.5 us); for the attention kernel
+// faster on short launches (HCA decode at 1M 30.15 -> 28.6 us, CSA decode at
+// 128K 46.69 -> 46.55 us) but slower on the persistent prefill launches
+// (CSA prefill 32K attention 22.25 -> 23.3 ms, HCA prefill 64K 21.9 -> 23.2
+// ms), so attention launches of at most kProgrammaticAttendItems work items
+// per CTA take it.
 constexpr bool kProgrammaticLaunch = false;
+constexpr int kProgrammaticAttendItems = 4;
 
 // As launch_ex, with programmatic serialisation against the previous kernel when `pdl`.
 template <typename... KArgs, typename... Args>
@@ -1008,8 +1016,9 @@ csa_status_t attend_launch(const AttendCall& c, const AttPlan& p, void* ws, void
     e = cudaFuncSetAttribute(csa::attend_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_fail(e, "csa_attend cluster attr");
   }
+  const bool pdl = p.items <= (long long)kProgrammaticAttendItems * sms;
   e = launch_ex_pdl(csa::attend_tc_kernel, dim3(grid), dim3(csa::ATT_THREADS), smem, st,
-                    p.cl_reduce ? p.ncs : 1, kProgrammaticLaunch, tmq, a);
+                    p.cl_reduce ? p.ncs : 1, pdl, tmq, a);
   if (e != cudaSuccess) return cuda_fail(e, "csa_attend tc launch");
   if (p.nch > 1 && (!p.cl_reduce || p.cl_partial)) {
     csa::CombineArgs ca;
