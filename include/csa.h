@@ -15,6 +15,12 @@
  *     except where a comment says otherwise.  The library never allocates,
  *     frees or synchronises in these calls; work is enqueued on `stream`
  *     (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *   - Stream order holds for every call.  The attention kernel of a short
+ *     csa_attend / hca_attend launch (at most 4 work items per CTA: decode)
+ *     is enqueued with programmatic stream serialisation: its CTAs may set
+ *     up barriers and tensor memory while the previous kernel on the stream
+ *     still runs, but they read and write no global memory before that
+ *     kernel has completed.
  *   - Tensors are dense and row-major in the shapes given (last dim fastest).
  *   - Argument, shape and alignment errors are returned before any launch.
  *     CSA_ERR_CUDA means a launch or runtime call failed (cudaGetLastError
